@@ -1,0 +1,351 @@
+"""Pins of the CPU oracle to facts fixed outside it (CPU only).
+
+Each test checks the oracle against something it does not itself compute:
+values printed on the pages (tests/golden/), numpy library routines on the
+special cases they cover, closed forms and invariants.  A plausible mistake
+in the oracle (dropped padding, swapped row/column, an offset applied after
+instead of before the bounds check, a transposed GEMM operand, a wrong
+rounding rule) fails at least one of them.
+"""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+import synth.workloads
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def read_golden(name):
+    out = {}
+    with open(os.path.join(GOLDEN, name)) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            k, v = (s.strip() for s in line.split("=", 1))
+            out[k] = [int(t) for t in v.split()]
+    return out
+
+
+def padded_reference(a, pad, margin):
+    """numpy's np.pad: the array surrounded by `margin` pad elements on every side."""
+    return np.pad(a, margin, mode="constant", constant_values=pad)
+
+
+# ----------------------------------------------------------------------------- generator
+
+def test_splitmix64_published_vector():
+    # SplitMix64 seeded with 0: the first three outputs of the reference generator
+    # (Steele, Lea & Flood 2014; the sequence used to seed xoshiro).
+    assert [synth.h(0, i) for i in range(3)] == [0xE220A8397B1DCDAF, 0x6E789E6AA1B965F4, 0x06C45D188009454F]
+
+
+def test_generator_distributions():
+    u = synth.uniform_f32(7, 100000, -1.0, 1.0)
+    assert u.min() >= -1.0 and u.max() < 1.0 and abs(u.mean()) < 0.01
+    z = synth.bf16_bits_to_f32(synth.normal_bf16(8, 200000)).astype(np.float64)
+    assert abs(z.mean()) < 0.01 and abs(z.std() - 1.0) < 0.01
+    k = synth.int_below(9, 100000, 82, lo=-1)
+    assert k.min() == -1 and k.max() == 80
+    p = synth.permutation_prefix(10, 1000, 1000)
+    assert sorted(p.tolist()) == list(range(1000))
+
+
+# ----------------------------------------------------------------------------- gather
+
+def test_gather_warp_example():
+    g = read_golden("warp_gather_even_rows.txt")
+    x = np.array(g["x"], np.float32).reshape(g["x_rows"][0], g["x_cols"][0])
+    idx = np.array(g["indices"], np.int32)
+    rows, cols = x.shape
+    out = oracle.gather_rows(x, rows, cols, cols, idx, tile_c=g["tile_shape"][1])
+    np.testing.assert_array_equal(out, np.array(g["expected"], np.float32).reshape(g["tile_shape"]))
+
+
+@pytest.mark.parametrize("bad", [-1, -2, np.iinfo(np.int32).min, 65, 66, np.iinfo(np.int32).max])
+def test_gather_sentinel_reads_pad(bad):
+    # warp.tile_load_indexed: a negative or past-the-end source index reads the padding value.
+    a = synth.uniform_f32(11, (65, 73), -1.0, 1.0)
+    idx = np.array([3, bad, 64], np.int32)
+    out = oracle.gather_rows(a, 65, 73, 73, idx, tile_c=73, pad=-1.0)
+    np.testing.assert_array_equal(out[0], a[3])
+    np.testing.assert_array_equal(out[1], np.full(73, -1.0, np.float32))
+    np.testing.assert_array_equal(out[2], a[64])
+
+
+def test_gather_offset_added_before_check_in_64bit():
+    a = synth.uniform_f32(12, (10, 8), -1.0, 1.0)
+    idx = np.array([np.iinfo(np.int32).max, -5, 2], np.int32)
+    out = oracle.gather_rows(a, 10, 8, 8, idx, tile_c=8, row_offset=5, pad=7.0)
+    # INT32_MAX + 5 overflows int32 but not int64: past the end -> pad.  -5 + 5 = row 0.
+    np.testing.assert_array_equal(out[0], np.full(8, 7.0, np.float32))
+    np.testing.assert_array_equal(out[1], a[0])
+    np.testing.assert_array_equal(out[2], a[7])
+    # An offset that needs more than 32 bits: truncating it would land on row 5.
+    out = oracle.gather_rows(a, 10, 8, 8, np.array([2], np.int32), tile_c=8, row_offset=2**32 + 3, pad=7.0)
+    np.testing.assert_array_equal(out[0], np.full(8, 7.0, np.float32))
+
+
+def test_gather_all_valid_equals_numpy_fancy_indexing():
+    a = synth.uniform_f32(13, (300, 50), -1.0, 1.0)
+    idx = synth.int_below(14, 97, 300).astype(np.int32)
+    out = oracle.gather_rows(a, 300, 50, 50, idx, tile_c=40, col_offset=6)
+    np.testing.assert_array_equal(out, a[idx][:, 6:46])
+
+
+def test_gather_general_equals_numpy_pad_and_clip():
+    # Out-of-range rows and columns, negative column offset, strided source, mask.
+    rows, cols, ld = 40, 30, 37
+    buf = synth.uniform_f32(15, (rows, ld), -1.0, 1.0)
+    idx = synth.int_below(16, 200, 60, lo=-10).astype(np.int32)
+    mask = synth.bernoulli_u8(17, (200, 45), 0.7)
+    pad = np.float32(-3.5)
+    for col_offset in (-7, 0, 5):
+        out = oracle.gather_rows(buf, rows, cols, ld, idx, tile_c=45, col_offset=col_offset, mask=mask,
+                                 pad=pad)
+        logical = buf[:, :cols]
+        big = padded_reference(logical, pad, 1)  # one pad row/column on each side
+        r = np.clip(idx.astype(np.int64), -1, rows) + 1
+        c = np.clip(np.arange(45) + col_offset, -1, cols) + 1
+        want = big[r][:, c]
+        want = np.where(mask != 0, want, pad)
+        np.testing.assert_array_equal(out, want)
+
+
+def test_gather_bf16_raw_bits_nan_negzero():
+    a = np.array([[0x7FC1, 0x8000, 0x3F80, 0xFF81]], np.uint16)  # NaN payload, -0.0, 1.0, -NaN
+    out = oracle.gather_rows(a, 1, 4, 4, np.array([0, -1], np.int32), tile_c=4, pad=0xBF80)
+    np.testing.assert_array_equal(out[0], a[0])
+    np.testing.assert_array_equal(out[1], np.full(4, 0xBF80, np.uint16))
+
+
+# ----------------------------------------------------------------------------- tile load / store
+
+def test_tile_load_tylo_concrete_edge():
+    g = read_golden("tylo_concrete_edge.txt")
+    M, K = g["a_shape"]
+    tr, tc = g["tile_shape"]
+    r0, c0 = g["origin"]
+    # bf16 values that are never zero, so "valid" == "nonzero"
+    a = (np.arange(M * K, dtype=np.uint32) % 0x3F00 + 0x0100).astype(np.uint16).reshape(M, K)
+    t = oracle.tile_load_padded(a, M, K, K, 1, r0, c0, 0, 0, 1, 1, tr, tc, pad=0)[0, 0]
+    nz_rows = np.nonzero(t.any(axis=1))[0]
+    nz_cols = np.nonzero(t.any(axis=0))[0]
+    assert nz_rows.size == g["valid_rows"][0] and nz_cols.size == g["valid_cols"][0]
+    assert np.count_nonzero(t) == g["valid_rows"][0] * g["valid_cols"][0]
+    np.testing.assert_array_equal(t[0, :9], a[64, 64:73])
+    v = g["vector_elems"][0]
+    # one full 16-byte vector of valid K values, then a vector with one valid element
+    assert np.count_nonzero(t[0, :v]) == v * g["full_vectors_in_valid_row"][0]
+    assert np.count_nonzero(t[0, v:2 * v]) == g["partial_vector_valid_elems"][0]
+    # the same tile as tile (1, 2) of the ceil-div grid of (64, 32) tiles over (65, 73)
+    gr, gc = -(-M // tr), -(-K // tc)
+    assert (gr, gc) == (2, 3)
+    grid = oracle.tile_load_padded(a, M, K, K, 1, 0, 0, tr, tc, gr, gc, tr, tc, pad=0)
+    np.testing.assert_array_equal(grid[1, 2], t)
+
+
+@pytest.mark.parametrize("origin", [(0, 0), (-5, -3), (3, 7), (-70, 2), (60, -40)])
+@pytest.mark.parametrize("stride_c", [1, 2])
+def test_tile_load_equals_numpy_pad_slice(origin, stride_c):
+    rows, cols = 65, 73
+    buf = synth.uniform_f32(21, (rows, cols * stride_c + 3), -1.0, 1.0)
+    ld = buf.shape[1]
+    logical = buf[:, : cols * stride_c : stride_c]
+    pad = np.float32(9.25)
+    tr, tc, sr, sc, gr, gc = 16, 8, 20, 12, 5, 8
+    tiles = oracle.tile_load_padded(buf, rows, cols, ld, stride_c, origin[0], origin[1], sr, sc, gr, gc, tr, tc,
+                                    pad=pad)
+    m = 200
+    big = padded_reference(logical, pad, m)
+    for ti in range(gr):
+        for tj in range(gc):
+            r, c = origin[0] + ti * sr + m, origin[1] + tj * sc + m
+            np.testing.assert_array_equal(tiles[ti, tj], big[r:r + tr, c:c + tc])
+
+
+def test_tile_load_valid_count_closed_form():
+    rows, cols = 37, 51
+    a = synth.uniform_f32(22, (rows, cols), 1.0, 2.0)  # no zero in the data
+    tr, tc = 16, 16
+    for r0, c0 in [(-9, -9), (30, 40), (0, 0), (-16, 10)]:
+        t = oracle.tile_load_padded(a, rows, cols, cols, 1, r0, c0, 0, 0, 1, 1, tr, tc, pad=0)[0, 0]
+        vr = max(0, min(r0 + tr, rows) - max(r0, 0))
+        vc = max(0, min(c0 + tc, cols) - max(c0, 0))
+        assert np.count_nonzero(t) == vr * vc
+
+
+def test_tile_grid_covers_array_once():
+    rows, cols = 65, 73
+    a = np.arange(rows * cols, dtype=np.int32).reshape(rows, cols)
+    gr, gc = -(-rows // 64), -(-cols // 32)
+    t = oracle.tile_load_padded(a, rows, cols, cols, 1, 0, 0, 64, 32, gr, gc, 64, 32, pad=-1)
+    vals = t[t >= 0]
+    assert vals.size == rows * cols and np.array_equal(np.sort(vals), np.arange(rows * cols))
+
+
+def test_tile_store_round_trip_and_clipping():
+    rows, cols = 65, 73
+    a = synth.uniform_f32(23, (rows, cols), -1.0, 1.0)
+    tr, tc = 64, 32
+    gr, gc = 2, 3
+    tiles = oracle.tile_load_padded(a, rows, cols, cols, 1, 0, 0, tr, tc, gr, gc, tr, tc, pad=5.0)
+    canary = np.array([synth.workloads.F32_CANARY_BITS], np.uint32).view(np.float32)[0]
+    canvas = np.full((70, 81), canary, np.float32)
+    view_off = 2 * 81 + 3
+    flat = canvas.reshape(-1)
+    sub = flat[view_off:]
+    oracle.tile_store_clipped(tiles, sub, rows, cols, 81, 1, 0, 0, tr, tc)
+    got = canvas[2:2 + rows, 3:3 + cols]
+    np.testing.assert_array_equal(got, a)
+    mask = np.ones(canvas.shape, bool)
+    mask[2:2 + rows, 3:3 + cols] = False
+    assert np.all(canvas.view(np.uint32)[mask] == synth.workloads.F32_CANARY_BITS)
+
+
+def test_tile_store_numpy_slice_assignment_with_negative_origin():
+    rows, cols = 30, 20
+    dst = np.zeros((rows, cols), np.float32)
+    tiles = synth.uniform_f32(24, (2, 2, 8, 8), 1.0, 2.0)
+    oracle.tile_store_clipped(tiles, dst, rows, cols, cols, 1, -4, 15, 26, 8)
+    want = np.zeros((rows + 100, cols + 100), np.float32)
+    m = 50
+    for ti in range(2):
+        for tj in range(2):
+            r, c = -4 + ti * 26 + m, 15 + tj * 8 + m
+            want[r:r + 8, c:c + 8] = tiles[ti, tj]
+    np.testing.assert_array_equal(dst, want[m:m + rows, m:m + cols])
+
+
+# ----------------------------------------------------------------------------- scatter
+
+def test_scatter_unique_equals_numpy_where():
+    rows, cols, n = 500, 40, 120
+    dst = synth.uniform_f32(31, (rows, cols), -1.0, 1.0)
+    before = dst.copy()
+    idx = synth.permutation_prefix(32, rows, n)
+    src = synth.uniform_f32(33, (n, cols), 5.0, 6.0)
+    mask = synth.bernoulli_u8(34, (n, cols), 0.9)
+    oracle.scatter_rows_masked(dst, rows, cols, cols, idx, src, cols, cols, mask=mask)
+    want = before.copy()
+    want[idx] = np.where(mask != 0, src, before[idx])
+    np.testing.assert_array_equal(dst, want)
+
+
+def test_scatter_out_of_bounds_rows_and_columns_clipped():
+    rows, cols = 10, 6
+    dst = np.zeros((rows, cols), np.float32)
+    idx = np.array([-1, 10, np.iinfo(np.int32).min, 4], np.int32)
+    src = np.arange(4 * 8, dtype=np.float32).reshape(4, 8) + 1
+    oracle.scatter_rows_masked(dst, rows, cols, cols, idx, src, 8, 8, col_offset=-1)
+    want = np.zeros((rows, cols), np.float32)
+    want[4, 0:6] = src[3, 1:7]
+    np.testing.assert_array_equal(dst, want)
+
+
+def test_scatter_duplicates_take_a_candidate():
+    rows, cols = 8, 4
+    dst = np.full((rows, cols), -1.0, np.float32)
+    idx = np.array([2, 2, 5, 2], np.int32)
+    src = synth.uniform_f32(35, (4, cols), 1.0, 2.0)
+    mask = synth.bernoulli_u8(36, (4, cols), 0.5)
+    oracle.scatter_rows_masked(dst, rows, cols, cols, idx, src, cols, cols, mask=mask)
+    for j in range(cols):
+        cands = {-1.0} | {float(src[k, j]) for k in (0, 1, 3) if mask[k, j]}
+        assert float(dst[2, j]) in cands
+
+
+# ----------------------------------------------------------------------------- ragged
+
+def test_ragged_equal_lengths_is_a_transpose():
+    B, T, H, D = 3, 20, 4, 16
+    x = synth.normal_bf16(41, (B * T, H, D))
+    cu = np.arange(B + 1, dtype=np.int32) * T
+    out = oracle.ragged_tile_load(x, B * T, H, D, H * D, D, cu, T)
+    np.testing.assert_array_equal(out, x.reshape(B, T, H, D).transpose(0, 2, 1, 3))
+
+
+def test_ragged_prefix_and_zero_rows():
+    d = synth.workloads.ragged_bf16(batch=6, max_len=50, heads=3, depth=8)
+    x, cu, lens = d["x"], d["cu_seqlens"], d["lens"]
+    t_pad = 40  # shorter than some sequences: rows >= t_pad are dropped
+    out = oracle.ragged_tile_load(x, d["total_rows"], 3, 8, 24, 8, cu, t_pad)
+    for b in range(6):
+        L = min(int(lens[b]), t_pad)
+        np.testing.assert_array_equal(out[b, :, :L], x[cu[b]:cu[b] + L].transpose(1, 0, 2))
+        assert not out[b, :, L:].any()
+
+
+def test_ragged_empty_and_out_of_range_metadata():
+    x = synth.normal_bf16(42, (10, 2, 4))
+    cu = np.array([0, 0, 8, 14], np.int32)  # empty sequence; the last one runs past total_rows=10
+    out = oracle.ragged_tile_load(x, 10, 2, 4, 8, 4, cu, 6)
+    assert not out[0].any()
+    np.testing.assert_array_equal(out[1], x[0:6].transpose(1, 0, 2))
+    np.testing.assert_array_equal(out[2, :, :2], x[8:10].transpose(1, 0, 2))
+    assert not out[2, :, 2:].any()
+
+
+# ----------------------------------------------------------------------------- GEMM and bf16 rounding
+
+def _bits_of(vals):
+    return (np.asarray(vals, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+
+
+@pytest.mark.parametrize("mnk", [(1, 1, 1), (3, 5, 7), (17, 13, 11), (16, 16, 64)])
+def test_gemm_integer_inputs_exact_vs_numpy_int_matmul(mnk):
+    M, N, K = mnk
+    a_int = synth.int_below(51, M * K, 5, lo=-2).reshape(M, K)
+    b_int = synth.int_below(52, K * N, 5, lo=-2).reshape(K, N)
+    lda, ldb = K + 1, N + 2
+    A = np.zeros((M, lda), np.uint16)
+    B = np.zeros((K, ldb), np.uint16)
+    A[:, :K] = _bits_of(a_int)
+    B[:, :N] = _bits_of(b_int)
+    C = oracle.gemm_f64(A, lda, B, ldb, M, N, K)
+    np.testing.assert_array_equal(C, (a_int @ b_int).astype(np.float64))
+
+
+def test_gemm_identity_and_random_vs_numpy():
+    M, N, K = 9, 14, 9
+    B = synth.normal_bf16(53, (K, N))
+    eye = np.zeros((M, K), np.uint16)
+    eye[np.arange(M), np.arange(M)] = 0x3F80
+    C = oracle.gemm_f64(eye, K, B, N, M, N, K)
+    np.testing.assert_array_equal(C, synth.bf16_bits_to_f32(B).astype(np.float64))
+    A = synth.normal_bf16(54, (21, 33))
+    B = synth.normal_bf16(55, (33, 12))
+    C = oracle.gemm_f64(A, 33, B, 12, 21, 12, 33)
+    want = synth.bf16_bits_to_f32(A).astype(np.float64) @ synth.bf16_bits_to_f32(B).astype(np.float64)
+    np.testing.assert_allclose(C, want, rtol=1e-12, atol=1e-12)
+    ms = np.array([0, 20, 7]); ns = np.array([11, 0, 5])
+    np.testing.assert_array_equal(oracle.gemm_f64_at(A, 33, B, 12, 33, ms, ns), C[ms, ns])
+
+
+@pytest.mark.parametrize("x,bits", [
+    (1.0, 0x3F80), (1.0 + 2**-8, 0x3F80), (1.0 + 3 * 2**-8, 0x3F82), (1.0 + 2**-8 + 2**-30, 0x3F81),
+    (-2.5, 0xC020), (0.0, 0x0000), (-0.0, 0x8000), (float("inf"), 0x7F80), (float("-inf"), 0xFF80),
+    (2**127 * (2 - 2**-7), 0x7F7F), (2**127 * (2 - 2**-8), 0x7F80), (2**127 * (2 - 2**-8) * (1 - 2**-40), 0x7F7F),
+    (2**-133, 0x0001), (2**-134, 0x0000), (1.5 * 2**-134, 0x0001), (3 * 2**-134, 0x0002), (2**-126, 0x0080),
+])
+def test_bf16_rne_pins(x, bits):
+    assert oracle.bf16_rne(x) == bits
+
+
+def test_bf16_rne_nan():
+    assert oracle.bf16_rne(float("nan")) & 0x7FC0 == 0x7FC0
+
+
+def test_bf16_rne_matches_torch_on_binary32_values():
+    # Values exactly representable in binary32 round identically through torch's
+    # float32 -> bfloat16 conversion (round to nearest even).
+    f = synth.normal_f32(56, 200000) * np.float32(1000.0)
+    f[:5] = [1.0 + 2**-8, 1.0 + 3 * 2**-8, -1.0 - 2**-8, 3.0e38, 1e-40]
+    want = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = oracle.round_bf16(f.astype(np.float64))
+    np.testing.assert_array_equal(got, want)
