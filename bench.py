@@ -1,0 +1,467 @@
+#!/usr/bin/env python3
+"""Benchmark of the bounds-checked tile-movement path on GB300.
+
+One step = one sbt_gather_rows launch over the row-gather workload (bf16
+table 1,000,000 x 512, 1,048,576 int32 indices of which 1 % are -1 and 0.5 %
+point past the end).  The JSON line's `value` is effective HBM GB/s over all
+ranks: algorithmic bytes (valid rows read + output written + indices) per
+step / device time per step.  `ops` adds the other operations at their own
+workloads (masked scatter, ragged load, tile load/store, bounded GEMM).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl sbt|reference]
+
+`--impl reference` times the CPU oracle (plain single-threaded C) on a
+bounded sample of the same workload; it is a slow baseline, not a target.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "effective HBM GB/s and % of GB300 peak per op; bounded-GEMM TFLOP/s"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+GATHER_WORKLOAD = ("row gather: bf16 table 1,000,000x512 N(0,1), 1,048,576 int32 indices uniform in [0,1e6) "
+                   "with 1% -1 and 0.5% >= 1e6 (read as 0.0), output 1,048,576x512 bf16")
+L2_NOTE = "inputs larger than L2 (1.02 GB table + 1.07 GB output per step > 129 MB L2); no flush needed"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="sbt", choices=["sbt", "reference"])
+    ap.add_argument("--no-ops", action="store_true", help="skip the per-operation extras")
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=8.0, help="CPU-baseline sample budget")
+    return ap.parse_args()
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+# ----------------------------------------------------------------------------- distributed plumbing
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+            import torch
+            backend = "nccl" if torch.cuda.is_available() else "gloo"
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        dev = "cuda" if self.pg.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def sum(self, x: float) -> float:
+        if not self.pg:
+            return x
+        import torch
+        dev = "cuda" if self.pg.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.SUM)
+        return float(t.item())
+
+    def close(self):
+        if self.pg:
+            self.pg.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi samples (every 100 ms) taken while the timed region runs."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.rows = []
+        self.proc = None
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "100",
+                 "-i", str(self.dev)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._reader = threading.Thread(target=self._read, daemon=True)
+            self._reader.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), line.strip()))
+
+    def mark(self, which: str):
+        setattr(self, which, time.time())
+
+    def stop(self):
+        if self.proc:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        parsed = []
+        for ts, line in self.rows:
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                parsed.append((ts, float(f[1]), float(f[2]), f[5:9]))
+            except ValueError:
+                continue
+        if not parsed:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no nvidia-smi samples"], "samples": 0}
+        inside = [p for p in parsed if self.t0 and self.t1 and self.t0 <= p[0] <= self.t1 + 0.1]
+        use = inside or sorted(parsed, key=lambda p: abs(p[0] - (self.t0 or p[0])))[:3]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for p in use for i, v in enumerate(p[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(p[1] for p in use), "sm_max_mhz": max(p[2] for p in use),
+                "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside)}
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def dev_bytes(a: np.ndarray):
+    import torch
+    flat = np.ascontiguousarray(a).reshape(-1).view(np.uint8)
+    return torch.from_numpy(flat).to("cuda")
+
+
+def time_launches(fn, reps: int, warmup: int = 3, flush=None):
+    """Median and mean device time (ms) of fn() over reps, CUDA events on the current stream."""
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(reps):
+        if flush is not None:
+            flush()
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        b.synchronize()
+        times.append(a.elapsed_time(b))
+    return statistics.median(times), statistics.fmean(times), min(times)
+
+
+def gather_bytes(idx: np.ndarray, n_rows: int, cols: int, es: int) -> int:
+    valid = int(np.count_nonzero((idx >= 0) & (idx < n_rows)))
+    return valid * cols * es + idx.size * cols * es + idx.size * 4
+
+
+def read_profile_traffic(name: str, source: str):
+    """dram read+write bytes per launch from a committed ncu summary, or None when the
+    kernel source changed since the counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", name)
+    try:
+        kv = {}
+        for line in open(path):
+            if ":" in line:
+                k, v = line.split(":", 1)
+                kv[k.strip()] = v.strip()
+        src = open(os.path.join(ROOT, "scatter_boundary_tile_gb300", "csrc", source), "rb").read()
+        if kv.get("kernel_source_sha256", "")[:16] != hashlib.sha256(src).hexdigest()[:16]:
+            return None
+        return int(kv["traffic_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) baseline
+
+def cpu_gather_sample(d, budget_s: float):
+    """Time the oracle's gather on a prefix of the index tile; returns (GB/s, rows, seconds)."""
+    import oracle
+    t, idx = d["table"], d["idx"]
+    n = 16384
+    while True:
+        t0 = time.perf_counter()
+        oracle.gather_rows(t, d["n_rows"], d["cols"], d["cols"], idx[:n], d["cols"])
+        dt = time.perf_counter() - t0
+        if dt > budget_s / 4 or n >= idx.size:
+            break
+        n = min(idx.size, int(n * max(2.0, (budget_s / 4) / max(dt, 1e-3))))
+    reps = max(1, int(budget_s / max(dt, 1e-3)))
+    reps = min(reps, 20)
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.gather_rows(t, d["n_rows"], d["cols"], d["cols"], idx[:n], d["cols"])
+    dt = (time.perf_counter() - t0) / reps
+    return gather_bytes(idx[:n], d["n_rows"], d["cols"], 2) / dt / 1e9, n, dt * reps
+
+
+# ----------------------------------------------------------------------------- extra operations
+
+def run_ops(ctx, pk):
+    import torch
+    import scatter_boundary_tile_gb300 as sbt
+    import synth.workloads as wl
+    ops = {}
+    hbm = pk["hbm_gbs"]
+
+    # masked scatter
+    d = wl.scatter_rows_f32()
+    rows, cols, n = d["dst_rows"], d["cols"], d["idx"].size
+    dst = torch.zeros(rows * cols * 4, dtype=torch.uint8, device="cuda")
+    s, i, m = dev_bytes(d["src"]), dev_bytes(d["idx"]), dev_bytes(d["mask"])
+    fn = lambda: sbt.scatter_rows_masked(ctx, dst, rows, cols, cols, i, n, s, cols, cols, mask=m, ld_mask=cols,
+                                         dtype="f32")
+    med, mean, best = time_launches(fn, 20)
+    nbytes = n * cols * 4 + n * cols + n * 4 + int(d["mask"].sum(dtype=np.int64)) * 4
+    ops["scatter_rows_masked"] = {"workload": "fp32 dst 4,194,304x256, 1,048,576 unique rows, Bernoulli(0.9) mask",
+                                  "ms": med, "GB/s": nbytes / med / 1e6, "frac_hbm": nbytes / med / 1e6 / hbm,
+                                  "algorithmic_bytes": nbytes}
+    del dst, s, i, m, d
+
+    # ragged 3D tile load
+    d = wl.ragged_bf16()
+    out = torch.empty(64 * 8 * 4096 * 128 * 2, dtype=torch.uint8, device="cuda")
+    x, cu = dev_bytes(d["x"]), dev_bytes(d["cu_seqlens"])
+    fn = lambda: sbt.ragged_tile_load(ctx, x, d["total_rows"], 8, 128, 1024, 128, cu, 64, 4096, out, dtype="bf16")
+    med, mean, best = time_launches(fn, 20)
+    nbytes = d["total_rows"] * 8 * 128 * 2 + out.numel() + 65 * 4
+    ops["ragged_tile_load"] = {"workload": "bf16 batch 64, len U[1,4096], 8 heads, depth 128 -> [64][8][4096][128]",
+                               "ms": med, "GB/s": nbytes / med / 1e6, "frac_hbm": nbytes / med / 1e6 / hbm,
+                               "algorithmic_bytes": nbytes}
+    del out, x, cu, d
+
+    # tile load / store over a 16381 x 16411 fp32 array, 64 x 32 tiles (aligned and unaligned rows)
+    import synth
+    for ld, tag in ((16416, "aligned_ld"), (16411, "unaligned_ld")):
+        r_, c_ = 16381, 16411
+        a = synth.uniform_f32(0x5B7101, (r_, ld), -1.0, 1.0)
+        gr, gc = -(-r_ // 64), -(-c_ // 32)
+        ad = dev_bytes(a)
+        tiles = torch.empty(gr * gc * 64 * 32 * 4, dtype=torch.uint8, device="cuda")
+        fn = lambda: sbt.tile_load_padded(ctx, ad, r_, c_, ld, 1, 0, 0, 64, 32, gr, gc, 64, 32, tiles, dtype="f32")
+        med, _, _ = time_launches(fn, 20)
+        nbytes = r_ * c_ * 4 + tiles.numel()
+        ops[f"tile_load_padded_{tag}"] = {"workload": f"fp32 16381x16411 ld {ld}, 64x32 tile grid {gr}x{gc}",
+                                          "ms": med, "GB/s": nbytes / med / 1e6, "frac_hbm": nbytes / med / 1e6 / hbm,
+                                          "algorithmic_bytes": nbytes}
+        fn = lambda: sbt.tile_store_clipped(ctx, tiles, gr, gc, 64, 32, ad, r_, c_, ld, 1, 0, 0, 64, 32, dtype="f32")
+        med, _, _ = time_launches(fn, 20)
+        nbytes = 2 * r_ * c_ * 4
+        ops[f"tile_store_clipped_{tag}"] = {"workload": f"fp32 16381x16411 ld {ld}, 64x32 tile grid {gr}x{gc}",
+                                            "ms": med, "GB/s": nbytes / med / 1e6,
+                                            "frac_hbm": nbytes / med / 1e6 / hbm, "algorithmic_bytes": nbytes}
+        del ad, tiles, a
+
+    # bounded GEMM
+    try:
+        for (M, N, K) in wl.GEMM_SHAPES:
+            g = wl.gemm_bf16(M=M, N=N, K=K)
+            A, B = dev_bytes(g["A"]), dev_bytes(g["B"])
+            C = torch.empty(M * g["ldc"] * 2, dtype=torch.uint8, device="cuda")
+            ws_n = sbt.gemm_bounded_workspace_size(ctx, M, N, K, g["lda"], g["ldb"])
+            ws = torch.empty(max(ws_n, 1), dtype=torch.uint8, device="cuda")
+            fn = lambda: sbt.gemm_bounded(ctx, A, g["lda"], B, g["ldb"], C, g["ldc"], M, N, K, ws, ws_n)
+            med, _, _ = time_launches(fn, 10 if M > 4000 else 30)
+            tf = 2.0 * M * N * K / med / 1e9
+            ops[f"gemm_bounded_{M}x{N}x{K}"] = {"ms": med, "TFLOP/s": tf, "frac_bf16": tf / pk["bf16_tflops"]}
+            del A, B, C, ws
+    except Exception as e:  # the GEMM may be unavailable in this build
+        ops["gemm_bounded"] = {"unavailable": str(e).splitlines()[0][:200]}
+    return ops
+
+
+# ----------------------------------------------------------------------------- arms
+
+def run_reference(args, dist):
+    if dist.rank != 0:
+        return 0
+    import multiprocessing
+    import synth.workloads as wl
+    d = wl.gather_rows_bf16()
+    n = 65536  # each step: the oracle on a 65,536-index prefix of the workload
+    import oracle
+    for _ in range(min(args.warmup, 3)):
+        oracle.gather_rows(d["table"], d["n_rows"], d["cols"], d["cols"], d["idx"][:n], d["cols"])
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        oracle.gather_rows(d["table"], d["n_rows"], d["cols"], d["cols"], d["idx"][:n], d["cols"])
+        times.append(time.perf_counter() - t0)
+        if sum(times) > 120:
+            break
+    dt = statistics.fmean(times)
+    gbs = gather_bytes(d["idx"][:n], d["n_rows"], d["cols"], 2) / dt / 1e9
+    sample = f"oracle gather of the first {n} of 1,048,576 indices per step ({len(times)} steps)"
+    line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": len(times), "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": GATHER_WORKLOAD, "l2": "CPU run"},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample,
+                             "host_cores_available": len(os.sched_getaffinity(0)),
+                             "cpu": multiprocessing.cpu_count()},
+            "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_sbt(args, dist):
+    import torch
+    import scatter_boundary_tile_gb300 as sbt
+    import synth.workloads as wl
+
+    torch.cuda.set_device(dist.local_rank)
+    pk, pk_src = peaks()
+    ctx = sbt.Context(dist.local_rank)
+
+    d = wl.gather_rows_bf16(seed=wl.SEED_GATHER + 1000 * dist.rank)  # each rank: its own batch (weak scaling)
+    table, idx = d["table"], d["idx"]
+    n, cols, n_rows = idx.size, d["cols"], d["n_rows"]
+    bytes_step = gather_bytes(idx, n_rows, cols, 2)
+    t_dev, i_dev = dev_bytes(table), dev_bytes(idx)
+    out = torch.empty(n * cols * 2, dtype=torch.uint8, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        sbt.gather_rows(ctx, t_dev, n_rows, cols, cols, i_dev, n, out, cols, cols, dtype="bf16")
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    ctx.check_status()
+
+    sampler = ClockSampler(torch.cuda.current_device())
+    sampler.start()
+    time.sleep(0.3)
+    dist.barrier()
+    torch.cuda.synchronize()
+    launches0 = ctx.launch_count
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler.mark("t0")
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    ev1.synchronize()
+    sampler.mark("t1")
+    torch.cuda.synchronize()
+    dist.barrier()
+    launches = ctx.launch_count - launches0
+    sampler.stop()
+    ms_total = ev0.elapsed_time(ev1)
+    ms_max = dist.max(ms_total)
+    total_bytes = dist.sum(float(bytes_step)) * args.steps
+    value = total_bytes / (ms_max / 1e3) / 1e9
+    ms_step = ms_max / args.steps
+    achieved = bytes_step / (ms_total / args.steps / 1e3) / 1e9  # this rank's kernel, per launch
+    ctx.check_status()
+
+    # end to end through host buffers: pinned table + indices in, gathered rows out
+    h_table = torch.from_numpy(np.ascontiguousarray(table).reshape(-1).view(np.uint8)).pin_memory()
+    h_idx = torch.from_numpy(np.ascontiguousarray(idx).reshape(-1).view(np.uint8)).pin_memory()
+    h_out = torch.empty(out.numel(), dtype=torch.uint8).pin_memory()
+
+    def e2e_step():
+        t_dev.copy_(h_table, non_blocking=True)
+        i_dev.copy_(h_idx, non_blocking=True)
+        step()
+        h_out.copy_(out, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    e1.synchronize()
+    e2e_ms = dist.max(e0.elapsed_time(e1)) / args.e2e_steps
+    e2e_value = dist.sum(float(bytes_step)) / (e2e_ms / 1e3) / 1e9
+    assert np.array_equal(h_out.numpy()[:cols * 2 * 64], out[:cols * 2 * 64].cpu().numpy())
+
+    traffic = read_profile_traffic("gather_rows_bf16_1Mx512.txt", "k_rows.cu")
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": dist.world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": GATHER_WORKLOAD, "l2": L2_NOTE, "parallelism": f"replicas x{dist.world}",
+                   "algorithmic_bytes_per_step": bytes_step,
+                   "note": "bf16 rows moved as raw 16-bit words; index arithmetic in int64"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / pk["hbm_gbs"], "traffic": traffic, "peak_source": pk_src,
+                     "kernel": "k_gather_rows<2,vector,no-mask>"},
+        "gpu_launches": launches,
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": h_table.numel() + h_idx.numel(),
+                "d2h_bytes_per_step": h_out.numel(), "ms_per_step": e2e_ms},
+        "clocks": sampler.summary(),
+    }
+    del h_table, h_out
+    if not args.no_ops:
+        del out, t_dev
+        torch.cuda.empty_cache()
+        line["ops"] = run_ops(ctx, pk)
+    if dist.rank == 0:
+        gbs, nrows, secs = cpu_gather_sample(d, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                "sample": f"oracle gather of the first {nrows} of {n} indices, {secs:.1f} s"}
+        print(json.dumps(line), flush=True)
+    ctx.close()
+    return 0
+
+
+def main():
+    args = parse()
+    if args.warmup < 3:
+        args.warmup = 3
+    dist = Dist()
+    try:
+        rc = run_reference(args, dist) if args.impl == "reference" else run_sbt(args, dist)
+    finally:
+        dist.close()
+    return rc
+
+
+if __name__ == "__main__":
+    sys.exit(main())

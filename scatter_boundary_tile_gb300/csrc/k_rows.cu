@@ -1,0 +1,393 @@
+// Row gather through an int32 index tile, and masked row scatter.
+//
+// Both kernels are persistent: the grid is (SMs x resident blocks), and each
+// block walks chunks of kChunkRows indices.  A chunk's indices are staged in
+// shared memory by one warp, which also checks every row against the array
+// bounds (64-bit, offset added first -- warp.tile_load_indexed, description)
+// and builds the chunk's row-valid mask with a warp ballot.  The block then
+// moves the chunk's rows with 16-byte vectors (when the host has checked that
+// every vector address is 16-byte aligned) or element by element.
+//
+// Per 16-byte vector the bounds decision follows the vector/scalar split of
+// Tylo.jl "Boundary tiles" (a vector wholly inside the array takes one
+// vector access; a partial vector goes element by element, and no pointer is
+// formed for an element outside the array).
+#include "sbt_internal.cuh"
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kChunkRows = 32;
+constexpr int kUnroll = 8;
+
+enum MaskMode { kNoMask = 0, kMaskVec = 1, kMaskBytes = 2 };
+
+struct RowParams {
+    const char* src;   // gather: table;  scatter: source rows
+    char* dst;         // gather: output; scatter: destination array
+    const int32_t* idx;
+    const uint8_t* mask;
+    int64_t rows, cols;        // bounds of the indexed array (table / destination)
+    int64_t ld_arr;            // row stride of the indexed array
+    int64_t ld_dense;          // row stride of the dense side (gather out / scatter src)
+    int64_t ld_mask;
+    int64_t n_idx, row_offset, col_offset;
+    int32_t tile_c;
+    int32_t nvec;              // tile_c / (16 / ES) on the vector path
+    uint32_t pad_word;
+};
+
+// Stage up to kChunkRows indices: s_row[i] = row_offset + idx[k0 + i], and a
+// ballot mask of the rows inside [0, rows).
+__device__ __forceinline__ uint32_t stage_index_chunk(const RowParams& p, int64_t k0, int nrows, int64_t* s_row,
+                                                      uint32_t* s_valid) {
+    if (threadIdx.x < 32) {
+        const int lane = threadIdx.x;
+        int64_t r = -1;
+        bool v = false;
+        if (lane < nrows) {
+            r = (int64_t)__ldg(p.idx + k0 + lane) + p.row_offset;
+            v = r >= 0 && r < p.rows;
+        }
+        const uint32_t ballot = __ballot_sync(0xffffffffu, v);
+        s_row[lane] = r;
+        if (lane == 0) *s_valid = ballot;
+    }
+    __syncthreads();
+    return *s_valid;
+}
+
+// Bit e set <=> mask element e of the vector starting at column j0 of row k is true.
+template <int ES, int MM>
+__device__ __forceinline__ uint32_t mask_bits(const RowParams& p, int64_t k, int64_t j0) {
+    constexpr int V = 16 / ES;
+    constexpr uint32_t kAll = (1u << V) - 1u;
+    if (MM == kNoMask) return kAll;
+    const uint8_t* m = p.mask + k * p.ld_mask + j0;
+    uint32_t bits = 0;
+    if (MM == kMaskVec) {
+        if (V == 8) {
+            const uint2 w = __ldg(reinterpret_cast<const uint2*>(m));
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                bits |= ((w.x >> (8 * e)) & 0xFFu) ? (1u << e) : 0u;
+                bits |= ((w.y >> (8 * e)) & 0xFFu) ? (1u << (e + 4)) : 0u;
+            }
+        } else {
+            const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(m));
+#pragma unroll
+            for (int e = 0; e < V; ++e) bits |= ((w >> (8 * e)) & 0xFFu) ? (1u << e) : 0u;
+        }
+    } else {
+#pragma unroll
+        for (int e = 0; e < V; ++e) bits |= __ldg(m + e) ? (1u << e) : 0u;
+    }
+    return bits;
+}
+
+template <int ES>
+__device__ __forceinline__ typename sbt_elem<ES>::T ld_elem(const char* base, int64_t off) {
+    return __ldg(reinterpret_cast<const typename sbt_elem<ES>::T*>(base) + off);
+}
+
+template <int ES>
+__device__ __forceinline__ void st_elem(char* base, int64_t off, typename sbt_elem<ES>::T v) {
+    reinterpret_cast<typename sbt_elem<ES>::T*>(base)[off] = v;
+}
+
+// ---------------------------------------------------------------------------- gather
+
+template <int ES, int MM>
+__device__ __forceinline__ uint4 gather_vector(const RowParams& p, int64_t k, int64_t r, bool row_ok, int vc) {
+    constexpr int V = 16 / ES;
+    constexpr uint32_t kAll = (1u << V) - 1u;
+    const uint4 padv = make_uint4(p.pad_word, p.pad_word, p.pad_word, p.pad_word);
+    if (!row_ok) return padv;
+    const int64_t j0 = (int64_t)vc * V;
+    const uint32_t mb = mask_bits<ES, MM>(p, k, j0);
+    if (mb == 0) return padv;
+    const int64_t c0 = p.col_offset + j0;
+    if (c0 >= 0 && c0 + V <= p.cols) {
+        uint4 v = sbt_ld_nc_v4(p.src + (r * p.ld_arr + c0) * ES);
+        if (mb != kAll) {
+#pragma unroll
+            for (int e = 0; e < V; ++e)
+                if (!((mb >> e) & 1u)) sbt_vec_set<ES>(v, e, (typename sbt_elem<ES>::T)p.pad_word);
+        }
+        return v;
+    }
+    if (c0 + V <= 0 || c0 >= p.cols) return padv;
+    uint4 v = padv;
+#pragma unroll
+    for (int e = 0; e < V; ++e) {
+        const int64_t c = c0 + e;
+        if (c >= 0 && c < p.cols && ((mb >> e) & 1u)) sbt_vec_set<ES>(v, e, ld_elem<ES>(p.src, r * p.ld_arr + c));
+    }
+    return v;
+}
+
+template <int ES, bool VEC, int MM>
+__global__ void __launch_bounds__(kThreads) k_gather_rows(const RowParams p) {
+    __shared__ int64_t s_row[kChunkRows];
+    __shared__ uint32_t s_valid;
+    constexpr int V = 16 / ES;
+    typedef typename sbt_elem<ES>::T T;
+    const int64_t nchunks = (p.n_idx + kChunkRows - 1) / kChunkRows;
+    for (int64_t chunk = blockIdx.x; chunk < nchunks; chunk += gridDim.x) {
+        const int64_t k0 = chunk * kChunkRows;
+        const int nrows = (int)(p.n_idx - k0 < kChunkRows ? p.n_idx - k0 : kChunkRows);
+        const uint32_t valid = stage_index_chunk(p, k0, nrows, s_row, &s_valid);
+        if (VEC) {
+            const int nvec = p.nvec;
+            const int ntask = nrows * nvec;
+            for (int base = threadIdx.x; base < ntask; base += kThreads * kUnroll) {
+                uint4 val[kUnroll];
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int t = base + u * kThreads;
+                    if (t < ntask) {
+                        const int row = t / nvec;
+                        const int vc = t - row * nvec;
+                        val[u] = gather_vector<ES, MM>(p, k0 + row, s_row[row], (valid >> row) & 1u, vc);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int t = base + u * kThreads;
+                    if (t < ntask) {
+                        const int row = t / nvec;
+                        const int vc = t - row * nvec;
+                        sbt_st_v4(p.dst + ((k0 + row) * p.ld_dense + (int64_t)vc * V) * ES, val[u]);
+                    }
+                }
+            }
+        } else {
+            const int tc = p.tile_c;
+            const int ntask = nrows * tc;
+            for (int base = threadIdx.x; base < ntask; base += kThreads * kUnroll) {
+                T val[kUnroll];
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int t = base + u * kThreads;
+                    val[u] = (T)p.pad_word;
+                    if (t < ntask) {
+                        const int row = t / tc;
+                        const int j = t - row * tc;
+                        const int64_t c = p.col_offset + j;
+                        const bool m = MM == kNoMask ? true : __ldg(p.mask + (k0 + row) * p.ld_mask + j) != 0;
+                        if (((valid >> row) & 1u) && m && c >= 0 && c < p.cols)
+                            val[u] = ld_elem<ES>(p.src, s_row[row] * p.ld_arr + c);
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int t = base + u * kThreads;
+                    if (t < ntask) {
+                        const int row = t / tc;
+                        const int j = t - row * tc;
+                        st_elem<ES>(p.dst, (k0 + row) * p.ld_dense + j, val[u]);
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// ---------------------------------------------------------------------------- scatter
+
+template <int ES, bool VEC, int MM>
+__global__ void __launch_bounds__(kThreads) k_scatter_rows(const RowParams p) {
+    __shared__ int64_t s_row[kChunkRows];
+    __shared__ uint32_t s_valid;
+    constexpr int V = 16 / ES;
+    constexpr uint32_t kAll = (1u << V) - 1u;
+    typedef typename sbt_elem<ES>::T T;
+    const int64_t nchunks = (p.n_idx + kChunkRows - 1) / kChunkRows;
+    for (int64_t chunk = blockIdx.x; chunk < nchunks; chunk += gridDim.x) {
+        const int64_t k0 = chunk * kChunkRows;
+        const int nrows = (int)(p.n_idx - k0 < kChunkRows ? p.n_idx - k0 : kChunkRows);
+        const uint32_t valid = stage_index_chunk(p, k0, nrows, s_row, &s_valid);
+        if (VEC) {
+            const int nvec = p.nvec;
+            const int ntask = nrows * nvec;
+            for (int base = threadIdx.x; base < ntask; base += kThreads * kUnroll) {
+                uint4 val[kUnroll];
+                uint32_t mb[kUnroll];
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int t = base + u * kThreads;
+                    mb[u] = 0;
+                    if (t < ntask) {
+                        const int row = t / nvec;
+                        const int vc = t - row * nvec;
+                        if ((valid >> row) & 1u) {
+                            const int64_t j0 = (int64_t)vc * V;
+                            const int64_t c0 = p.col_offset + j0;
+                            if (c0 + V > 0 && c0 < p.cols) {
+                                mb[u] = mask_bits<ES, MM>(p, k0 + row, j0);
+                                if (mb[u]) val[u] = sbt_ld_nc_v4(p.src + ((k0 + row) * p.ld_dense + j0) * ES);
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    if (!mb[u]) continue;
+                    const int t = base + u * kThreads;
+                    const int row = t / nvec;
+                    const int vc = t - row * nvec;
+                    const int64_t c0 = p.col_offset + (int64_t)vc * V;
+                    char* drow = p.dst + s_row[row] * p.ld_arr * ES;
+                    if (mb[u] == kAll && c0 >= 0 && c0 + V <= p.cols) {
+                        sbt_st_v4(drow + c0 * ES, val[u]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < V; ++e) {
+                            const int64_t c = c0 + e;
+                            if (((mb[u] >> e) & 1u) && c >= 0 && c < p.cols)
+                                st_elem<ES>(drow, c, sbt_vec_get<ES>(val[u], e));
+                        }
+                    }
+                }
+            }
+        } else {
+            const int tc = p.tile_c;
+            const int ntask = nrows * tc;
+            for (int base = threadIdx.x; base < ntask; base += kThreads * kUnroll) {
+                T val[kUnroll];
+                bool ok[kUnroll];
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    const int t = base + u * kThreads;
+                    ok[u] = false;
+                    if (t < ntask) {
+                        const int row = t / tc;
+                        const int j = t - row * tc;
+                        const int64_t c = p.col_offset + j;
+                        if (((valid >> row) & 1u) && c >= 0 && c < p.cols) {
+                            ok[u] = MM == kNoMask ? true : __ldg(p.mask + (k0 + row) * p.ld_mask + j) != 0;
+                            if (ok[u]) val[u] = ld_elem<ES>(p.src, (k0 + row) * p.ld_dense + j);
+                        }
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kUnroll; ++u) {
+                    if (!ok[u]) continue;
+                    const int t = base + u * kThreads;
+                    const int row = t / tc;
+                    const int j = t - row * tc;
+                    st_elem<ES>(p.dst, s_row[row] * p.ld_arr + p.col_offset + j, val[u]);
+                }
+            }
+        }
+        __syncthreads();
+    }
+}
+
+template <int ES, bool VEC, int MM>
+sbt_status launch_gather_t(sbt_context* ctx, const RowParams& p, cudaStream_t stream) {
+    auto kern = k_gather_rows<ES, VEC, MM>;
+    const int64_t nchunks = sbt_cdiv(p.n_idx, kChunkRows);
+    const int grid = sbt_persistent_grid(ctx, (const void*)kern, kThreads, 0, nchunks);
+    kern<<<grid, kThreads, 0, stream>>>(p);
+    return sbt_after_launch(ctx, "gather_rows");
+}
+
+template <int ES, bool VEC, int MM>
+sbt_status launch_scatter_t(sbt_context* ctx, const RowParams& p, cudaStream_t stream) {
+    auto kern = k_scatter_rows<ES, VEC, MM>;
+    const int64_t nchunks = sbt_cdiv(p.n_idx, kChunkRows);
+    const int grid = sbt_persistent_grid(ctx, (const void*)kern, kThreads, 0, nchunks);
+    kern<<<grid, kThreads, 0, stream>>>(p);
+    return sbt_after_launch(ctx, "scatter_rows_masked");
+}
+
+template <int ES>
+sbt_status dispatch_rows(sbt_context* ctx, bool gather, bool vec, int mm, const RowParams& p, cudaStream_t s) {
+#define SBT_ROWS_CASE(VEC_, MM_) \
+    return gather ? launch_gather_t<ES, VEC_, MM_>(ctx, p, s) : launch_scatter_t<ES, VEC_, MM_>(ctx, p, s)
+    if (vec) {
+        if (mm == kNoMask) SBT_ROWS_CASE(true, kNoMask);
+        if (mm == kMaskVec) SBT_ROWS_CASE(true, kMaskVec);
+        SBT_ROWS_CASE(true, kMaskBytes);
+    }
+    if (mm == kNoMask) SBT_ROWS_CASE(false, kNoMask);
+    SBT_ROWS_CASE(false, kMaskBytes);
+#undef SBT_ROWS_CASE
+}
+
+// The vector path needs every 16-byte vector of both sides aligned: the
+// indexed array at (row r, column col_offset + 16*v bytes) for every r, and
+// the dense side at (row k, 16*v bytes) for every k.
+bool rows_vector_ok(int es, const void* arr, int64_t ld_arr, int64_t col_offset, const void* dense,
+                    int64_t ld_dense, int32_t tile_c) {
+    const int V = 16 / es;
+    if (tile_c % V) return false;
+    if (!sbt_mul16(ld_arr, es) || !sbt_mul16(ld_dense, es) || !sbt_mul16(col_offset, es)) return false;
+    if (!sbt_aligned16(dense)) return false;
+    if (arr && !sbt_aligned16(arr)) return false;
+    return true;
+}
+
+int pick_mask_mode(int es, bool vec, const uint8_t* mask, int64_t ld_mask) {
+    if (!mask) return kNoMask;
+    const int V = 16 / es;
+    if (vec && (reinterpret_cast<uintptr_t>(mask) % V) == 0 && (ld_mask % V) == 0) return kMaskVec;
+    return kMaskBytes;
+}
+
+}  // namespace
+
+sbt_status sbt_launch_gather(sbt_context* ctx, int es, const void* src, int64_t rows, int64_t cols, int64_t ld_src,
+                             const int32_t* idx, int64_t n_idx, int64_t row_offset, int64_t col_offset,
+                             int32_t tile_c, const uint8_t* mask, int64_t ld_mask, void* out, int64_t ld_out,
+                             uint32_t pad_word, cudaStream_t stream) {
+    RowParams p;
+    p.src = (const char*)src;
+    p.dst = (char*)out;
+    p.idx = idx;
+    p.mask = mask;
+    p.rows = (src && cols > 0) ? rows : 0;  // an empty table makes every row invalid
+    p.cols = cols;
+    p.ld_arr = ld_src;
+    p.ld_dense = ld_out;
+    p.ld_mask = ld_mask;
+    p.n_idx = n_idx;
+    p.row_offset = row_offset;
+    p.col_offset = col_offset;
+    p.tile_c = tile_c;
+    p.pad_word = pad_word;
+    bool vec = rows_vector_ok(es, src, ld_src, col_offset, out, ld_out, tile_c);
+    if (ctx->path == SBT_PATH_SCALAR) vec = false;
+    p.nvec = vec ? tile_c / (16 / es) : 0;
+    const int mm = pick_mask_mode(es, vec, mask, ld_mask);
+    return es == 4 ? dispatch_rows<4>(ctx, true, vec, mm, p, stream) : dispatch_rows<2>(ctx, true, vec, mm, p, stream);
+}
+
+sbt_status sbt_launch_scatter(sbt_context* ctx, int es, void* dst, int64_t rows, int64_t cols, int64_t ld_dst,
+                              const int32_t* idx, int64_t n_idx, int64_t row_offset, int64_t col_offset,
+                              const void* src, int64_t ld_src, int32_t tile_c, const uint8_t* mask, int64_t ld_mask,
+                              cudaStream_t stream) {
+    RowParams p;
+    p.src = (const char*)src;
+    p.dst = (char*)dst;
+    p.idx = idx;
+    p.mask = mask;
+    p.rows = rows;
+    p.cols = cols;
+    p.ld_arr = ld_dst;
+    p.ld_dense = ld_src;
+    p.ld_mask = ld_mask;
+    p.n_idx = n_idx;
+    p.row_offset = row_offset;
+    p.col_offset = col_offset;
+    p.tile_c = tile_c;
+    p.pad_word = 0;
+    bool vec = rows_vector_ok(es, dst, ld_dst, col_offset, src, ld_src, tile_c);
+    if (ctx->path == SBT_PATH_SCALAR) vec = false;
+    p.nvec = vec ? tile_c / (16 / es) : 0;
+    const int mm = pick_mask_mode(es, vec, mask, ld_mask);
+    return es == 4 ? dispatch_rows<4>(ctx, false, vec, mm, p, stream)
+                   : dispatch_rows<2>(ctx, false, vec, mm, p, stream);
+}

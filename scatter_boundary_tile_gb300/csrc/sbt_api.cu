@@ -1,0 +1,285 @@
+// C ABI of libsbt.so: context, argument validation and dispatch.
+// Every check here runs before any launch; a failing call launches nothing.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <string>
+
+#include "sbt_internal.cuh"
+
+// Per-device status flag set by kernels whose bounded waits ran out.
+__device__ unsigned int g_sbt_status_flag;
+
+static thread_local std::string t_last_error;
+
+sbt_status sbt_fail(sbt_status st, const std::string& msg) {
+    t_last_error = msg;
+    return st;
+}
+
+sbt_status sbt_ok() { return SBT_OK; }
+
+sbt_status sbt_cuda_check(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return SBT_OK;
+    return sbt_fail(SBT_ERR_CUDA, std::string(what) + ": " + cudaGetErrorString(e));
+}
+
+sbt_status sbt_use_device(sbt_context* ctx) { return sbt_cuda_check(cudaSetDevice(ctx->device), "cudaSetDevice"); }
+
+uint32_t sbt_pad_word(const void* pad, int es) {
+    if (!pad) return 0u;
+    if (es == 4) {
+        uint32_t w;
+        memcpy(&w, pad, 4);
+        return w;
+    }
+    uint16_t h;
+    memcpy(&h, pad, 2);
+    return (uint32_t)h | ((uint32_t)h << 16);
+}
+
+int sbt_persistent_grid(const sbt_context* ctx, const void* kernel, int threads, size_t smem, int64_t work_units) {
+    int per_sm = 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess || per_sm < 1)
+        per_sm = 1;
+    int64_t g = (int64_t)ctx->sm_count * per_sm;
+    if (work_units < g) g = work_units;
+    return (int)(g < 1 ? 1 : g);
+}
+
+sbt_status sbt_after_launch(sbt_context* ctx, const char* what) {
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return sbt_fail(SBT_ERR_CUDA, std::string(what) + " launch: " + cudaGetErrorString(e));
+    ctx->launches++;
+    return SBT_OK;
+}
+
+#define SBT_REQUIRE(cond, msg)                                          \
+    do {                                                                \
+        if (!(cond)) return sbt_fail(SBT_ERR_INVALID_ARG, (msg));       \
+    } while (0)
+
+extern "C" {
+
+const char* sbt_last_error_message(void) { return t_last_error.c_str(); }
+
+sbt_status sbt_create(int device, sbt_context** out) {
+    if (!out) return sbt_fail(SBT_ERR_INVALID_ARG, "sbt_create: out is NULL");
+    *out = nullptr;
+    int n = 0;
+    sbt_status st = sbt_cuda_check(cudaGetDeviceCount(&n), "cudaGetDeviceCount");
+    if (st) return st;
+    if (device < 0 || device >= n) return sbt_fail(SBT_ERR_INVALID_ARG, "sbt_create: no such device");
+    if ((st = sbt_cuda_check(cudaSetDevice(device), "cudaSetDevice"))) return st;
+    sbt_context* c = new sbt_context();
+    c->device = device;
+    cudaDeviceProp prop;
+    if ((st = sbt_cuda_check(cudaGetDeviceProperties(&prop, device), "cudaGetDeviceProperties"))) {
+        delete c;
+        return st;
+    }
+    c->sm_count = prop.multiProcessorCount;
+    c->cc_major = prop.major;
+    c->cc_minor = prop.minor;
+    c->smem_optin = prop.sharedMemPerBlockOptin;
+    if (!(prop.major == 10 && prop.minor == 3)) {
+        delete c;
+        return sbt_fail(SBT_ERR_UNSUPPORTED, "sbt_create: libsbt is built for sm_103a (compute capability 10.3)");
+    }
+    void* flag = nullptr;
+    if ((st = sbt_cuda_check(cudaGetSymbolAddress(&flag, g_sbt_status_flag), "cudaGetSymbolAddress(status)"))) {
+        delete c;
+        return st;
+    }
+    c->status = (unsigned int*)flag;
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if ((st = sbt_cuda_check(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                                              cudaEnableDefault, &q),
+                             "cudaGetDriverEntryPointByVersion")) ||
+        q != cudaDriverEntryPointSuccess || !fn) {
+        delete c;
+        return st ? st : sbt_fail(SBT_ERR_CUDA, "cuTensorMapEncodeTiled entry point not found");
+    }
+    c->encode_tiled = (sbt_encode_tiled_fn)fn;
+    *out = c;
+    return SBT_OK;
+}
+
+sbt_status sbt_destroy(sbt_context* ctx) {
+    delete ctx;
+    return SBT_OK;
+}
+
+sbt_status sbt_set_path(sbt_context* ctx, sbt_path path) {
+    if (!ctx) return sbt_fail(SBT_ERR_INVALID_ARG, "ctx is NULL");
+    if (path < SBT_PATH_AUTO || path > SBT_PATH_TMA) return sbt_fail(SBT_ERR_INVALID_ARG, "unknown path");
+    ctx->path = path;
+    return SBT_OK;
+}
+
+sbt_status sbt_set_wait_limit_ns(sbt_context* ctx, uint64_t ns) {
+    if (!ctx) return sbt_fail(SBT_ERR_INVALID_ARG, "ctx is NULL");
+    if (ns == 0) return sbt_fail(SBT_ERR_INVALID_ARG, "wait limit must be positive");
+    ctx->wait_limit_ns = ns;
+    return SBT_OK;
+}
+
+uint64_t sbt_launch_count(const sbt_context* ctx) { return ctx ? ctx->launches : 0; }
+
+sbt_status sbt_check_status(sbt_context* ctx, void* stream) {
+    if (!ctx) return sbt_fail(SBT_ERR_INVALID_ARG, "ctx is NULL");
+    sbt_status st = sbt_use_device(ctx);
+    if (st) return st;
+    if ((st = sbt_cuda_check(cudaStreamSynchronize((cudaStream_t)stream), "cudaStreamSynchronize"))) return st;
+    unsigned int flag = 0, zero = 0;
+    if ((st = sbt_cuda_check(cudaMemcpy(&flag, ctx->status, 4, cudaMemcpyDeviceToHost), "read status"))) return st;
+    if (flag) {
+        if ((st = sbt_cuda_check(cudaMemcpy(ctx->status, &zero, 4, cudaMemcpyHostToDevice), "clear status")))
+            return st;
+        return sbt_fail(SBT_ERR_DEVICE_TIMEOUT, "a bounded device-side wait ran out (code " + std::to_string(flag) + ")");
+    }
+    return SBT_OK;
+}
+
+static sbt_status check_dtype_move(sbt_dtype dtype, int* es) {
+    *es = sbt_dtype_size(dtype);
+    if (*es != 2 && *es != 4) return sbt_fail(SBT_ERR_UNSUPPORTED, "unsupported dtype");
+    return SBT_OK;
+}
+
+sbt_status sbt_tile_load_padded(sbt_context* ctx, sbt_dtype dtype, const void* src, int64_t rows, int64_t cols,
+                                int64_t stride_r, int64_t stride_c, int64_t origin_r, int64_t origin_c,
+                                int64_t step_r, int64_t step_c, int32_t grid_r, int32_t grid_c, int32_t tile_r,
+                                int32_t tile_c, void* dst_tiles, const void* pad_value, void* stream) {
+    SBT_REQUIRE(ctx, "ctx is NULL");
+    int es;
+    sbt_status st = check_dtype_move(dtype, &es);
+    if (st) return st;
+    SBT_REQUIRE(rows >= 0 && cols >= 0, "tile_load_padded: negative extent");
+    SBT_REQUIRE(grid_r >= 0 && grid_c >= 0, "tile_load_padded: negative grid");
+    SBT_REQUIRE(tile_r >= 1 && tile_r <= 256 && tile_c >= 1 && tile_c <= 256, "tile_load_padded: tile dims must be in [1, 256]");
+    if ((int64_t)grid_r * grid_c == 0) return SBT_OK;
+    SBT_REQUIRE(dst_tiles, "tile_load_padded: dst_tiles is NULL");
+    SBT_REQUIRE(stride_r != 0 && stride_c != 0, "tile_load_padded: strides must be nonzero");
+    SBT_REQUIRE(rows * cols == 0 || src, "tile_load_padded: src is NULL");
+    if ((st = sbt_use_device(ctx))) return st;
+    return sbt_launch_tile_load(ctx, es, src, rows, cols, stride_r, stride_c, origin_r, origin_c, step_r, step_c,
+                                grid_r, grid_c, tile_r, tile_c, dst_tiles, sbt_pad_word(pad_value, es),
+                                (cudaStream_t)stream);
+}
+
+sbt_status sbt_tile_store_clipped(sbt_context* ctx, sbt_dtype dtype, const void* src_tiles, int32_t grid_r,
+                                  int32_t grid_c, int32_t tile_r, int32_t tile_c, void* dst, int64_t rows,
+                                  int64_t cols, int64_t stride_r, int64_t stride_c, int64_t origin_r,
+                                  int64_t origin_c, int64_t step_r, int64_t step_c, void* stream) {
+    SBT_REQUIRE(ctx, "ctx is NULL");
+    int es;
+    sbt_status st = check_dtype_move(dtype, &es);
+    if (st) return st;
+    SBT_REQUIRE(rows >= 0 && cols >= 0, "tile_store_clipped: negative extent");
+    SBT_REQUIRE(grid_r >= 0 && grid_c >= 0, "tile_store_clipped: negative grid");
+    SBT_REQUIRE(tile_r >= 1 && tile_r <= 256 && tile_c >= 1 && tile_c <= 256, "tile_store_clipped: tile dims must be in [1, 256]");
+    if ((int64_t)grid_r * grid_c == 0 || rows * cols == 0) return SBT_OK;
+    SBT_REQUIRE(src_tiles && dst, "tile_store_clipped: NULL pointer");
+    SBT_REQUIRE(stride_r != 0 && stride_c != 0, "tile_store_clipped: strides must be nonzero");
+    if ((st = sbt_use_device(ctx))) return st;
+    return sbt_launch_tile_store(ctx, es, src_tiles, grid_r, grid_c, tile_r, tile_c, dst, rows, cols, stride_r,
+                                 stride_c, origin_r, origin_c, step_r, step_c, (cudaStream_t)stream);
+}
+
+sbt_status sbt_gather_rows(sbt_context* ctx, sbt_dtype dtype, const void* src, int64_t rows, int64_t cols,
+                           int64_t ld_src, const int32_t* idx, int64_t n_idx, int64_t row_offset,
+                           int64_t col_offset, int32_t tile_c, const uint8_t* mask, int64_t ld_mask, void* out,
+                           int64_t ld_out, const void* pad_value, void* stream) {
+    SBT_REQUIRE(ctx, "ctx is NULL");
+    int es;
+    sbt_status st = check_dtype_move(dtype, &es);
+    if (st) return st;
+    SBT_REQUIRE(rows >= 0 && cols >= 0 && n_idx >= 0, "gather_rows: negative extent");
+    SBT_REQUIRE(tile_c >= 1 && tile_c <= 65536, "gather_rows: tile_c must be in [1, 65536]");
+    SBT_REQUIRE(ld_out >= tile_c, "gather_rows: ld_out < tile_c");
+    if (n_idx == 0) return SBT_OK;
+    SBT_REQUIRE(idx && out, "gather_rows: NULL idx or out");
+    SBT_REQUIRE(rows * cols == 0 || src, "gather_rows: src is NULL");
+    SBT_REQUIRE(rows * cols == 0 || ld_src >= cols, "gather_rows: ld_src < cols");
+    SBT_REQUIRE(!mask || ld_mask >= tile_c, "gather_rows: ld_mask < tile_c");
+    if ((st = sbt_use_device(ctx))) return st;
+    return sbt_launch_gather(ctx, es, src, rows, cols, ld_src, idx, n_idx, row_offset, col_offset, tile_c, mask,
+                             ld_mask, out, ld_out, sbt_pad_word(pad_value, es), (cudaStream_t)stream);
+}
+
+sbt_status sbt_scatter_rows_masked(sbt_context* ctx, sbt_dtype dtype, void* dst, int64_t rows, int64_t cols,
+                                   int64_t ld_dst, const int32_t* idx, int64_t n_idx, int64_t row_offset,
+                                   int64_t col_offset, const void* src, int64_t ld_src, int32_t tile_c,
+                                   const uint8_t* mask, int64_t ld_mask, void* stream) {
+    SBT_REQUIRE(ctx, "ctx is NULL");
+    int es;
+    sbt_status st = check_dtype_move(dtype, &es);
+    if (st) return st;
+    SBT_REQUIRE(rows >= 0 && cols >= 0 && n_idx >= 0, "scatter_rows_masked: negative extent");
+    SBT_REQUIRE(tile_c >= 1 && tile_c <= 65536, "scatter_rows_masked: tile_c must be in [1, 65536]");
+    if (n_idx == 0 || rows * cols == 0) return SBT_OK;
+    SBT_REQUIRE(dst && idx && src, "scatter_rows_masked: NULL pointer");
+    SBT_REQUIRE(ld_dst >= cols, "scatter_rows_masked: ld_dst < cols");
+    SBT_REQUIRE(ld_src >= tile_c, "scatter_rows_masked: ld_src < tile_c");
+    SBT_REQUIRE(!mask || ld_mask >= tile_c, "scatter_rows_masked: ld_mask < tile_c");
+    if ((st = sbt_use_device(ctx))) return st;
+    return sbt_launch_scatter(ctx, es, dst, rows, cols, ld_dst, idx, n_idx, row_offset, col_offset, src, ld_src,
+                              tile_c, mask, ld_mask, (cudaStream_t)stream);
+}
+
+sbt_status sbt_ragged_tile_load(sbt_context* ctx, sbt_dtype dtype, const void* x, int64_t total_rows, int32_t heads,
+                                int32_t depth, int64_t ld_row, int64_t ld_head, const int32_t* cu_seqlens,
+                                int32_t batch, int32_t t_pad, void* out, void* stream) {
+    SBT_REQUIRE(ctx, "ctx is NULL");
+    int es;
+    sbt_status st = check_dtype_move(dtype, &es);
+    if (st) return st;
+    SBT_REQUIRE(total_rows >= 0 && heads >= 0 && depth >= 0 && batch >= 0 && t_pad >= 0,
+                "ragged_tile_load: negative extent");
+    if ((int64_t)batch * heads * t_pad * depth == 0) return SBT_OK;
+    SBT_REQUIRE(out && cu_seqlens, "ragged_tile_load: NULL out or cu_seqlens");
+    SBT_REQUIRE(total_rows == 0 || x, "ragged_tile_load: x is NULL");
+    SBT_REQUIRE(ld_row > 0 && ld_head > 0, "ragged_tile_load: strides must be positive");
+    if ((st = sbt_use_device(ctx))) return st;
+    return sbt_launch_ragged(ctx, es, x, total_rows, heads, depth, ld_row, ld_head, cu_seqlens, batch, t_pad, out,
+                             (cudaStream_t)stream);
+}
+
+sbt_status sbt_gemm_bounded_workspace_size(sbt_context* ctx, int64_t M, int64_t N, int64_t K, int64_t lda,
+                                           int64_t ldb, size_t* bytes) {
+    SBT_REQUIRE(ctx && bytes, "NULL argument");
+    SBT_REQUIRE(M >= 0 && N >= 0 && K >= 0, "gemm_bounded: negative extent");
+    SBT_REQUIRE(lda >= K && ldb >= N, "gemm_bounded: leading dimension smaller than the extent");
+    *bytes = sbt_gemm_workspace_bytes(M, N, K);
+    return SBT_OK;
+}
+
+sbt_status sbt_gemm_bounded(sbt_context* ctx, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+                            int64_t ldc, sbt_dtype c_dtype, int64_t M, int64_t N, int64_t K, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+    SBT_REQUIRE(ctx, "ctx is NULL");
+    SBT_REQUIRE(M >= 0 && N >= 0 && K >= 0, "gemm_bounded: negative extent");
+    if (c_dtype != SBT_BF16 && c_dtype != SBT_F32)
+        return sbt_fail(SBT_ERR_UNSUPPORTED, "gemm_bounded: c_dtype must be SBT_BF16 or SBT_F32");
+    SBT_REQUIRE(lda >= K && ldb >= N && ldc >= N, "gemm_bounded: leading dimension smaller than the extent");
+    if (M == 0 || N == 0) return SBT_OK;
+    SBT_REQUIRE(C, "gemm_bounded: C is NULL");
+    SBT_REQUIRE(K == 0 || (A && B), "gemm_bounded: NULL A or B");
+    size_t need = sbt_gemm_workspace_bytes(M, N, K);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need)
+            return sbt_fail(SBT_ERR_ALIGNMENT, "gemm_bounded: workspace smaller than sbt_gemm_bounded_workspace_size()");
+        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+            return sbt_fail(SBT_ERR_ALIGNMENT, "gemm_bounded: workspace must be 256-byte aligned");
+    }
+    sbt_status st = sbt_use_device(ctx);
+    if (st) return st;
+    return sbt_launch_gemm(ctx, A, lda, B, ldb, C, ldc, c_dtype, M, N, K, workspace, workspace_bytes,
+                           (cudaStream_t)stream);
+}
+
+}  // extern "C"

@@ -1,0 +1,126 @@
+// Internal declarations shared by the translation units of libsbt.so.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "../../include/sbt.h"
+
+// ----------------------------------------------------------------------------
+// Host side
+// ----------------------------------------------------------------------------
+
+typedef CUresult (*sbt_encode_tiled_fn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                        const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                        CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+struct sbt_context {
+    int device = 0;
+    int sm_count = 0;
+    int cc_major = 0, cc_minor = 0;
+    size_t smem_optin = 0;
+    sbt_path path = SBT_PATH_AUTO;
+    uint64_t wait_limit_ns = 2000000000ull;
+    unsigned int* status = nullptr;  // device address of this device's status flag
+    sbt_encode_tiled_fn encode_tiled = nullptr;
+    uint64_t launches = 0;
+};
+
+// Thread-local error message; returns `st` so call sites can `return sbt_fail(...)`.
+sbt_status sbt_fail(sbt_status st, const std::string& msg);
+sbt_status sbt_ok();
+sbt_status sbt_cuda_check(cudaError_t e, const char* what);
+// Makes ctx->device current.
+sbt_status sbt_use_device(sbt_context* ctx);
+
+inline int sbt_dtype_size(sbt_dtype t) {
+    switch (t) {
+        case SBT_F32: return 4;
+        case SBT_BF16: return 2;
+        case SBT_F16: return 2;
+    }
+    return 0;
+}
+
+inline bool sbt_aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline bool sbt_mul16(int64_t elems, int es) { return ((elems * es) % 16) == 0; }
+inline int64_t sbt_cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Replicates one element's bits into a 32-bit word (es = 2 or 4).
+uint32_t sbt_pad_word(const void* pad, int es);
+
+// Grid size for a persistent kernel: SMs x resident blocks, capped by the work.
+int sbt_persistent_grid(const sbt_context* ctx, const void* kernel, int threads, size_t smem, int64_t work_units);
+
+// Launchers of the movement kernels (one translation unit each).
+sbt_status sbt_launch_tile_load(sbt_context* ctx, int es, const void* src, int64_t rows, int64_t cols,
+                                int64_t stride_r, int64_t stride_c, int64_t origin_r, int64_t origin_c,
+                                int64_t step_r, int64_t step_c, int32_t grid_r, int32_t grid_c, int32_t tile_r,
+                                int32_t tile_c, void* dst, uint32_t pad_word, cudaStream_t stream);
+sbt_status sbt_launch_tile_store(sbt_context* ctx, int es, const void* src_tiles, int32_t grid_r, int32_t grid_c,
+                                 int32_t tile_r, int32_t tile_c, void* dst, int64_t rows, int64_t cols,
+                                 int64_t stride_r, int64_t stride_c, int64_t origin_r, int64_t origin_c,
+                                 int64_t step_r, int64_t step_c, cudaStream_t stream);
+sbt_status sbt_launch_gather(sbt_context* ctx, int es, const void* src, int64_t rows, int64_t cols, int64_t ld_src,
+                             const int32_t* idx, int64_t n_idx, int64_t row_offset, int64_t col_offset,
+                             int32_t tile_c, const uint8_t* mask, int64_t ld_mask, void* out, int64_t ld_out,
+                             uint32_t pad_word, cudaStream_t stream);
+sbt_status sbt_launch_scatter(sbt_context* ctx, int es, void* dst, int64_t rows, int64_t cols, int64_t ld_dst,
+                              const int32_t* idx, int64_t n_idx, int64_t row_offset, int64_t col_offset,
+                              const void* src, int64_t ld_src, int32_t tile_c, const uint8_t* mask, int64_t ld_mask,
+                              cudaStream_t stream);
+sbt_status sbt_launch_ragged(sbt_context* ctx, int es, const void* x, int64_t total_rows, int32_t heads,
+                             int32_t depth, int64_t ld_row, int64_t ld_head, const int32_t* cu_seqlens,
+                             int32_t batch, int32_t t_pad, void* out, cudaStream_t stream);
+sbt_status sbt_launch_gemm(sbt_context* ctx, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
+                           int64_t ldc, sbt_dtype c_dtype, int64_t M, int64_t N, int64_t K, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream);
+size_t sbt_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+
+// Checks the launch that was just enqueued and counts it.
+sbt_status sbt_after_launch(sbt_context* ctx, const char* what);
+
+// ----------------------------------------------------------------------------
+// Device side: raw element types and 16-byte vector accesses
+// ----------------------------------------------------------------------------
+
+template <int ES> struct sbt_elem;
+template <> struct sbt_elem<2> { typedef uint16_t T; };
+template <> struct sbt_elem<4> { typedef uint32_t T; };
+
+// Read-only 16-byte load that does not allocate in L1 (streamed data).
+__device__ __forceinline__ uint4 sbt_ld_nc_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void sbt_st_v4(void* p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
+// Element e (0..16/ES-1) of a 16-byte vector.
+template <int ES>
+__device__ __forceinline__ typename sbt_elem<ES>::T sbt_vec_get(const uint4& v, int e) {
+    uint32_t w = e * ES / 4 == 0 ? v.x : e * ES / 4 == 1 ? v.y : e * ES / 4 == 2 ? v.z : v.w;
+    if (ES == 4) return (typename sbt_elem<ES>::T)w;
+    return (typename sbt_elem<ES>::T)((e & 1) ? (w >> 16) : (w & 0xFFFFu));
+}
+
+template <int ES>
+__device__ __forceinline__ void sbt_vec_set(uint4& v, int e, typename sbt_elem<ES>::T x) {
+    uint32_t* w = e * ES / 4 == 0 ? &v.x : e * ES / 4 == 1 ? &v.y : e * ES / 4 == 2 ? &v.z : &v.w;
+    if (ES == 4) {
+        *w = (uint32_t)x;
+    } else if (e & 1) {
+        *w = (*w & 0x0000FFFFu) | ((uint32_t)x << 16);
+    } else {
+        *w = (*w & 0xFFFF0000u) | (uint32_t)x;
+    }
+}

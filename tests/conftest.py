@@ -24,3 +24,22 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def sbt_ctx():
+    """One library context on cuda:0 (the build must exist: no fallback)."""
+    import scatter_boundary_tile_gb300 as sbt
+
+    sbt.load_library()
+    ctx = sbt.Context(0)
+    yield ctx
+    ctx.close()
+
+
+@pytest.fixture
+def ctx(sbt_ctx):
+    sbt_ctx.set_path("auto")
+    yield sbt_ctx
+    sbt_ctx.set_path("auto")
+    sbt_ctx.check_status()

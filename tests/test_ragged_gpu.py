@@ -1,0 +1,75 @@
+"""GPU parity of sbt_ragged_tile_load against the CPU oracle (bit-exact)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import scatter_boundary_tile_gb300 as sbt
+import synth
+import synth.workloads as wl
+from gpu_helpers import Canvas, dev, host, sync
+
+pytestmark = pytest.mark.gpu
+
+
+def gpu_ragged(ctx, x, total_rows, heads, depth, ld_row, ld_head, cu, t_pad, dtype, path="auto"):
+    batch = cu.size - 1
+    es = x.dtype.itemsize
+    canvas = Canvas(batch * heads * t_pad * depth * es)
+    xd, cd = dev(x), dev(cu.astype(np.int32))
+    ctx.set_path(path)
+    sbt.ragged_tile_load(ctx, xd, total_rows, heads, depth, ld_row, ld_head, cd, batch, t_pad, canvas.ptr,
+                         dtype=dtype)
+    sync()
+    assert canvas.guards_intact()
+    return canvas.inner(x.dtype, (batch, heads, t_pad, depth))
+
+
+@pytest.mark.parametrize("t_pad", [300, 256, 100, 129])
+@pytest.mark.parametrize("depth", [128, 24, 20])
+def test_small_batches(ctx, t_pad, depth):
+    d = wl.ragged_bf16(batch=5, max_len=300, heads=3, depth=depth)
+    x, cu = d["x"], d["cu_seqlens"]
+    want = oracle.ragged_tile_load(x, d["total_rows"], 3, depth, 3 * depth, depth, cu, t_pad)
+    for path in ("auto", "scalar"):
+        got = gpu_ragged(ctx, x, d["total_rows"], 3, depth, 3 * depth, depth, cu, t_pad, "bf16", path=path)
+        assert np.array_equal(got, want), path
+
+
+def test_fp32_strided_heads(ctx):
+    # heads interleaved with padding: ld_head 40 > depth 32, ld_row 4*40 + 8
+    total, H, D, ldh, ldr = 90, 4, 32, 40, 168
+    x = synth.uniform_f32(401, (total, ldr))
+    cu = np.array([0, 10, 10, 70, 90], np.int32)
+    want = oracle.ragged_tile_load(x, total, H, D, ldr, ldh, cu, 64)
+    got = gpu_ragged(ctx, x, total, H, D, ldr, ldh, cu, 64, "f32")
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+def test_inconsistent_metadata_reads_zero(ctx):
+    x = synth.normal_bf16(402, (10, 2, 8))
+    cu = np.array([0, 0, 8, 14, 3, -5, 4], np.int32)  # empty, past total_rows, negative length, negative start
+    want = oracle.ragged_tile_load(x, 10, 2, 8, 16, 8, cu, 6)
+    got = gpu_ragged(ctx, x, 10, 2, 8, 16, 8, cu, 6, "bf16")
+    assert np.array_equal(got, want)
+
+
+def test_equal_lengths_is_transpose(ctx):
+    B, T, H, D = 4, 256, 8, 128
+    x = synth.normal_bf16(403, (B * T, H, D))
+    cu = np.arange(B + 1, dtype=np.int32) * T
+    got = gpu_ragged(ctx, x, B * T, H, D, H * D, D, cu, T, "bf16")
+    assert np.array_equal(got, x.reshape(B, T, H, D).transpose(0, 2, 1, 3))
+
+
+def test_full_size_workload_bit_exact(ctx):
+    """batch 64, lengths uniform in [1, 4096], 8 heads, depth 128, bf16 -> [64][8][4096][128]:
+    the launch the benchmark times; the whole output is compared."""
+    d = wl.ragged_bf16()
+    x, cu = d["x"], d["cu_seqlens"]
+    out = torch.empty(64 * 8 * 4096 * 128 * 2, dtype=torch.uint8, device="cuda")
+    xd, cd = dev(x), dev(cu)
+    sbt.ragged_tile_load(ctx, xd, d["total_rows"], 8, 128, 8 * 128, 128, cd, 64, 4096, out, dtype="bf16")
+    got = host(out, np.uint16, (64, 8, 4096, 128))
+    want = oracle.ragged_tile_load(x, d["total_rows"], 8, 128, 1024, 128, cu, 4096)
+    assert np.array_equal(got, want)
