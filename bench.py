@@ -45,6 +45,11 @@ def parse():
     ap.add_argument("--no-ops", action="store_true", help="skip the per-operation extras")
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=8.0, help="CPU-baseline sample budget")
+    ap.add_argument("--profile", default=None,
+                    choices=["gather", "scatter", "ragged", "tile_load", "tile_store", "tile_load_unaligned",
+                             "tile_store_unaligned", "gemm"],
+                    help="only launch one operation's workload (warmup + steps launches) for ncu")
+    ap.add_argument("--scale", type=float, default=1.0, help="--profile: fraction of the workload's rows")
     return ap.parse_args()
 
 
@@ -451,8 +456,67 @@ def run_sbt(args, dist):
     return 0
 
 
+def run_profile(args):
+    """Launch one operation `warmup + steps` times on its workload (scaled by --scale) and
+    print the mean device time; used as the command under ncu."""
+    import torch
+    import scatter_boundary_tile_gb300 as sbt
+    import synth
+    import synth.workloads as wl
+    ctx = sbt.Context(0)
+    op, f = args.profile, args.scale
+    if op == "gather":
+        d = wl.gather_rows_bf16(n_rows=max(1, int(1_000_000 * f)), n_idx=max(1, int(1_048_576 * f)))
+        t, i = dev_bytes(d["table"]), dev_bytes(d["idx"])
+        n, rows = d["idx"].size, d["n_rows"]
+        out = torch.empty(n * 512 * 2, dtype=torch.uint8, device="cuda")
+        fn = lambda: sbt.gather_rows(ctx, t, rows, 512, 512, i, n, out, 512, 512, dtype="bf16")
+    elif op == "scatter":
+        d = wl.scatter_rows_f32(dst_rows=max(1, int(4_194_304 * f)), n_idx=max(1, int(1_048_576 * f)))
+        rows, n = d["dst_rows"], d["idx"].size
+        dst = torch.zeros(rows * 256 * 4, dtype=torch.uint8, device="cuda")
+        s_, i, m = dev_bytes(d["src"]), dev_bytes(d["idx"]), dev_bytes(d["mask"])
+        fn = lambda: sbt.scatter_rows_masked(ctx, dst, rows, 256, 256, i, n, s_, 256, 256, mask=m, ld_mask=256,
+                                             dtype="f32")
+    elif op == "ragged":
+        d = wl.ragged_bf16(batch=max(1, int(64 * f)))
+        b = d["cu_seqlens"].size - 1
+        out = torch.empty(b * 8 * 4096 * 128 * 2, dtype=torch.uint8, device="cuda")
+        x, cu = dev_bytes(d["x"]), dev_bytes(d["cu_seqlens"])
+        fn = lambda: sbt.ragged_tile_load(ctx, x, d["total_rows"], 8, 128, 1024, 128, cu, b, 4096, out,
+                                          dtype="bf16")
+    elif op.startswith("tile"):
+        r_, c_ = max(64, int(16381 * f)), 16411
+        ld = 16411 if op.endswith("unaligned") else 16416
+        a = synth.uniform_f32(0x5B7101, (r_, ld), -1.0, 1.0)
+        gr, gc = -(-r_ // 64), -(-c_ // 32)
+        ad = dev_bytes(a)
+        tiles = torch.empty(gr * gc * 64 * 32 * 4, dtype=torch.uint8, device="cuda")
+        if op.startswith("tile_load"):
+            fn = lambda: sbt.tile_load_padded(ctx, ad, r_, c_, ld, 1, 0, 0, 64, 32, gr, gc, 64, 32, tiles,
+                                              dtype="f32")
+        else:
+            fn = lambda: sbt.tile_store_clipped(ctx, tiles, gr, gc, 64, 32, ad, r_, c_, ld, 1, 0, 0, 64, 32,
+                                                dtype="f32")
+    else:  # gemm: (8191, 8193, 4097) scaled along M
+        M, N, K = max(1, int(8191 * f)), 8193, 4097
+        g = wl.gemm_bf16(M=M, N=N, K=K)
+        A, B = dev_bytes(g["A"]), dev_bytes(g["B"])
+        C = torch.empty(M * g["ldc"] * 2, dtype=torch.uint8, device="cuda")
+        ws_n = sbt.gemm_bounded_workspace_size(ctx, M, N, K, g["lda"], g["ldb"])
+        ws = torch.empty(max(ws_n, 256), dtype=torch.uint8, device="cuda")
+        fn = lambda: sbt.gemm_bounded(ctx, A, g["lda"], B, g["ldb"], C, g["ldc"], M, N, K, ws, ws_n)
+    med, mean, best = time_launches(fn, args.steps, warmup=args.warmup)
+    ctx.check_status()
+    print(json.dumps({"profile": op, "scale": f, "ms_median": med, "ms_mean": mean, "ms_best": best,
+                      "launches": ctx.launch_count}), flush=True)
+    return 0
+
+
 def main():
     args = parse()
+    if args.profile:
+        return run_profile(args)
     if args.warmup < 3:
         args.warmup = 3
     dist = Dist()

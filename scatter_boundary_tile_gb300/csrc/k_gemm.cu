@@ -1,15 +1,405 @@
-// Boundary-tile bf16 GEMM (placeholder until the tcgen05 kernel lands).
+// Boundary-tile bf16 GEMM  C = A * B  on tcgen05 tensor cores.
+//
+// cuTile.jl "Operations", muladd: (M,K) x (K,N) -> (M,N), bf16 inputs with an
+// fp32 accumulator.  Tylo.jl "Boundary tiles", section "Accumulator stores
+// and GEMM": ceiling-division K loop and output grid; boundary tiles are
+// zero-filled; the accumulator is converted to the output type at the store
+// and stores outside M x N are suppressed.
+//
+// Pipeline (all on the caller's stream):
+//  1. Operand staging (the bounded copy of Tylo.jl "Boundary tiles"): A and
+//     B may have any leading dimension (odd ones included), which TMA cannot
+//     address (its row strides are multiples of 16 bytes).  Two kernels copy
+//     A -> A' [Mp][Kp] and B -> B' [Np][Kp] (B transposed, so both operands
+//     are K-major), zero-filling every element past M, N or K, with
+//     Mp, Np, Kp rounded up to whole tiles.  A' and B' live in the caller's
+//     workspace.
+//  2. A persistent, warp-specialised kernel: warp 0 issues TMA tile loads
+//     into a 4-stage shared-memory ring (128-byte swizzle), warp 1 issues
+//     tcgen05.mma (M=128, N<=256, K=16, fp32 accumulator in TMEM, two
+//     256-column accumulators so the epilogue of one tile overlaps the main
+//     loop of the next), warps 2-5 drain TMEM with tcgen05.ld, round to bf16
+//     (or keep fp32) and store through a shared-memory transpose so that
+//     each store instruction writes one contiguous row segment.
+//  Every mbarrier wait is bounded; a wait that runs out sets the device
+//  status word, and the kernel drains and returns.
+#include <cuda_bf16.h>
+
+#include <algorithm>
+#include <string>
+
 #include "sbt_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace {
+
+using namespace sbt_ptx;
+
+constexpr int BM = 128, BN = 256, BK = 64;
+constexpr int kStages = 4;
+constexpr int kGemmThreads = 192;  // warp 0: TMA, warp 1: MMA, warps 2..5: epilogue
+constexpr uint32_t kABytes = BM * BK * 2;
+constexpr uint32_t kBBytes = BN * BK * 2;
+constexpr uint32_t kStageBytes = kABytes + kBBytes;
+constexpr int kEpiWarps = 4;
+constexpr int kEpiWords = 32 * 33;  // per-warp 32x32 transpose buffer, padded rows
+constexpr uint32_t kTmemCols = 2 * BN;
+constexpr int kNumBars = 2 * kStages + 5;
+constexpr size_t kGemmSmem = 1024 + (size_t)kStages * kStageBytes + (size_t)kEpiWarps * kEpiWords * 4 +
+                             kNumBars * 8 + 16;
+
+enum : unsigned int { kCodeProducer = 0x100, kCodeMma = 0x200, kCodeEpilogue = 0x400, kCodeTeardown = 0x800 };
+
+struct GemmParams {
+    char* C;
+    int64_t ldc;
+    int c_f32;
+    int M, N, K;
+    int m_tiles, n_tiles, k_blocks;
+    unsigned int* status;
+    uint64_t wait_ns;
+};
+
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    k_gemm_bf16_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* epi = reinterpret_cast<float*>(smem + (size_t)kStages * kStageBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(epi + kEpiWarps * kEpiWords);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const uint32_t bar0 = smem_u32(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kStages + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kStages + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kStages + 2 + a); };
+    const uint32_t mma_done_bar = bar0 + 8u * (2 * kStages + 4);
+
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x / 32), 0);
+    const int lane = threadIdx.x % 32;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), kEpiWarps * 32);
+        }
+        mbar_init(mma_done_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int num_tiles = p.m_tiles * p.n_tiles;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            int64_t issued = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, p.wait_ns, abort_flag, p.status,
+                                           kCodeProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t sa = smem_u32(smem + (size_t)stage * kStageBytes);
+                    mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
+                    tma_load_2d(sa, &tmA, kb * BK, mt * BM, full_bar(stage));
+                    tma_load_2d(sa + kABytes, &tmB, kb * BK, nt * BN, full_bar(stage));
+                    ++issued;
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // Drain: wait (bounded) until the copies still in flight have landed.
+                uint32_t s = stage, ph = phase;
+                for (int64_t j = 0; j < issued && j < kStages; ++j) {
+                    if (s == 0) {
+                        s = kStages - 1;
+                        ph ^= 1u;
+                    } else {
+                        --s;
+                    }
+                    const uint64_t t0 = globaltimer();
+                    while (!mbar_try_wait(full_bar(s), ph) && globaltimer() - t0 < p.wait_ns) {
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            int local = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
+                const int acc = local & 1;
+                const uint32_t use = (uint32_t)(local >> 1);
+                const int nt = tile / p.m_tiles;
+                const int n_valid = min(BN, p.N - nt * BN);
+                const uint32_t idesc = idesc_bf16_f32(BM, (uint32_t)((n_valid + 15) & ~15));
+                if (!mbar_wait_bounded(tempty_bar(acc), (use & 1u) ^ 1u, p.wait_ns, abort_flag, p.status,
+                                       kCodeMma)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait_bounded(full_bar(stage), phase, p.wait_ns, abort_flag, p.status, kCodeMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int k_rem = p.K - kb * BK;
+                    const int k_steps = k_rem >= BK ? BK / 16 : (k_rem + 15) / 16;
+                    const uint32_t sa = smem_u32(smem + (size_t)stage * kStageBytes);
+                    const uint32_t sb = sa + kABytes;
+                    for (int ks = 0; ks < k_steps; ++ks) {
+                        tc_mma_f16(d_tmem, smem_desc_sw128(sa + 32u * ks), smem_desc_sw128(sb + 32u * ks), idesc,
+                                   (kb | ks) != 0 ? 1u : 0u);
+                    }
+                    tc_commit(empty_bar(stage));
+                    if (++stage == kStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (ok) tc_commit(tfull_bar(acc));
+            }
+            // every MMA this thread issued has completed once mma_done flips
+            tc_commit(mma_done_bar);
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(mma_done_bar, 0)) {
+                if (globaltimer() - t0 > p.wait_ns) {
+                    atomicOr(p.status, (unsigned int)kCodeTeardown);
+                    break;
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue (warps 2..5)
+        const int q = warp & 3;  // TMEM lane quarter this warp may read
+        float* buf = epi + (warp - 2) * kEpiWords;
+        int local = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+            const int acc = local & 1;
+            const uint32_t use = (uint32_t)(local >> 1);
+            const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+            if (!mbar_wait_bounded(tfull_bar(acc), use & 1u, p.wait_ns, abort_flag, p.status, kCodeEpilogue)) break;
+            tc_fence_after();
+            const int n0 = nt * BN;
+            const int n_valid = min(BN, p.N - n0);
+            const int chunks = (n_valid + 31) / 32;
+            const int row0 = mt * BM + q * 32;
+            for (int c = 0; c < chunks; ++c) {
+                uint32_t r[32];
+                tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c * 32), r);
+                tmem_ld_wait();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) buf[lane * 33 + j] = __uint_as_float(r[j]);
+                __syncwarp();
+                const int col = n0 + c * 32 + lane;
+                if (col < p.N) {
+                    if (p.c_f32) {
+                        float* Cp = reinterpret_cast<float*>(p.C);
+                        for (int rr = 0; rr < 32 && row0 + rr < p.M; ++rr)
+                            Cp[(int64_t)(row0 + rr) * p.ldc + col] = buf[rr * 33 + lane];
+                    } else {
+                        __nv_bfloat16* Cp = reinterpret_cast<__nv_bfloat16*>(p.C);
+                        for (int rr = 0; rr < 32 && row0 + rr < p.M; ++rr)
+                            Cp[(int64_t)(row0 + rr) * p.ldc + col] = __float2bfloat16_rn(buf[rr * 33 + lane]);
+                    }
+                }
+                __syncwarp();
+            }
+            tc_fence_before();
+            mbar_arrive(tempty_bar(acc));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------- operand staging
+
+// A' [Mp][Kp] <- A [M][K] (row stride lda), zero past M or K.  One 16-byte vector of A' per task.
+__global__ void __launch_bounds__(256) k_stage_a(const uint16_t* __restrict__ A, int64_t lda, int M, int K,
+                                                 uint16_t* __restrict__ Ap, int Kp, int64_t total_vecs) {
+    const int kv = Kp / 8;
+    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < total_vecs;
+         v += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t m = v / kv;
+        const int k0 = (int)(v - m * kv) * 8;
+        uint32_t w[4] = {0, 0, 0, 0};
+        if (m < M) {
+            const uint16_t* row = A + m * lda;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const int k = k0 + e;
+                const uint32_t x = k < K ? (uint32_t)__ldg(row + k) : 0u;
+                w[e >> 1] |= x << (16 * (e & 1));
+            }
+        }
+        sbt_st_v4(Ap + m * Kp + k0, make_uint4(w[0], w[1], w[2], w[3]));
+    }
+}
+
+// B' [Np][Kp] <- transpose of B [K][N] (row stride ldb), zero past K or N.
+// 64 x 64 tiles through shared memory: coalesced reads along n, 16-byte writes along k.
+__global__ void __launch_bounds__(256) k_stage_bt(const uint16_t* __restrict__ B, int64_t ldb, int K, int N,
+                                                  uint16_t* __restrict__ Bp, int Kp) {
+    __shared__ uint16_t t[64][66];
+    const int k0 = blockIdx.x * 64, n0 = blockIdx.y * 64;
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const int idx = i * 256 + threadIdx.x;
+        const int kk = idx >> 6, nn = idx & 63;
+        const int k = k0 + kk, n = n0 + nn;
+        t[kk][nn] = (k < K && n < N) ? __ldg(B + (int64_t)k * ldb + n) : (uint16_t)0;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        const int task = i * 256 + threadIdx.x;  // 64 rows of B' x 8 vectors
+        const int nn = task >> 3, kv = task & 7;
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            w[e] = (uint32_t)t[kv * 8 + 2 * e][nn] | ((uint32_t)t[kv * 8 + 2 * e + 1][nn] << 16);
+        sbt_st_v4(Bp + (int64_t)(n0 + nn) * Kp + k0 + kv * 8, make_uint4(w[0], w[1], w[2], w[3]));
+    }
+}
+
+// C[m][n] = 0 for m < M, n < N (the K = 0 product).
+__global__ void k_zero_c(char* C, int64_t ldc, int M, int N, int es) {
+    const int64_t total = (int64_t)M * N;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t m = i / N, n = i - m * N;
+        if (es == 4)
+            reinterpret_cast<float*>(C)[m * ldc + n] = 0.f;
+        else
+            reinterpret_cast<uint16_t*>(C)[m * ldc + n] = 0;
+    }
+}
+
+struct GemmDims {
+    int64_t Mp, Np, Kp;
+    size_t a_bytes, b_bytes;
+};
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+GemmDims gemm_dims(int64_t M, int64_t N, int64_t K) {
+    GemmDims d;
+    d.Mp = sbt_cdiv(M, BM) * BM;
+    d.Np = sbt_cdiv(N, BN) * BN;
+    d.Kp = sbt_cdiv(K, BK) * BK;
+    d.a_bytes = round_up((size_t)d.Mp * d.Kp * 2, 256);
+    d.b_bytes = round_up((size_t)d.Np * d.Kp * 2, 256);
+    return d;
+}
+
+sbt_status encode_kmajor(sbt_context* ctx, CUtensorMap* map, void* base, int64_t rows, int64_t kp, int box_rows) {
+    cuuint64_t dims[2] = {(cuuint64_t)kp, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)kp * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = ctx->encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+                                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return sbt_fail(SBT_ERR_TENSOR_MAP, "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
+    return SBT_OK;
+}
+
+}  // namespace
 
 size_t sbt_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
-    (void)M; (void)N; (void)K;
-    return 0;
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    const GemmDims d = gemm_dims(M, N, K);
+    return d.a_bytes + d.b_bytes;
 }
 
 sbt_status sbt_launch_gemm(sbt_context* ctx, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
                            int64_t ldc, sbt_dtype c_dtype, int64_t M, int64_t N, int64_t K, void* workspace,
                            size_t workspace_bytes, cudaStream_t stream) {
-    (void)ctx; (void)A; (void)lda; (void)B; (void)ldb; (void)C; (void)ldc; (void)c_dtype; (void)M; (void)N; (void)K;
-    (void)workspace; (void)workspace_bytes; (void)stream;
-    return sbt_fail(SBT_ERR_UNSUPPORTED, "gemm_bounded: not built yet");
+    (void)workspace_bytes;
+    const int es_c = c_dtype == SBT_F32 ? 4 : 2;
+    if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2)
+        return sbt_fail(SBT_ERR_INVALID_ARG, "gemm_bounded: extents must be below 2^30");
+    if (K == 0) {
+        const int grid = (int)std::min<int64_t>(sbt_cdiv(M * N, 256), (int64_t)ctx->sm_count * 8);
+        k_zero_c<<<grid, 256, 0, stream>>>((char*)C, ldc, (int)M, (int)N, es_c);
+        return sbt_after_launch(ctx, "gemm_bounded (K=0)");
+    }
+    const GemmDims d = gemm_dims(M, N, K);
+    if (d.Np / 64 > 65535 || d.Kp / 64 > INT32_MAX)
+        return sbt_fail(SBT_ERR_INVALID_ARG, "gemm_bounded: N too large for the staging grid");
+    uint16_t* Ap = (uint16_t*)workspace;
+    uint16_t* Bp = (uint16_t*)((char*)workspace + d.a_bytes);
+
+    // 1. operand staging
+    {
+        const int64_t vecs = d.Mp * (d.Kp / 8);
+        const int grid = (int)std::min<int64_t>(sbt_cdiv(vecs, 256), (int64_t)ctx->sm_count * 8);
+        k_stage_a<<<grid, 256, 0, stream>>>((const uint16_t*)A, lda, (int)M, (int)K, Ap, (int)d.Kp, vecs);
+        sbt_status st = sbt_after_launch(ctx, "gemm_bounded (stage A)");
+        if (st) return st;
+        dim3 g2((unsigned)(d.Kp / 64), (unsigned)(d.Np / 64));
+        k_stage_bt<<<g2, 256, 0, stream>>>((const uint16_t*)B, ldb, (int)K, (int)N, Bp, (int)d.Kp);
+        if ((st = sbt_after_launch(ctx, "gemm_bounded (stage B)"))) return st;
+    }
+
+    // 2. tensor-core main kernel
+    CUtensorMap tmA, tmB;
+    sbt_status st = encode_kmajor(ctx, &tmA, Ap, d.Mp, d.Kp, BM);
+    if (st) return st;
+    if ((st = encode_kmajor(ctx, &tmB, Bp, d.Np, d.Kp, BN))) return st;
+    GemmParams p;
+    p.C = (char*)C;
+    p.ldc = ldc;
+    p.c_f32 = c_dtype == SBT_F32;
+    p.M = (int)M;
+    p.N = (int)N;
+    p.K = (int)K;
+    p.m_tiles = (int)(d.Mp / BM);
+    p.n_tiles = (int)(d.Np / BN);
+    p.k_blocks = (int)(d.Kp / BK);
+    p.status = ctx->status;
+    p.wait_ns = ctx->wait_limit_ns;
+    static bool attr_set[64] = {false};
+    if (!attr_set[ctx->device & 63]) {
+        cudaError_t e = cudaFuncSetAttribute(k_gemm_bf16_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
+        if (e != cudaSuccess) return sbt_cuda_check(e, "cudaFuncSetAttribute(gemm smem)");
+        attr_set[ctx->device & 63] = true;
+    }
+    const int tiles = p.m_tiles * p.n_tiles;
+    const int grid = std::min(tiles, ctx->sm_count);
+    k_gemm_bf16_tc<<<grid, kGemmThreads, kGemmSmem, stream>>>(tmA, tmB, p);
+    return sbt_after_launch(ctx, "gemm_bounded (tcgen05)");
 }

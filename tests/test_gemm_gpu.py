@@ -1,0 +1,163 @@
+"""GPU parity of sbt_gemm_bounded (tcgen05) against the fp64 CPU oracle.
+
+Gate (spec tolerance, read for a bf16 output): relative Frobenius error
+||C - bf16(ref)||_F / ||ref||_F <= 1e-3, where ref is the exact-product,
+double-accumulated oracle and bf16() its round-to-nearest-even.  An fp32
+output is compared with ref directly at the same bound.  Integer-valued
+inputs make every partial sum exact in fp32, so those cases must match bit
+for bit.  Operand leading-dimension padding holds NaN, so a read past K or N
+would show.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import scatter_boundary_tile_gb300 as sbt
+import synth
+import synth.workloads as wl
+from gpu_helpers import Canvas, dev, host, sync
+
+pytestmark = pytest.mark.gpu
+TOL = 1e-3
+
+
+def run_gemm(ctx, g, c_dtype="bf16", ws_pad=0):
+    M, N, K, lda, ldb, ldc = g["M"], g["N"], g["K"], g["lda"], g["ldb"], g["ldc"]
+    es = 2 if c_dtype == "bf16" else 4
+    A, B = dev(g["A"]), dev(g["B"])
+    canvas = Canvas(M * ldc * es)
+    ws_n = sbt.gemm_bounded_workspace_size(ctx, M, N, K, lda, ldb)
+    ws = torch.empty(max(ws_n + ws_pad, 256), dtype=torch.uint8, device="cuda")
+    sbt.gemm_bounded(ctx, A, lda, B, ldb, canvas.ptr, ldc, M, N, K, ws, ws_n, c_dtype=c_dtype)
+    sync()
+    ctx.check_status()
+    assert canvas.guards_intact()
+    full = canvas.inner(np.uint16 if es == 2 else np.float32, (M, ldc))
+    orig = canvas.original(np.uint16 if es == 2 else np.float32, (M, ldc))
+    assert np.array_equal(full[:, N:].view(np.uint8), orig[:, N:].view(np.uint8)), "padding columns of C written"
+    if es == 2:
+        return synth.bf16_bits_to_f32(full[:, :N]).astype(np.float64), full[:, :N]
+    return full[:, :N].astype(np.float64), None
+
+
+def rel_fro(x, ref):
+    return float(np.linalg.norm(x - ref) / max(np.linalg.norm(ref), 1e-300))
+
+
+SHAPES = [(1, 1, 1), (3, 5, 7), (17, 13, 11), (65, 97, 73), (128, 256, 64), (129, 257, 65), (1, 300, 200),
+          (300, 1, 17), (257, 513, 129), (200, 16, 1000)]
+
+
+@pytest.mark.parametrize("mnk", SHAPES)
+@pytest.mark.parametrize("c_dtype", ["bf16", "f32"])
+def test_shapes_vs_oracle(ctx, mnk, c_dtype):
+    M, N, K = mnk
+    g = wl.gemm_bf16(M=M, N=N, K=K, tag=7)
+    got, bits = run_gemm(ctx, g, c_dtype)
+    ref = oracle.gemm_f64(g["A"], g["lda"], g["B"], g["ldb"], M, N, K)
+    if c_dtype == "bf16":
+        ref_b = oracle.round_bf16(ref)
+        err = rel_fro(got, synth.bf16_bits_to_f32(ref_b).astype(np.float64))
+        # fp32 accumulation rarely moves a result across a bf16 rounding boundary
+        assert np.mean(bits != ref_b) < 0.02
+    else:
+        err = rel_fro(got, ref)
+    assert err <= TOL, err
+
+
+@pytest.mark.parametrize("mnk", [(16, 16, 64), (65, 97, 64), (130, 300, 48)])
+def test_integer_inputs_exact(ctx, mnk):
+    M, N, K = mnk
+    lda, ldb = K + 1, N + 3
+    a = synth.int_below(501, M * K, 5, lo=-2).reshape(M, K).astype(np.float32)
+    b = synth.int_below(502, K * N, 5, lo=-2).reshape(K, N).astype(np.float32)
+    A = np.full((M, lda), wl.BF16_NAN_BITS, np.uint16)
+    B = np.full((K, ldb), wl.BF16_NAN_BITS, np.uint16)
+    A[:, :K] = (a.view(np.uint32) >> 16).astype(np.uint16)
+    B[:, :N] = (b.view(np.uint32) >> 16).astype(np.uint16)
+    g = {"A": A, "B": B, "M": M, "N": N, "K": K, "lda": lda, "ldb": ldb, "ldc": N + 1}
+    want = a.astype(np.int64) @ b.astype(np.int64)
+    got, _ = run_gemm(ctx, g, "bf16")
+    np.testing.assert_array_equal(got, want.astype(np.float64))
+    got32, _ = run_gemm(ctx, g, "f32")
+    np.testing.assert_array_equal(got32, want.astype(np.float64))
+
+
+def test_many_tiles_per_block(ctx):
+    """More tiles than SMs: the persistent loop and both TMEM accumulators are used."""
+    M, N, K = 4096, 2560, 128
+    g = wl.gemm_bf16(M=M, N=N, K=K, tag=8)
+    got, _ = run_gemm(ctx, g, "bf16")
+    ref = oracle.gemm_f64(g["A"], g["lda"], g["B"], g["ldb"], M, N, K)
+    ref_b = synth.bf16_bits_to_f32(oracle.round_bf16(ref)).astype(np.float64)
+    assert rel_fro(got, ref_b) <= TOL
+
+
+def test_config_1000_full(ctx):
+    g = wl.gemm_bf16(M=1000, N=1000, K=1000)
+    got, _ = run_gemm(ctx, g, "bf16")
+    ref = oracle.gemm_f64(g["A"], g["lda"], g["B"], g["ldb"], 1000, 1000, 1000)
+    ref_b = synth.bf16_bits_to_f32(oracle.round_bf16(ref)).astype(np.float64)
+    assert rel_fro(got, ref_b) <= TOL
+    # the bf16 output rounding alone puts the error against the unrounded reference near 1.6e-3
+    assert rel_fro(got, ref) < 3e-3
+
+
+def test_large_config_sampled(ctx):
+    """(8191, 8193, 4097), odd leading dimensions: the launch the benchmark times.  The
+    oracle computes 6,000 sampled entries (plus the corners and the last row/column)."""
+    M, N, K = 8191, 8193, 4097
+    g = wl.gemm_bf16(M=M, N=N, K=K)
+    A, B = dev(g["A"]), dev(g["B"])
+    ldc = g["ldc"]
+    C = torch.full((M * ldc,), 0x7FC1, dtype=torch.int16, device="cuda")
+    ws_n = sbt.gemm_bounded_workspace_size(ctx, M, N, K, g["lda"], g["ldb"])
+    ws = torch.empty(ws_n, dtype=torch.uint8, device="cuda")
+    sbt.gemm_bounded(ctx, A, g["lda"], B, g["ldb"], C, ldc, M, N, K, ws, ws_n)
+    sync()
+    ctx.check_status()
+    Ch = C.cpu().numpy().view(np.uint16).reshape(M, ldc)
+    assert np.all(Ch[:, N:] == 0x7FC1)
+    rng = np.random.default_rng(0)
+    ms = np.concatenate([rng.integers(0, M, 6000), [0, 0, M - 1, M - 1], np.full(64, M - 1), np.arange(64)])
+    ns = np.concatenate([rng.integers(0, N, 6000), [0, N - 1, 0, N - 1], np.arange(64), np.full(64, N - 1)])
+    ref = oracle.gemm_f64_at(g["A"], g["lda"], g["B"], g["ldb"], K, ms, ns)
+    got = synth.bf16_bits_to_f32(Ch[ms, ns]).astype(np.float64)
+    ref_b = synth.bf16_bits_to_f32(oracle.round_bf16(ref)).astype(np.float64)
+    assert rel_fro(got, ref_b) <= TOL
+    assert not np.isnan(synth.bf16_bits_to_f32(Ch[:, :N])).any()
+
+
+def test_k_zero_and_empty(ctx):
+    g = wl.gemm_bf16(M=5, N=7, K=1)
+    canvas = Canvas(5 * 7 * 2, fill=np.full(35, 0x3F80, np.uint16))
+    A, B = dev(g["A"]), dev(g["B"])
+    sbt.gemm_bounded(ctx, A, 1, B, 7, canvas.ptr, 7, 5, 7, 0, None, 0)
+    sync()
+    assert not canvas.inner(np.uint16, (5, 7)).any()
+    before = ctx.launch_count
+    sbt.gemm_bounded(ctx, A, 1, B, 7, canvas.ptr, 7, 0, 7, 1, None, 0)
+    assert ctx.launch_count == before
+
+
+def test_workspace_errors(ctx):
+    g = wl.gemm_bf16(M=65, N=97, K=73)
+    A, B = dev(g["A"]), dev(g["B"])
+    C = torch.empty(65 * g["ldc"] * 2, dtype=torch.uint8, device="cuda")
+    n = sbt.gemm_bounded_workspace_size(ctx, 65, 97, 73, g["lda"], g["ldb"])
+    ws = torch.empty(n + 512, dtype=torch.uint8, device="cuda")
+    before = ctx.launch_count
+    with pytest.raises(sbt.SbtError) as e:
+        sbt.gemm_bounded(ctx, A, g["lda"], B, g["ldb"], C, g["ldc"], 65, 97, 73, ws, n - 1)
+    assert e.value.status == sbt.SBT_ERR_ALIGNMENT
+    with pytest.raises(sbt.SbtError) as e:
+        sbt.gemm_bounded(ctx, A, g["lda"], B, g["ldb"], C, g["ldc"], 65, 97, 73, ws.data_ptr() + 16, n)
+    assert e.value.status == sbt.SBT_ERR_ALIGNMENT
+    with pytest.raises(sbt.SbtError) as e:
+        sbt.gemm_bounded(ctx, A, 72, B, g["ldb"], C, g["ldc"], 65, 97, 73, ws, n)  # lda < K
+    assert e.value.status == sbt.SBT_ERR_INVALID_ARG
+    with pytest.raises(sbt.SbtError) as e:
+        sbt.gemm_bounded(ctx, A, g["lda"], B, g["ldb"], C, g["ldc"], 65, 97, 73, ws, n, c_dtype=sbt.SBT_F16)
+    assert e.value.status == sbt.SBT_ERR_UNSUPPORTED
+    assert ctx.launch_count == before
