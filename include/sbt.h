@@ -202,6 +202,33 @@ SBT_API sbt_status sbt_gemm_bounded(sbt_context* ctx, const void* A, int64_t lda
                             int64_t ldc, sbt_dtype c_dtype, int64_t M, int64_t N, int64_t K, void* workspace,
                             size_t workspace_bytes, void* stream);
 
+/*
+ * Boundary-tile GEMM without any device allocation.
+ * The pages have no counterpart to this call; it exists for callers that
+ * cannot allocate device memory when they multiply: code running while a
+ * stream is captured into a CUDA graph (cudaMalloc is not allowed there),
+ * plugins confined to another framework's memory pool, and latency-critical
+ * paths that cannot take cudaMalloc's implicit device synchronisation.
+ *
+ * Same arguments and result as sbt_gemm_bounded, minus the workspace: the
+ * operand-staging scratch is a fixed array of SBT_GEMM_NOALLOC_SCRATCH_BYTES
+ * inside the library (one per device, held from module load until process
+ * exit).  Shapes whose sbt_gemm_bounded_workspace_size() exceeds that size
+ * are rejected with SBT_ERR_INVALID_ARG before anything is launched.  The
+ * call itself allocates nothing (no cudaMalloc, no cudaFree).
+ *
+ * The first call on a device looks up the array's device address with
+ * cudaGetSymbolAddress (with that device current) and caches it; make that
+ * first call before any stream capture.  All calls share the one array and
+ * it keeps the previous call's contents (the call rewrites every byte it
+ * reads, so nothing needs clearing); calls that can overlap on the GPU --
+ * different streams, or unsynchronised host threads -- race on it.
+ */
+#define SBT_GEMM_NOALLOC_SCRATCH_BYTES (16u << 20)
+SBT_API sbt_status sbt_gemm_bounded_noalloc(sbt_context* ctx, const void* A, int64_t lda, const void* B, int64_t ldb,
+                                            void* C, int64_t ldc, sbt_dtype c_dtype, int64_t M, int64_t N, int64_t K,
+                                            void* stream);
+
 #ifdef __cplusplus
 }
 #endif

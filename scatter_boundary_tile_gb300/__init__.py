@@ -33,7 +33,8 @@ PATHS = {"auto": 0, "scalar": 1, "vector": 2, "tma": 3}
 EXPORTS = ("sbt_create", "sbt_destroy", "sbt_set_path", "sbt_set_wait_limit_ns", "sbt_launch_count",
            "sbt_check_status", "sbt_last_error_message", "sbt_tile_load_padded", "sbt_tile_store_clipped",
            "sbt_gather_rows", "sbt_scatter_rows_masked", "sbt_ragged_tile_load", "sbt_gemm_bounded_workspace_size",
-           "sbt_gemm_bounded")
+           "sbt_gemm_bounded", "sbt_gemm_bounded_noalloc")
+GEMM_NOALLOC_SCRATCH_BYTES = 16 << 20  # SBT_GEMM_NOALLOC_SCRATCH_BYTES in include/sbt.h
 
 
 class SbtError(RuntimeError):
@@ -69,6 +70,7 @@ def load_library(path: str = LIB_PATH):
             "sbt_ragged_tile_load": [p, ci, p, i64, i32, i32, i64, i64, p, i32, i32, p, p],
             "sbt_gemm_bounded_workspace_size": [p, i64, i64, i64, i64, i64, ctypes.POINTER(ctypes.c_size_t)],
             "sbt_gemm_bounded": [p, p, i64, p, i64, p, i64, ci, i64, i64, i64, p, ctypes.c_size_t, p],
+            "sbt_gemm_bounded_noalloc": [p, p, i64, p, i64, p, i64, ci, i64, i64, i64, p],
         }
         for name, args in sig.items():
             f = getattr(lib, name)
@@ -222,3 +224,17 @@ def gemm_bounded(ctx, A, lda, B, ldb, C, ldc, M, N, K, workspace=None, workspace
     code = {"bf16": SBT_BF16, "f32": SBT_F32}[c_dtype] if isinstance(c_dtype, str) else int(c_dtype)
     _check(load_library().sbt_gemm_bounded(ctx.handle, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, code, M, N, K,
                                            _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def gemm_bounded_noalloc(ctx, A, lda, B, ldb, C, ldc, M, N, K, c_dtype="bf16", stream=None):
+    """sbt_gemm_bounded_noalloc: the bounded GEMM with the library's fixed staging scratch.
+
+    For callers that cannot allocate device memory at the call (inside a CUDA
+    graph capture, inside another framework's memory pool, or on paths that
+    cannot take cudaMalloc's implicit synchronisation).  Shapes needing more
+    than GEMM_NOALLOC_SCRATCH_BYTES of staging are rejected; calls that may
+    overlap on the GPU race on the shared scratch.
+    """
+    code = {"bf16": SBT_BF16, "f32": SBT_F32}[c_dtype] if isinstance(c_dtype, str) else int(c_dtype)
+    _check(load_library().sbt_gemm_bounded_noalloc(ctx.handle, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, code, M, N,
+                                                   K, _stream(stream)))
