@@ -105,6 +105,14 @@ class Dist:
             self.pg.destroy_process_group()
 
 
+def aggregate(dist, bytes_per_step: float, ms_total: float, steps: int):
+    """Whole-job GB/s over all ranks: every rank's bytes / the slowest rank's time.
+    Returns (GB/s, max ms over ranks)."""
+    ms_max = dist.max(ms_total)
+    total_bytes = dist.sum(float(bytes_per_step)) * steps
+    return total_bytes / (ms_max / 1e3) / 1e9, ms_max
+
+
 # ----------------------------------------------------------------------------- clocks
 
 class ClockSampler:
@@ -394,9 +402,7 @@ def run_sbt(args, dist):
     launches = ctx.launch_count - launches0
     sampler.stop()
     ms_total = ev0.elapsed_time(ev1)
-    ms_max = dist.max(ms_total)
-    total_bytes = dist.sum(float(bytes_step)) * args.steps
-    value = total_bytes / (ms_max / 1e3) / 1e9
+    value, ms_max = aggregate(dist, bytes_step, ms_total, args.steps)
     ms_step = ms_max / args.steps
     achieved = bytes_step / (ms_total / args.steps / 1e3) / 1e9  # this rank's kernel, per launch
     ctx.check_status()
