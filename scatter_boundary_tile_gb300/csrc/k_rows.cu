@@ -2,9 +2,10 @@
 //
 // Both kernels are persistent: the grid is (SMs x resident blocks), and each
 // block walks chunks of kChunkRows indices.  A chunk's indices are staged in
-// shared memory by one warp, which also checks every row against the array
-// bounds (64-bit, offset added first -- warp.tile_load_indexed, description)
-// and builds the chunk's row-valid mask with a warp ballot.  The block then
+// shared memory (double-buffered) by one warp, which also checks every row
+// against the array bounds (64-bit, offset added first --
+// warp.tile_load_indexed, description) and builds the chunk's row-valid mask
+// with a warp ballot.  The block then
 // moves the chunk's rows with 16-byte vectors (when the host has checked that
 // every vector address is 16-byte aligned) or element by element.
 //
@@ -37,24 +38,27 @@ struct RowParams {
     uint32_t pad_word;
 };
 
-// Stage up to kChunkRows indices: s_row[i] = row_offset + idx[k0 + i], and a
-// ballot mask of the rows inside [0, rows).
-__device__ __forceinline__ uint32_t stage_index_chunk(const RowParams& p, int64_t k0, int nrows, int64_t* s_row,
-                                                      uint32_t* s_valid) {
-    if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        int64_t r = -1;
-        bool v = false;
-        if (lane < nrows) {
-            r = (int64_t)__ldg(p.idx + k0 + lane) + p.row_offset;
-            v = r >= 0 && r < p.rows;
-        }
-        const uint32_t ballot = __ballot_sync(0xffffffffu, v);
-        s_row[lane] = r;
-        if (lane == 0) *s_valid = ballot;
-    }
-    __syncthreads();
-    return *s_valid;
+// Index staging, double-buffered across chunks.  Warp 0 issues the loads of
+// the next chunk's indices before the block moves the current chunk, and
+// finishes staging them (row = row_offset + idx in 64-bit, bounds check,
+// ballot of the rows inside [0, rows)) afterwards, so their latency hides
+// behind the data movement.
+__device__ __forceinline__ int32_t issue_index_load(const RowParams& p, int64_t chunk, int64_t nchunks) {
+    const int lane = threadIdx.x & 31;
+    const int64_t k = chunk * kChunkRows + lane;
+    return (chunk < nchunks && k < p.n_idx) ? __ldg(p.idx + k) : 0;
+}
+
+__device__ __forceinline__ void finish_index_stage(const RowParams& p, int64_t chunk, int64_t nchunks, int32_t raw,
+                                                   int64_t* s_row, uint32_t* s_valid) {
+    const int lane = threadIdx.x & 31;
+    const int64_t k = chunk * kChunkRows + lane;
+    const bool present = chunk < nchunks && k < p.n_idx;
+    const int64_t r = present ? (int64_t)raw + p.row_offset : -1;
+    const bool v = present && r >= 0 && r < p.rows;
+    const uint32_t ballot = __ballot_sync(0xffffffffu, v);
+    s_row[lane] = r;
+    if (lane == 0) *s_valid = ballot;
 }
 
 // Bit e set <=> mask element e of the vector starting at column j0 of row k is true.
@@ -128,15 +132,22 @@ __device__ __forceinline__ uint4 gather_vector(const RowParams& p, int64_t k, in
 
 template <int ES, bool VEC, int MM>
 __global__ void __launch_bounds__(kThreads) k_gather_rows(const RowParams p) {
-    __shared__ int64_t s_row[kChunkRows];
-    __shared__ uint32_t s_valid;
+    __shared__ int64_t s_row[2][kChunkRows];
+    __shared__ uint32_t s_valid[2];
     constexpr int V = 16 / ES;
     typedef typename sbt_elem<ES>::T T;
     const int64_t nchunks = (p.n_idx + kChunkRows - 1) / kChunkRows;
-    for (int64_t chunk = blockIdx.x; chunk < nchunks; chunk += gridDim.x) {
+    const bool stager = threadIdx.x < 32;
+    if (stager) finish_index_stage(p, blockIdx.x, nchunks, issue_index_load(p, blockIdx.x, nchunks), s_row[0], &s_valid[0]);
+    __syncthreads();
+    int buf = 0;
+    for (int64_t chunk = blockIdx.x; chunk < nchunks; chunk += gridDim.x, buf ^= 1) {
+        const int64_t next = chunk + gridDim.x;
+        const int32_t next_raw = stager ? issue_index_load(p, next, nchunks) : 0;
         const int64_t k0 = chunk * kChunkRows;
         const int nrows = (int)(p.n_idx - k0 < kChunkRows ? p.n_idx - k0 : kChunkRows);
-        const uint32_t valid = stage_index_chunk(p, k0, nrows, s_row, &s_valid);
+        const uint32_t valid = s_valid[buf];
+        const int64_t* rows_of = s_row[buf];
         if (VEC) {
             const int nvec = p.nvec;
             const int ntask = nrows * nvec;
@@ -148,7 +159,7 @@ __global__ void __launch_bounds__(kThreads) k_gather_rows(const RowParams p) {
                     if (t < ntask) {
                         const int row = t / nvec;
                         const int vc = t - row * nvec;
-                        val[u] = gather_vector<ES, MM>(p, k0 + row, s_row[row], (valid >> row) & 1u, vc);
+                        val[u] = gather_vector<ES, MM>(p, k0 + row, rows_of[row], (valid >> row) & 1u, vc);
                     }
                 }
 #pragma unroll
@@ -176,7 +187,7 @@ __global__ void __launch_bounds__(kThreads) k_gather_rows(const RowParams p) {
                         const int64_t c = p.col_offset + j;
                         const bool m = MM == kNoMask ? true : __ldg(p.mask + (k0 + row) * p.ld_mask + j) != 0;
                         if (((valid >> row) & 1u) && m && c >= 0 && c < p.cols)
-                            val[u] = ld_elem<ES>(p.src, s_row[row] * p.ld_arr + c);
+                            val[u] = ld_elem<ES>(p.src, rows_of[row] * p.ld_arr + c);
                     }
                 }
 #pragma unroll
@@ -190,6 +201,7 @@ __global__ void __launch_bounds__(kThreads) k_gather_rows(const RowParams p) {
                 }
             }
         }
+        if (stager) finish_index_stage(p, next, nchunks, next_raw, s_row[buf ^ 1], &s_valid[buf ^ 1]);
         __syncthreads();
     }
 }
@@ -198,22 +210,31 @@ __global__ void __launch_bounds__(kThreads) k_gather_rows(const RowParams p) {
 
 template <int ES, bool VEC, int MM>
 __global__ void __launch_bounds__(kThreads) k_scatter_rows(const RowParams p) {
-    __shared__ int64_t s_row[kChunkRows];
-    __shared__ uint32_t s_valid;
+    __shared__ int64_t s_row[2][kChunkRows];
+    __shared__ uint32_t s_valid[2];
     constexpr int V = 16 / ES;
     constexpr uint32_t kAll = (1u << V) - 1u;
     typedef typename sbt_elem<ES>::T T;
     const int64_t nchunks = (p.n_idx + kChunkRows - 1) / kChunkRows;
-    for (int64_t chunk = blockIdx.x; chunk < nchunks; chunk += gridDim.x) {
+    const bool stager = threadIdx.x < 32;
+    if (stager) finish_index_stage(p, blockIdx.x, nchunks, issue_index_load(p, blockIdx.x, nchunks), s_row[0], &s_valid[0]);
+    __syncthreads();
+    int buf = 0;
+    for (int64_t chunk = blockIdx.x; chunk < nchunks; chunk += gridDim.x, buf ^= 1) {
+        const int64_t next = chunk + gridDim.x;
+        const int32_t next_raw = stager ? issue_index_load(p, next, nchunks) : 0;
         const int64_t k0 = chunk * kChunkRows;
         const int nrows = (int)(p.n_idx - k0 < kChunkRows ? p.n_idx - k0 : kChunkRows);
-        const uint32_t valid = stage_index_chunk(p, k0, nrows, s_row, &s_valid);
+        const uint32_t valid = s_valid[buf];
+        const int64_t* rows_of = s_row[buf];
         if (VEC) {
             const int nvec = p.nvec;
             const int ntask = nrows * nvec;
             for (int base = threadIdx.x; base < ntask; base += kThreads * kUnroll) {
                 uint4 val[kUnroll];
                 uint32_t mb[kUnroll];
+                // Source vector and mask bits are loaded side by side (no dependence
+                // between them); a vector whose row or columns lie outside is skipped.
 #pragma unroll
                 for (int u = 0; u < kUnroll; ++u) {
                     const int t = base + u * kThreads;
@@ -221,13 +242,11 @@ __global__ void __launch_bounds__(kThreads) k_scatter_rows(const RowParams p) {
                     if (t < ntask) {
                         const int row = t / nvec;
                         const int vc = t - row * nvec;
-                        if ((valid >> row) & 1u) {
-                            const int64_t j0 = (int64_t)vc * V;
-                            const int64_t c0 = p.col_offset + j0;
-                            if (c0 + V > 0 && c0 < p.cols) {
-                                mb[u] = mask_bits<ES, MM>(p, k0 + row, j0);
-                                if (mb[u]) val[u] = sbt_ld_nc_v4(p.src + ((k0 + row) * p.ld_dense + j0) * ES);
-                            }
+                        const int64_t j0 = (int64_t)vc * V;
+                        const int64_t c0 = p.col_offset + j0;
+                        if (((valid >> row) & 1u) && c0 + V > 0 && c0 < p.cols) {
+                            val[u] = sbt_ld_nc_v4(p.src + ((k0 + row) * p.ld_dense + j0) * ES);
+                            mb[u] = mask_bits<ES, MM>(p, k0 + row, j0);
                         }
                     }
                 }
@@ -238,7 +257,7 @@ __global__ void __launch_bounds__(kThreads) k_scatter_rows(const RowParams p) {
                     const int row = t / nvec;
                     const int vc = t - row * nvec;
                     const int64_t c0 = p.col_offset + (int64_t)vc * V;
-                    char* drow = p.dst + s_row[row] * p.ld_arr * ES;
+                    char* drow = p.dst + rows_of[row] * p.ld_arr * ES;
                     if (mb[u] == kAll && c0 >= 0 && c0 + V <= p.cols) {
                         sbt_st_v4(drow + c0 * ES, val[u]);
                     } else {
@@ -266,8 +285,8 @@ __global__ void __launch_bounds__(kThreads) k_scatter_rows(const RowParams p) {
                         const int j = t - row * tc;
                         const int64_t c = p.col_offset + j;
                         if (((valid >> row) & 1u) && c >= 0 && c < p.cols) {
+                            val[u] = ld_elem<ES>(p.src, (k0 + row) * p.ld_dense + j);
                             ok[u] = MM == kNoMask ? true : __ldg(p.mask + (k0 + row) * p.ld_mask + j) != 0;
-                            if (ok[u]) val[u] = ld_elem<ES>(p.src, (k0 + row) * p.ld_dense + j);
                         }
                     }
                 }
@@ -277,10 +296,11 @@ __global__ void __launch_bounds__(kThreads) k_scatter_rows(const RowParams p) {
                     const int t = base + u * kThreads;
                     const int row = t / tc;
                     const int j = t - row * tc;
-                    st_elem<ES>(p.dst, s_row[row] * p.ld_arr + p.col_offset + j, val[u]);
+                    st_elem<ES>(p.dst, rows_of[row] * p.ld_arr + p.col_offset + j, val[u]);
                 }
             }
         }
+        if (stager) finish_index_stage(p, next, nchunks, next_raw, s_row[buf ^ 1], &s_valid[buf ^ 1]);
         __syncthreads();
     }
 }

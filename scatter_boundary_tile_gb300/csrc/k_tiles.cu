@@ -20,37 +20,51 @@
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kUnroll = 4;
+
+// Copy paths of the tile kernels (chosen per call on the host):
+//   kAligned -- every vector of the call is 16-byte aligned on both sides;
+//   kRealign -- the tile side is aligned, the array's rows are not: a vector
+//               of the array is assembled from the two aligned 16-byte chunks
+//               that cover it (only when both chunks lie inside the array's
+//               byte span, so nothing outside the caller's buffer is read);
+//   kElem    -- element by element (column stride != 1, odd tile widths, or
+//               unaligned stores).
+enum TileMode { kAligned = 0, kRealign = 1, kElem = 2 };
 
 struct TileParams {
-    const char* arr;  // load: source array; store: unused
-    char* arr_w;      // store: destination array
+    const char* arr;      // load: source array
+    char* arr_w;          // store: destination array
     const char* tiles_r;  // store: source tiles
     char* tiles_w;        // load: destination tiles
     int64_t rows, cols, stride_r, stride_c, origin_r, origin_c, step_r, step_c;
     int32_t grid_c, tile_r, tile_c;
-    int32_t nvc;       // vectors per tile row (vector path)
-    int64_t total;     // tasks: vectors (vector path) or elements
+    uint32_t per_row;      // tasks per tile row: vectors or elements
+    uint32_t per_tile;     // tile_r * per_row
+    sbt_fastdiv div_per_tile, div_per_row, div_grid_c;
+    uint32_t tile0;        // first tile of this launch
+    uint32_t ntasks;       // tasks of this launch (< 2^31)
     uint32_t pad_word;
+    uint64_t arr_lo, arr_hi;  // byte span [lo, hi) of the array (realign path)
 };
 
 struct TaskPos {
-    int64_t r, c;  // array coordinates of the task's first element
+    int64_t r, c;      // array coordinates of the task's first element
+    int64_t linear;    // index of the task in the whole contiguous tile array
 };
 
-// Task t of the contiguous tile side -> array coordinates.  `per_row` is the
-// number of tasks per tile row and `w` the elements each task covers.
-__device__ __forceinline__ TaskPos tile_task_pos(const TileParams& p, int64_t t, int per_row, int w) {
-    const int64_t per_tile = (int64_t)p.tile_r * per_row;
-    const int64_t tile = t / per_tile;
-    const int within = (int)(t - tile * per_tile);
-    const int i = within / per_row;
-    const int j = (within - i * per_row) * w;
-    const int64_t ti = tile / p.grid_c;
-    const int64_t tj = tile - ti * p.grid_c;
+// Task t of this launch -> array coordinates, with 32-bit multiply-shift divisions.
+__device__ __forceinline__ TaskPos tile_task_pos(const TileParams& p, uint32_t t, int w) {
+    const uint32_t tile_rel = sbt_div(p.div_per_tile, t);
+    const uint32_t within = t - tile_rel * p.per_tile;
+    const uint32_t i = sbt_div(p.div_per_row, within);
+    const uint32_t j = (within - i * p.per_row) * (uint32_t)w;
+    const uint32_t tile = p.tile0 + tile_rel;
+    const uint32_t ti = sbt_div(p.div_grid_c, tile);
+    const uint32_t tj = tile - ti * (uint32_t)p.grid_c;
     TaskPos q;
-    q.r = p.origin_r + ti * p.step_r + i;
-    q.c = p.origin_c + tj * p.step_c + j;
+    q.r = p.origin_r + (int64_t)ti * p.step_r + i;
+    q.c = p.origin_c + (int64_t)tj * p.step_c + j;
+    q.linear = (int64_t)p.tile0 * p.per_tile + t;
     return q;
 }
 
@@ -64,24 +78,66 @@ __device__ __forceinline__ void st_elem(char* base, int64_t off, typename sbt_el
     reinterpret_cast<typename sbt_elem<ES>::T*>(base)[off] = v;
 }
 
-template <int ES, bool VEC>
+__device__ __forceinline__ uint32_t pick8(const uint32_t (&w)[8], uint32_t i) {
+    uint32_t r = w[0];
+#pragma unroll
+    for (uint32_t k = 1; k < 8; ++k) r = (i == k) ? w[k] : r;
+    return r;
+}
+
+// Bytes [s, s + 16) of the 32 bytes (lo, hi), 0 < s < 16.
+__device__ __forceinline__ uint4 realign16(const uint4& lo, const uint4& hi, uint32_t s) {
+    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+    const uint32_t q = s >> 2, b = (s & 3u) * 8u;
+    uint4 r;
+    r.x = __funnelshift_r(pick8(w, q), pick8(w, q + 1), b);
+    r.y = __funnelshift_r(pick8(w, q + 1), pick8(w, q + 2), b);
+    r.z = __funnelshift_r(pick8(w, q + 2), pick8(w, q + 3), b);
+    r.w = __funnelshift_r(pick8(w, q + 3), pick8(w, q + 4), b);
+    return r;
+}
+
+// One 16-byte vector of array row r starting at column c (the whole vector in bounds).
+template <int ES, int MODE>
+__device__ __forceinline__ uint4 load_row_vector(const TileParams& p, int64_t r, int64_t c) {
+    const char* a = p.arr + (r * p.stride_r + c) * ES;
+    if (MODE == kAligned) return sbt_ld_nc_v4(a);
+    const uint64_t addr = reinterpret_cast<uint64_t>(a);
+    const uint32_t s = (uint32_t)(addr & 15u);
+    if (s == 0) return sbt_ld_nc_v4(a);
+    const uint64_t base = addr - s;
+    if (base >= p.arr_lo && base + 32 <= p.arr_hi) {
+        const uint4 lo = sbt_ld_nc_v4_l1(reinterpret_cast<const void*>(base));
+        const uint4 hi = sbt_ld_nc_v4_l1(reinterpret_cast<const void*>(base + 16));
+        return realign16(lo, hi, s);
+    }
+    uint4 v = make_uint4(0, 0, 0, 0);
+#pragma unroll
+    for (int e = 0; e < 16 / ES; ++e) sbt_vec_set<ES>(v, e, ld_elem<ES>(p.arr, r * p.stride_r + c + e));
+    return v;
+}
+
+template <int ES, int MODE>
 __global__ void __launch_bounds__(kThreads) k_tile_load(const TileParams p) {
     constexpr int V = 16 / ES;
+    constexpr int U = MODE == kElem ? 8 : 4;
     typedef typename sbt_elem<ES>::T T;
-    const int64_t stride = (int64_t)gridDim.x * kThreads;
-    for (int64_t base = (int64_t)blockIdx.x * kThreads + threadIdx.x; base < p.total; base += stride * kUnroll) {
-        if (VEC) {
-            uint4 val[kUnroll];
+    const uint32_t stride = gridDim.x * kThreads;
+    for (uint32_t base = blockIdx.x * kThreads + threadIdx.x; base < p.ntasks; base += stride * U) {
+        if (MODE != kElem) {
+            uint4 val[U];
+            int64_t lin[U];
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int64_t t = base + u * stride;
-                const uint4 padv = make_uint4(p.pad_word, p.pad_word, p.pad_word, p.pad_word);
-                val[u] = padv;
-                if (t < p.total) {
-                    const TaskPos q = tile_task_pos(p, t, p.nvc, V);
+            for (int u = 0; u < U; ++u) {
+                const uint32_t t = base + u * stride;
+                val[u] = make_uint4(p.pad_word, p.pad_word, p.pad_word, p.pad_word);
+                lin[u] = -1;
+                if (t < p.ntasks) {
+                    const TaskPos q = tile_task_pos(p, t, V);
+                    lin[u] = q.linear;
                     if (q.r >= 0 && q.r < p.rows) {
                         if (q.c >= 0 && q.c + V <= p.cols) {
-                            val[u] = sbt_ld_nc_v4(p.arr + (q.r * p.stride_r + q.c) * ES);
+                            val[u] = load_row_vector<ES, MODE>(p, q.r, q.c);
                         } else if (q.c + V > 0 && q.c < p.cols) {
 #pragma unroll
                             for (int e = 0; e < V; ++e) {
@@ -94,49 +150,49 @@ __global__ void __launch_bounds__(kThreads) k_tile_load(const TileParams p) {
                 }
             }
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int64_t t = base + u * stride;
-                if (t < p.total) sbt_st_v4(p.tiles_w + t * 16, val[u]);
-            }
+            for (int u = 0; u < U; ++u)
+                if (lin[u] >= 0) sbt_st_v4(p.tiles_w + lin[u] * 16, val[u]);
         } else {
-            T val[kUnroll];
+            T val[U];
+            int64_t lin[U];
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int64_t t = base + u * stride;
+            for (int u = 0; u < U; ++u) {
+                const uint32_t t = base + u * stride;
                 val[u] = (T)p.pad_word;
-                if (t < p.total) {
-                    const TaskPos q = tile_task_pos(p, t, p.tile_c, 1);
+                lin[u] = -1;
+                if (t < p.ntasks) {
+                    const TaskPos q = tile_task_pos(p, t, 1);
+                    lin[u] = q.linear;
                     if (q.r >= 0 && q.r < p.rows && q.c >= 0 && q.c < p.cols)
                         val[u] = ld_elem<ES>(p.arr, q.r * p.stride_r + q.c * p.stride_c);
                 }
             }
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int64_t t = base + u * stride;
-                if (t < p.total) st_elem<ES>(p.tiles_w, t, val[u]);
-            }
+            for (int u = 0; u < U; ++u)
+                if (lin[u] >= 0) st_elem<ES>(p.tiles_w, lin[u], val[u]);
         }
     }
 }
 
-template <int ES, bool VEC>
+template <int ES, int MODE>
 __global__ void __launch_bounds__(kThreads) k_tile_store(const TileParams p) {
     constexpr int V = 16 / ES;
+    constexpr int U = MODE == kElem ? 8 : 4;
     typedef typename sbt_elem<ES>::T T;
-    const int64_t stride = (int64_t)gridDim.x * kThreads;
-    for (int64_t base = (int64_t)blockIdx.x * kThreads + threadIdx.x; base < p.total; base += stride * kUnroll) {
-        if (VEC) {
-            uint4 val[kUnroll];
+    const uint32_t stride = gridDim.x * kThreads;
+    for (uint32_t base = blockIdx.x * kThreads + threadIdx.x; base < p.ntasks; base += stride * U) {
+        if (MODE != kElem) {
+            uint4 val[U];
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int64_t t = base + u * stride;
-                if (t < p.total) val[u] = sbt_ld_nc_v4(p.tiles_r + t * 16);
+            for (int u = 0; u < U; ++u) {
+                const uint32_t t = base + u * stride;
+                if (t < p.ntasks) val[u] = sbt_ld_nc_v4(p.tiles_r + ((int64_t)p.tile0 * p.per_tile + t) * 16);
             }
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int64_t t = base + u * stride;
-                if (t >= p.total) continue;
-                const TaskPos q = tile_task_pos(p, t, p.nvc, V);
+            for (int u = 0; u < U; ++u) {
+                const uint32_t t = base + u * stride;
+                if (t >= p.ntasks) continue;
+                const TaskPos q = tile_task_pos(p, t, V);
                 if (q.r < 0 || q.r >= p.rows) continue;
                 if (q.c >= 0 && q.c + V <= p.cols) {
                     sbt_st_v4(p.arr_w + (q.r * p.stride_r + q.c) * ES, val[u]);
@@ -149,17 +205,17 @@ __global__ void __launch_bounds__(kThreads) k_tile_store(const TileParams p) {
                 }
             }
         } else {
-            T val[kUnroll];
+            T val[U];
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int64_t t = base + u * stride;
-                if (t < p.total) val[u] = ld_elem<ES>(p.tiles_r, t);
+            for (int u = 0; u < U; ++u) {
+                const uint32_t t = base + u * stride;
+                if (t < p.ntasks) val[u] = ld_elem<ES>(p.tiles_r, (int64_t)p.tile0 * p.per_tile + t);
             }
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
-                const int64_t t = base + u * stride;
-                if (t >= p.total) continue;
-                const TaskPos q = tile_task_pos(p, t, p.tile_c, 1);
+            for (int u = 0; u < U; ++u) {
+                const uint32_t t = base + u * stride;
+                if (t >= p.ntasks) continue;
+                const TaskPos q = tile_task_pos(p, t, 1);
                 if (q.r >= 0 && q.r < p.rows && q.c >= 0 && q.c < p.cols)
                     st_elem<ES>(p.arr_w, q.r * p.stride_r + q.c * p.stride_c, val[u]);
             }
@@ -231,20 +287,20 @@ __global__ void __launch_bounds__(kThreads) k_ragged_load(const RaggedParams p) 
     }
 }
 
-template <int ES, bool VEC>
-sbt_status launch_tile_load_t(sbt_context* ctx, const TileParams& p, cudaStream_t s) {
-    auto kern = k_tile_load<ES, VEC>;
-    const int grid = sbt_persistent_grid(ctx, (const void*)kern, kThreads, 0, sbt_cdiv(p.total, kThreads));
-    kern<<<grid, kThreads, 0, s>>>(p);
-    return sbt_after_launch(ctx, "tile_load_padded");
-}
-
-template <int ES, bool VEC>
-sbt_status launch_tile_store_t(sbt_context* ctx, const TileParams& p, cudaStream_t s) {
-    auto kern = k_tile_store<ES, VEC>;
-    const int grid = sbt_persistent_grid(ctx, (const void*)kern, kThreads, 0, sbt_cdiv(p.total, kThreads));
-    kern<<<grid, kThreads, 0, s>>>(p);
-    return sbt_after_launch(ctx, "tile_store_clipped");
+// Launches `kern` over all tiles, splitting so that each launch has fewer than 2^31 tasks.
+template <typename Kern>
+sbt_status launch_tiles(sbt_context* ctx, Kern kern, TileParams p, int64_t ntiles, const char* what, cudaStream_t s) {
+    const int64_t max_tiles = ((int64_t)1 << 31) / 2 / p.per_tile;
+    for (int64_t t0 = 0; t0 < ntiles; t0 += max_tiles) {
+        const int64_t nt = ntiles - t0 < max_tiles ? ntiles - t0 : max_tiles;
+        p.tile0 = (uint32_t)t0;
+        p.ntasks = (uint32_t)(nt * p.per_tile);
+        const int grid = sbt_persistent_grid(ctx, (const void*)kern, kThreads, 0, sbt_cdiv(p.ntasks, kThreads));
+        kern<<<grid, kThreads, 0, s>>>(p);
+        sbt_status st = sbt_after_launch(ctx, what);
+        if (st) return st;
+    }
+    return SBT_OK;
 }
 
 template <int ES, bool VEC>
@@ -267,10 +323,10 @@ bool tiles_vector_ok(int es, const void* arr, int64_t stride_r, int64_t stride_c
     return true;
 }
 
-TileParams make_tile_params(int64_t rows, int64_t cols, int64_t stride_r, int64_t stride_c, int64_t origin_r,
-                            int64_t origin_c, int64_t step_r, int64_t step_c, int32_t grid_r, int32_t grid_c,
-                            int32_t tile_r, int32_t tile_c, bool vec, int es) {
-    TileParams p;
+sbt_status make_tile_params(TileParams* pp, int64_t rows, int64_t cols, int64_t stride_r, int64_t stride_c,
+                            int64_t origin_r, int64_t origin_c, int64_t step_r, int64_t step_c, int32_t grid_r,
+                            int32_t grid_c, int32_t tile_r, int32_t tile_c, bool vec, int es, int64_t* ntiles) {
+    TileParams& p = *pp;
     p.arr = nullptr;
     p.arr_w = nullptr;
     p.tiles_r = nullptr;
@@ -286,11 +342,23 @@ TileParams make_tile_params(int64_t rows, int64_t cols, int64_t stride_r, int64_
     p.grid_c = grid_c;
     p.tile_r = tile_r;
     p.tile_c = tile_c;
-    p.nvc = vec ? tile_c / (16 / es) : 0;
-    const int64_t elems = (int64_t)grid_r * grid_c * tile_r * tile_c;
-    p.total = vec ? elems / (16 / es) : elems;
+    p.per_row = vec ? (uint32_t)(tile_c / (16 / es)) : (uint32_t)tile_c;
+    p.per_tile = (uint32_t)tile_r * p.per_row;
+    p.div_per_tile = sbt_make_fastdiv(p.per_tile);
+    p.div_per_row = sbt_make_fastdiv(p.per_row);
+    p.div_grid_c = sbt_make_fastdiv((uint32_t)grid_c);
+    p.tile0 = 0;
+    p.ntasks = 0;
     p.pad_word = 0;
-    return p;
+    p.arr_lo = p.arr_hi = 0;
+    *ntiles = (int64_t)grid_r * grid_c;
+    if (*ntiles >= ((int64_t)1 << 31)) return sbt_fail(SBT_ERR_UNSUPPORTED, "tile grid with 2^31 or more tiles");
+    return SBT_OK;
+}
+
+// The realign path: column stride 1, rows moving forward, the tile side aligned.
+bool tiles_realign_ok(int es, int64_t stride_r, int64_t stride_c, int32_t tile_c, const void* tiles) {
+    return stride_c == 1 && stride_r > 0 && tile_c % (16 / es) == 0 && sbt_aligned16(tiles);
 }
 
 }  // namespace
@@ -299,30 +367,56 @@ sbt_status sbt_launch_tile_load(sbt_context* ctx, int es, const void* src, int64
                                 int64_t stride_r, int64_t stride_c, int64_t origin_r, int64_t origin_c,
                                 int64_t step_r, int64_t step_c, int32_t grid_r, int32_t grid_c, int32_t tile_r,
                                 int32_t tile_c, void* dst, uint32_t pad_word, cudaStream_t stream) {
-    bool vec = tiles_vector_ok(es, src, stride_r, stride_c, origin_c, step_c, grid_c, tile_c, dst);
-    if (ctx->path == SBT_PATH_SCALAR) vec = false;
-    TileParams p = make_tile_params(src ? rows : 0, src ? cols : 0, stride_r, stride_c, origin_r, origin_c, step_r,
-                                    step_c, grid_r, grid_c, tile_r, tile_c, vec, es);
+    if (!src) rows = cols = 0;  // an empty array: every element is padding
+    int mode = tiles_vector_ok(es, src, stride_r, stride_c, origin_c, step_c, grid_c, tile_c, dst) ? kAligned
+               : (src && tiles_realign_ok(es, stride_r, stride_c, tile_c, dst)) ? kRealign
+                                                                                : kElem;
+    if (ctx->path == SBT_PATH_SCALAR) mode = kElem;
+    TileParams p;
+    int64_t ntiles = 0;
+    sbt_status st = make_tile_params(&p, rows, cols, stride_r, stride_c, origin_r, origin_c, step_r, step_c, grid_r,
+                                     grid_c, tile_r, tile_c, mode != kElem, es, &ntiles);
+    if (st) return st;
     p.arr = (const char*)src;
     p.tiles_w = (char*)dst;
     p.pad_word = pad_word;
-    if (es == 4) return vec ? launch_tile_load_t<4, true>(ctx, p, stream) : launch_tile_load_t<4, false>(ctx, p, stream);
-    return vec ? launch_tile_load_t<2, true>(ctx, p, stream) : launch_tile_load_t<2, false>(ctx, p, stream);
+    if (mode == kRealign) {
+        p.arr_lo = reinterpret_cast<uint64_t>(src);
+        p.arr_hi = p.arr_lo + (uint64_t)(((rows > 0 ? rows - 1 : 0) * stride_r + cols) * es);
+    }
+    const char* what = "tile_load_padded";
+#define SBT_TL(ES_, M_) return launch_tiles(ctx, k_tile_load<ES_, M_>, p, ntiles, what, stream)
+    if (es == 4) {
+        if (mode == kAligned) SBT_TL(4, kAligned);
+        if (mode == kRealign) SBT_TL(4, kRealign);
+        SBT_TL(4, kElem);
+    }
+    if (mode == kAligned) SBT_TL(2, kAligned);
+    if (mode == kRealign) SBT_TL(2, kRealign);
+    SBT_TL(2, kElem);
+#undef SBT_TL
 }
 
 sbt_status sbt_launch_tile_store(sbt_context* ctx, int es, const void* src_tiles, int32_t grid_r, int32_t grid_c,
                                  int32_t tile_r, int32_t tile_c, void* dst, int64_t rows, int64_t cols,
                                  int64_t stride_r, int64_t stride_c, int64_t origin_r, int64_t origin_c,
                                  int64_t step_r, int64_t step_c, cudaStream_t stream) {
-    bool vec = tiles_vector_ok(es, dst, stride_r, stride_c, origin_c, step_c, grid_c, tile_c, src_tiles);
-    if (ctx->path == SBT_PATH_SCALAR) vec = false;
-    TileParams p = make_tile_params(rows, cols, stride_r, stride_c, origin_r, origin_c, step_r, step_c, grid_r,
-                                    grid_c, tile_r, tile_c, vec, es);
+    int mode = tiles_vector_ok(es, dst, stride_r, stride_c, origin_c, step_c, grid_c, tile_c, src_tiles) ? kAligned
+                                                                                                         : kElem;
+    if (ctx->path == SBT_PATH_SCALAR) mode = kElem;
+    TileParams p;
+    int64_t ntiles = 0;
+    sbt_status st = make_tile_params(&p, rows, cols, stride_r, stride_c, origin_r, origin_c, step_r, step_c, grid_r,
+                                     grid_c, tile_r, tile_c, mode != kElem, es, &ntiles);
+    if (st) return st;
     p.arr_w = (char*)dst;
     p.tiles_r = (const char*)src_tiles;
+    const char* what = "tile_store_clipped";
     if (es == 4)
-        return vec ? launch_tile_store_t<4, true>(ctx, p, stream) : launch_tile_store_t<4, false>(ctx, p, stream);
-    return vec ? launch_tile_store_t<2, true>(ctx, p, stream) : launch_tile_store_t<2, false>(ctx, p, stream);
+        return mode == kAligned ? launch_tiles(ctx, k_tile_store<4, kAligned>, p, ntiles, what, stream)
+                                : launch_tiles(ctx, k_tile_store<4, kElem>, p, ntiles, what, stream);
+    return mode == kAligned ? launch_tiles(ctx, k_tile_store<2, kAligned>, p, ntiles, what, stream)
+                            : launch_tiles(ctx, k_tile_store<2, kElem>, p, ntiles, what, stream);
 }
 
 sbt_status sbt_launch_ragged(sbt_context* ctx, int es, const void* x, int64_t total_rows, int32_t heads,

@@ -100,9 +100,42 @@ __device__ __forceinline__ uint4 sbt_ld_nc_v4(const void* p) {
     return v;
 }
 
+// Read-only 16-byte load that may allocate in L1 (neighbouring tasks reuse it).
+__device__ __forceinline__ uint4 sbt_ld_nc_v4_l1(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ void sbt_st_v4(void* p, uint4 v) {
     asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
+}
+
+// n / d for 0 <= n < 2^31 by one 64-bit multiply and a shift (division by an
+// invariant integer, Granlund & Montgomery 1994): with s = ceil(log2 d) and
+// m = ceil(2^(32+s) / d), floor(n * m / 2^(32+s)) = floor(n / d) because the
+// rounding error of m contributes less than 2^-(1+s) <= 1/(2d).
+struct sbt_fastdiv {
+    uint32_t d;
+    uint32_t shift;
+    uint64_t mul;
+};
+
+inline sbt_fastdiv sbt_make_fastdiv(uint32_t d) {
+    sbt_fastdiv f;
+    uint32_t s = 0;
+    while ((1ull << s) < d) ++s;
+    f.d = d;
+    f.shift = 32 + s;
+    f.mul = ((1ull << f.shift) + d - 1) / d;
+    return f;
+}
+
+__device__ __forceinline__ uint32_t sbt_div(const sbt_fastdiv& f, uint32_t n) {
+    return (uint32_t)(((uint64_t)n * f.mul) >> f.shift);
 }
 
 // Element e (0..16/ES-1) of a 16-byte vector.
