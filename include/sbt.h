@@ -72,6 +72,13 @@ SBT_API sbt_status sbt_destroy(sbt_context* ctx);
 SBT_API sbt_status sbt_set_path(sbt_context* ctx, sbt_path path);
 /* Limit of every bounded device-side wait, in nanoseconds (default 2e9). */
 SBT_API sbt_status sbt_set_wait_limit_ns(sbt_context* ctx, uint64_t ns);
+/* Test hook for the bounded device waits.  SBT_TEST_WITHHOLD_LOAD makes the
+ * next GEMM and bulk row launches on this context skip their first copy, so
+ * a consumer's bounded wait runs out (no fault, no hang): the kernel sets the
+ * status flag, drains and returns, and sbt_check_status() reports
+ * SBT_ERR_DEVICE_TIMEOUT.  Stays set until reset with SBT_TEST_NONE. */
+typedef enum { SBT_TEST_NONE = 0, SBT_TEST_WITHHOLD_LOAD = 1 } sbt_test_hook;
+SBT_API sbt_status sbt_set_test_hook(sbt_context* ctx, sbt_test_hook hook);
 /* Number of kernels this context has launched so far. */
 SBT_API uint64_t sbt_launch_count(const sbt_context* ctx);
 /* Synchronise `stream`, then read and clear the device status flag of the

@@ -30,7 +30,7 @@ SBT_F32, SBT_BF16, SBT_F16 = 0, 1, 2
 PATHS = {"auto": 0, "scalar": 1, "vector": 2, "tma": 3}
 
 # Every symbol include/sbt.h declares.
-EXPORTS = ("sbt_create", "sbt_destroy", "sbt_set_path", "sbt_set_wait_limit_ns", "sbt_launch_count",
+EXPORTS = ("sbt_create", "sbt_destroy", "sbt_set_path", "sbt_set_wait_limit_ns", "sbt_set_test_hook", "sbt_launch_count",
            "sbt_check_status", "sbt_last_error_message", "sbt_tile_load_padded", "sbt_tile_store_clipped",
            "sbt_gather_rows", "sbt_scatter_rows_masked", "sbt_ragged_tile_load", "sbt_gemm_bounded_workspace_size",
            "sbt_gemm_bounded", "sbt_gemm_bounded_noalloc")
@@ -62,6 +62,7 @@ def load_library(path: str = LIB_PATH):
             "sbt_destroy": [p],
             "sbt_set_path": [p, ci],
             "sbt_set_wait_limit_ns": [p, u64],
+            "sbt_set_test_hook": [p, ci],
             "sbt_check_status": [p, p],
             "sbt_tile_load_padded": [p, ci, p, i64, i64, i64, i64, i64, i64, i64, i64, i32, i32, i32, i32, p, p, p],
             "sbt_tile_store_clipped": [p, ci, p, i32, i32, i32, i32, p, i64, i64, i64, i64, i64, i64, i64, i64, p],
@@ -165,6 +166,10 @@ class Context:
 
     def set_wait_limit_ns(self, ns: int):
         _check(load_library().sbt_set_wait_limit_ns(self._h, ns))
+
+    def set_test_hook(self, withhold_load: bool):
+        """Test only: make the next GEMM / bulk row launches withhold their first copy."""
+        _check(load_library().sbt_set_test_hook(self._h, 1 if withhold_load else 0))
 
     @property
     def launch_count(self) -> int:

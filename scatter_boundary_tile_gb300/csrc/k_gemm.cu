@@ -58,6 +58,7 @@ struct GemmParams {
     int m_tiles, n_tiles, k_blocks;
     unsigned int* status;
     uint64_t wait_ns;
+    int withhold_first_load;  // test hook: block 0 never issues its first stage
 };
 
 __global__ void __launch_bounds__(kGemmThreads, 1)
@@ -120,6 +121,16 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                         break;
                     }
                     const uint32_t sa = smem_u32(smem + (size_t)stage * kStageBytes);
+                    if (p.withhold_first_load && blockIdx.x == 0 && issued == 0) {
+                        // test hook: this stage's full barrier is never armed, so the MMA
+                        // warp's bounded wait on it runs out
+                        ++issued;
+                        if (++stage == kStages) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                        continue;
+                    }
                     mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
                     tma_load_2d(sa, &tmA, kb * BK, mt * BM, full_bar(stage));
                     tma_load_2d(sa + kABytes, &tmB, kb * BK, nt * BN, full_bar(stage));
@@ -392,6 +403,7 @@ sbt_status sbt_launch_gemm(sbt_context* ctx, const void* A, int64_t lda, const v
     p.k_blocks = (int)(d.Kp / BK);
     p.status = ctx->status;
     p.wait_ns = ctx->wait_limit_ns;
+    p.withhold_first_load = ctx->test_hook == SBT_TEST_WITHHOLD_LOAD;
     static bool attr_set[64] = {false};
     if (!attr_set[ctx->device & 63]) {
         cudaError_t e = cudaFuncSetAttribute(k_gemm_bf16_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);

@@ -378,6 +378,12 @@ sbt_status sbt_launch_gather(sbt_context* ctx, int es, const void* src, int64_t 
     p.col_offset = col_offset;
     p.tile_c = tile_c;
     p.pad_word = pad_word;
+    // The bulk-copy gather is taken only on request: on the 1 KiB-row workload the
+    // register-staged vector path below moves ~3% more bytes per second.
+    if (ctx->path == SBT_PATH_TMA && p.rows > 0 &&
+        sbt_gather_bulk_ok(es, src, cols, ld_src, col_offset, tile_c, mask, out, ld_out))
+        return sbt_launch_gather_bulk(ctx, es, src, rows, ld_src, idx, n_idx, row_offset, col_offset, tile_c, out,
+                                      ld_out, pad_word, stream);
     bool vec = rows_vector_ok(es, src, ld_src, col_offset, out, ld_out, tile_c);
     if (ctx->path == SBT_PATH_SCALAR) vec = false;
     p.nvec = vec ? tile_c / (16 / es) : 0;
@@ -404,6 +410,10 @@ sbt_status sbt_launch_scatter(sbt_context* ctx, int es, void* dst, int64_t rows,
     p.col_offset = col_offset;
     p.tile_c = tile_c;
     p.pad_word = 0;
+    if ((ctx->path == SBT_PATH_AUTO || ctx->path == SBT_PATH_TMA) &&
+        sbt_scatter_bulk_ok(es, src, ld_src, tile_c, mask, ld_mask))
+        return sbt_launch_scatter_bulk(ctx, es, dst, rows, cols, ld_dst, idx, n_idx, row_offset, col_offset, src,
+                                       ld_src, tile_c, mask, ld_mask, stream);
     bool vec = rows_vector_ok(es, dst, ld_dst, col_offset, src, ld_src, tile_c);
     if (ctx->path == SBT_PATH_SCALAR) vec = false;
     p.nvec = vec ? tile_c / (16 / es) : 0;

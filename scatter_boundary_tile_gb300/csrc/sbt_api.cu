@@ -127,6 +127,13 @@ sbt_status sbt_set_wait_limit_ns(sbt_context* ctx, uint64_t ns) {
     return SBT_OK;
 }
 
+sbt_status sbt_set_test_hook(sbt_context* ctx, sbt_test_hook hook) {
+    if (!ctx) return sbt_fail(SBT_ERR_INVALID_ARG, "ctx is NULL");
+    if (hook != SBT_TEST_NONE && hook != SBT_TEST_WITHHOLD_LOAD) return sbt_fail(SBT_ERR_INVALID_ARG, "unknown test hook");
+    ctx->test_hook = hook;
+    return SBT_OK;
+}
+
 uint64_t sbt_launch_count(const sbt_context* ctx) { return ctx ? ctx->launches : 0; }
 
 sbt_status sbt_check_status(sbt_context* ctx, void* stream) {

@@ -27,6 +27,7 @@ struct sbt_context {
     unsigned int* status = nullptr;  // device address of this device's status flag
     sbt_encode_tiled_fn encode_tiled = nullptr;
     uint64_t launches = 0;
+    int test_hook = 0;  // sbt_test_hook
 };
 
 // Thread-local error message; returns `st` so call sites can `return sbt_fail(...)`.
@@ -79,6 +80,18 @@ sbt_status sbt_launch_gemm(sbt_context* ctx, const void* A, int64_t lda, const v
                            int64_t ldc, sbt_dtype c_dtype, int64_t M, int64_t N, int64_t K, void* workspace,
                            size_t workspace_bytes, cudaStream_t stream);
 size_t sbt_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+// TMA bulk-copy variants of the row gather / scatter (k_bulk.cu) and their preconditions.
+bool sbt_gather_bulk_ok(int es, const void* src, int64_t cols, int64_t ld_src, int64_t col_offset, int32_t tile_c,
+                        const uint8_t* mask, const void* out, int64_t ld_out);
+bool sbt_scatter_bulk_ok(int es, const void* src, int64_t ld_src, int32_t tile_c, const uint8_t* mask,
+                         int64_t ld_mask);
+sbt_status sbt_launch_gather_bulk(sbt_context* ctx, int es, const void* src, int64_t rows, int64_t ld_src,
+                                  const int32_t* idx, int64_t n_idx, int64_t row_offset, int64_t col_offset,
+                                  int32_t tile_c, void* out, int64_t ld_out, uint32_t pad_word, cudaStream_t stream);
+sbt_status sbt_launch_scatter_bulk(sbt_context* ctx, int es, void* dst, int64_t rows, int64_t cols, int64_t ld_dst,
+                                   const int32_t* idx, int64_t n_idx, int64_t row_offset, int64_t col_offset,
+                                   const void* src, int64_t ld_src, int32_t tile_c, const uint8_t* mask,
+                                   int64_t ld_mask, cudaStream_t stream);
 
 // Checks the launch that was just enqueued and counts it.
 sbt_status sbt_after_launch(sbt_context* ctx, const char* what);

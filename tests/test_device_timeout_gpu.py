@@ -1,0 +1,86 @@
+"""Bounded device waits: a withheld copy makes a consumer's wait run out.
+
+The test hook makes the GEMM's TMA producer (or the bulk row kernels'
+producer warp) skip its first copy, so the barrier that copy would complete is
+never armed.  Nothing faults and nothing hangs: the waiting warp gives up
+after the context's wait limit, the kernel sets the device status flag, drains
+its copies in flight (bounded), frees its TMEM and returns.  The host reads
+SBT_ERR_DEVICE_TIMEOUT from sbt_check_status, and the same context then runs
+the same call correctly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import scatter_boundary_tile_gb300 as sbt
+import synth
+import synth.workloads as wl
+from gpu_helpers import dev, host, sync
+
+pytestmark = pytest.mark.gpu
+LIMIT_NS = 20_000_000  # 20 ms
+
+
+def expect_timeout(ctx, launch):
+    ctx.set_wait_limit_ns(LIMIT_NS)
+    ctx.set_test_hook(True)
+    try:
+        launch()
+        with pytest.raises(sbt.SbtError) as e:
+            ctx.check_status()
+        assert e.value.status == sbt.SBT_ERR_DEVICE_TIMEOUT
+    finally:
+        ctx.set_test_hook(False)
+        ctx.set_wait_limit_ns(2_000_000_000)
+    ctx.check_status()  # the flag was cleared by the read above
+
+
+def test_gemm_wait_runs_out_then_recovers(ctx):
+    M, N, K = 1000, 1000, 1000
+    g = wl.gemm_bf16(M=M, N=N, K=K, tag=21)
+    A, B = dev(g["A"]), dev(g["B"])
+    C = torch.empty(M * g["ldc"] * 2, dtype=torch.uint8, device="cuda")
+    ws_n = sbt.gemm_bounded_workspace_size(ctx, M, N, K, g["lda"], g["ldb"])
+    ws = torch.empty(ws_n, dtype=torch.uint8, device="cuda")
+    run = lambda: sbt.gemm_bounded(ctx, A, g["lda"], B, g["ldb"], C, g["ldc"], M, N, K, ws, ws_n)
+    expect_timeout(ctx, run)
+    run()
+    sync()
+    ctx.check_status()
+    got = synth.bf16_bits_to_f32(host(C, np.uint16, (M, g["ldc"]))[:, :N]).astype(np.float64)
+    ref = oracle.gemm_f64(g["A"], g["lda"], g["B"], g["ldb"], M, N, K)
+    ref_b = synth.bf16_bits_to_f32(oracle.round_bf16(ref)).astype(np.float64)
+    assert np.linalg.norm(got - ref_b) / np.linalg.norm(ref) <= 1e-3
+
+
+def test_bulk_scatter_wait_runs_out_then_recovers(ctx):
+    d = wl.scatter_rows_f32(dst_rows=20000, n_idx=5000, cols=256)
+    rows, n = d["dst_rows"], d["idx"].size
+    dst = torch.zeros(rows * 256 * 4, dtype=torch.uint8, device="cuda")
+    s_, i, m = dev(d["src"]), dev(d["idx"]), dev(d["mask"])
+    ctx.set_path("tma")
+    run = lambda: sbt.scatter_rows_masked(ctx, dst, rows, 256, 256, i, n, s_, 256, 256, mask=m, ld_mask=256,
+                                          dtype="f32")
+    expect_timeout(ctx, run)
+    dst.zero_()
+    run()
+    sync()
+    ctx.check_status()
+    want = oracle.scatter_rows_masked(np.zeros((rows, 256), np.float32), rows, 256, 256, d["idx"], d["src"], 256, 256,
+                                      mask=d["mask"])
+    assert np.array_equal(host(dst, np.uint32, (rows, 256)), want.view(np.uint32))
+
+
+def test_bulk_gather_wait_runs_out_then_recovers(ctx):
+    d = wl.gather_rows_bf16(n_rows=5000, n_idx=3000, cols=512)
+    t, idx = dev(d["table"]), dev(d["idx"])
+    out = torch.empty(3000 * 512 * 2, dtype=torch.uint8, device="cuda")
+    ctx.set_path("tma")
+    run = lambda: sbt.gather_rows(ctx, t, 5000, 512, 512, idx, 3000, out, 512, 512, dtype="bf16")
+    expect_timeout(ctx, run)
+    run()
+    sync()
+    ctx.check_status()
+    want = oracle.gather_rows(d["table"], 5000, 512, 512, d["idx"], 512)
+    assert np.array_equal(host(out, np.uint16, (3000, 512)), want)

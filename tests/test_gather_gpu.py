@@ -64,7 +64,7 @@ def test_small_fp32_table_pad_minus_one(ctx, path):
 def test_sentinels_and_offsets(ctx, row_offset):
     a = synth.uniform_f32(101, (40, 64), -1.0, 1.0)
     idx = np.array([-1, 0, 39, 40, 41, I32_MIN, I32_MAX, -2, 3, -5, 7, 35, 36, 37, 1, 2, 11], np.int32)
-    for path in ("auto", "scalar"):
+    for path in ("auto", "tma", "vector", "scalar"):
         got = run_gather(ctx, a, 40, 64, 64, idx, 64, "f32", row_offset=row_offset, pad=-1.0, path=path)
         want = oracle_gather(a, 40, 64, 64, idx, 64, row_offset=row_offset, pad=np.float32(-1.0))
         assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), path
@@ -75,7 +75,7 @@ def test_sentinels_and_offsets(ctx, row_offset):
 def test_bf16_rows_vector_and_edges(ctx, n_idx, col_offset, tile_c):
     d = wl.gather_rows_bf16(n_rows=5000, n_idx=n_idx, cols=512)
     t, idx = d["table"], d["idx"]
-    for path in ("auto", "scalar"):
+    for path in ("auto", "tma", "vector", "scalar"):
         got = run_gather(ctx, t, 5000, 512, 512, idx, tile_c, "bf16", col_offset=col_offset, path=path)
         want = oracle_gather(t, 5000, 512, 512, idx, tile_c, col_offset=col_offset, pad=0)
         assert np.array_equal(got, want), path
@@ -88,7 +88,7 @@ def test_bf16_mask_and_wide_output(ctx, ld_mask_extra):
     ld_mask = 128 + ld_mask_extra
     mask = synth.bernoulli_u8(102, (257, ld_mask), 0.8)
     ld_out = 136  # columns >= tile_c of the output must stay untouched
-    for path in ("auto", "scalar"):
+    for path in ("auto", "tma", "vector", "scalar"):
         got = run_gather(ctx, t, 700, 128, 128, idx, 128, "bf16", mask=mask, ld_mask=ld_mask, pad=0xBF80,
                          ld_out=ld_out, path=path)
         want = oracle_gather(t, 700, 128, 128, idx, 128, mask=mask, ld_mask=ld_mask, pad=0xBF80, ld_out=ld_out)
@@ -147,7 +147,8 @@ def test_invalid_arguments_launch_nothing(ctx):
     assert ctx.launch_count == before
 
 
-def test_full_size_workload_bit_exact(ctx):
+@pytest.mark.parametrize("path", ["auto", "tma", "vector"])
+def test_full_size_workload_bit_exact(ctx, path):
     """1,000,000 x 512 bf16 table, 1,048,576 indices (1 % -1, 0.5 % past the end), the
     launch the benchmark times; the whole 1 GiB output is compared with the oracle."""
     d = wl.gather_rows_bf16()
@@ -156,6 +157,7 @@ def test_full_size_workload_bit_exact(ctx):
     t_dev, i_dev = dev(t), dev(idx)
     import torch
     out = torch.empty(n * 512 * 2, dtype=torch.uint8, device="cuda")
+    ctx.set_path(path)
     sbt.gather_rows(ctx, t_dev, 1_000_000, 512, 512, i_dev, n, out, 512, 512, dtype="bf16")
     got = host(out, np.uint16, (n, 512))
     del t_dev, out

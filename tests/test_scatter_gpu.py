@@ -30,7 +30,7 @@ def test_unique_rows_fp32(ctx, n_idx):
     d = wl.scatter_rows_f32(dst_rows=5000, n_idx=n_idx, cols=256)
     dst = np.zeros((5000, 256), np.float32)
     want = oracle.scatter_rows_masked(dst.copy(), 5000, 256, 256, d["idx"], d["src"], 256, 256, mask=d["mask"])
-    for path in ("auto", "scalar"):
+    for path in ("auto", "tma", "vector", "scalar"):
         got = gpu_scatter(ctx, dst, 5000, 256, 256, d["idx"], d["src"], 256, 256, "f32", mask=d["mask"],
                           ld_mask=256, path=path)
         assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), path
@@ -62,7 +62,7 @@ def test_edge_cases(ctx, case, dtype):
     mask = synth.bernoulli_u8(303, (n, ld_mask), 0.85) if ld_mask else None
     want = oracle.scatter_rows_masked(dst.copy(), rows, cols, ld_dst, idx, src, ld_src, tile_c,
                                       row_offset=row_offset, col_offset=col_offset, mask=mask, ld_mask=ld_mask or None)
-    for path in ("auto", "scalar"):
+    for path in ("auto", "tma", "vector", "scalar"):
         got = gpu_scatter(ctx, dst, rows, cols, ld_dst, idx, src, ld_src, tile_c, dtype, row_offset=row_offset,
                           col_offset=col_offset, mask=mask, ld_mask=ld_mask, path=path)
         assert np.array_equal(got.view(np.uint8), want.view(np.uint8)), path
@@ -93,13 +93,15 @@ def test_empty_and_invalid(ctx):
     assert ctx.launch_count == before
 
 
-def test_full_size_workload_bit_exact(ctx):
+@pytest.mark.parametrize("path", ["auto", "tma", "vector"])
+def test_full_size_workload_bit_exact(ctx, path):
     """4,194,304 x 256 fp32 destination (zero), 1,048,576 unique rows, Bernoulli(0.9) mask:
     the launch the benchmark times; the whole 4 GiB destination is compared."""
     d = wl.scatter_rows_f32()
     rows, cols = d["dst_rows"], d["cols"]
     dst_dev = torch.zeros(rows * cols * 4, dtype=torch.uint8, device="cuda")
     s, i, m = dev(d["src"]), dev(d["idx"]), dev(d["mask"])
+    ctx.set_path(path)
     sbt.scatter_rows_masked(ctx, dst_dev, rows, cols, cols, i, d["idx"].size, s, cols, cols, mask=m, ld_mask=cols,
                             dtype="f32")
     got = host(dst_dev, np.uint32, (rows, cols))
