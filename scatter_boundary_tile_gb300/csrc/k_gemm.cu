@@ -61,6 +61,51 @@ struct GemmParams {
     int withhold_first_load;  // test hook: block 0 never issues its first stage
 };
 
+// Tile order: groups of kGroupM M-tiles are walked N column by N column, so the
+// tiles running at the same time share a few A row blocks and B column blocks
+// (a working set of tens of MB that stays in L2) instead of sweeping all of A
+// for every N column.
+constexpr int kGroupM = 8;
+__device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, int* mt, int* nt) {
+    const int per_group = kGroupM * n_tiles;
+    const int g = tile / per_group;
+    const int within = tile - g * per_group;
+    const int first_m = g * kGroupM;
+    const int gm = min(kGroupM, m_tiles - first_m);
+    *mt = first_m + within % gm;
+    *nt = within / gm;
+}
+
+// Drain one 128 x BN accumulator from TMEM (this warp's 32-lane quarter `q`),
+// round (or keep fp32) and store rows row0.. of C through a padded shared
+// transpose so that each store instruction covers 32 consecutive columns.
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tmem_acc, int q, int lane, float* buf,
+                                              int row0, int n0) {
+    const int n_valid = min(BN, p.N - n0);
+    const int chunks = (n_valid + 31) / 32;
+    for (int c = 0; c < chunks; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem_acc + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) buf[lane * 33 + j] = __uint_as_float(r[j]);
+        __syncwarp();
+        const int col = n0 + c * 32 + lane;
+        if (col < p.N) {
+            if (p.c_f32) {
+                float* Cp = reinterpret_cast<float*>(p.C);
+                for (int rr = 0; rr < 32 && row0 + rr < p.M; ++rr)
+                    Cp[(int64_t)(row0 + rr) * p.ldc + col] = buf[rr * 33 + lane];
+            } else {
+                __nv_bfloat16* Cp = reinterpret_cast<__nv_bfloat16*>(p.C);
+                for (int rr = 0; rr < 32 && row0 + rr < p.M; ++rr)
+                    Cp[(int64_t)(row0 + rr) * p.ldc + col] = __float2bfloat16_rn(buf[rr * 33 + lane]);
+            }
+        }
+        __syncwarp();
+    }
+}
+
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_gemm_bf16_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p) {
@@ -113,7 +158,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             int64_t issued = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+                int mt, nt;
+                tile_coords(tile, p.m_tiles, p.n_tiles, &mt, &nt);
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, p.wait_ns, abort_flag, p.status,
                                            kCodeProducer)) {
@@ -166,7 +212,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++local) {
                 const int acc = local & 1;
                 const uint32_t use = (uint32_t)(local >> 1);
-                const int nt = tile / p.m_tiles;
+                int mt_unused, nt;
+                tile_coords(tile, p.m_tiles, p.n_tiles, &mt_unused, &nt);
                 const int n_valid = min(BN, p.N - nt * BN);
                 const uint32_t idesc = idesc_bf16_f32(BM, (uint32_t)((n_valid + 15) & ~15));
                 if (!mbar_wait_bounded(tempty_bar(acc), (use & 1u) ^ 1u, p.wait_ns, abort_flag, p.status,
@@ -216,34 +263,11 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
             const int acc = local & 1;
             const uint32_t use = (uint32_t)(local >> 1);
-            const int mt = tile % p.m_tiles, nt = tile / p.m_tiles;
+            int mt, nt;
+                tile_coords(tile, p.m_tiles, p.n_tiles, &mt, &nt);
             if (!mbar_wait_bounded(tfull_bar(acc), use & 1u, p.wait_ns, abort_flag, p.status, kCodeEpilogue)) break;
             tc_fence_after();
-            const int n0 = nt * BN;
-            const int n_valid = min(BN, p.N - n0);
-            const int chunks = (n_valid + 31) / 32;
-            const int row0 = mt * BM + q * 32;
-            for (int c = 0; c < chunks; ++c) {
-                uint32_t r[32];
-                tmem_ld_32x32b_x32(tmem_base + ((uint32_t)(q * 32) << 16) + (uint32_t)(acc * BN + c * 32), r);
-                tmem_ld_wait();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) buf[lane * 33 + j] = __uint_as_float(r[j]);
-                __syncwarp();
-                const int col = n0 + c * 32 + lane;
-                if (col < p.N) {
-                    if (p.c_f32) {
-                        float* Cp = reinterpret_cast<float*>(p.C);
-                        for (int rr = 0; rr < 32 && row0 + rr < p.M; ++rr)
-                            Cp[(int64_t)(row0 + rr) * p.ldc + col] = buf[rr * 33 + lane];
-                    } else {
-                        __nv_bfloat16* Cp = reinterpret_cast<__nv_bfloat16*>(p.C);
-                        for (int rr = 0; rr < 32 && row0 + rr < p.M; ++rr)
-                            Cp[(int64_t)(row0 + rr) * p.ldc + col] = __float2bfloat16_rn(buf[rr * 33 + lane]);
-                    }
-                }
-                __syncwarp();
-            }
+            epilogue_tile(p, tmem_base + (uint32_t)(acc * BN), q, lane, buf, mt * BM + q * 32, nt * BN);
             tc_fence_before();
             mbar_arrive(tempty_bar(acc));
         }
@@ -254,6 +278,178 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, kTmemCols);
+    }
+}
+
+// ---------------------------------------------------------------------------- CTA-pair kernel
+//
+// Two CTAs of a cluster compute one 256 x 256 tile with tcgen05.mma.cta_group::2
+// (M = 256: 128 rows in each CTA's TMEM; B split 128 + 128 rows between the
+// CTAs' shared memory).  Each CTA loads only its own half of B, so a CTA
+// pulls 32 KB per 64-deep K step instead of 48 KB, and the 6-stage ring holds
+// twice as many steps of latency.  Each CTA's TMA completes on the leader's
+// full barrier; the leader's MMA commits are multicast to both CTAs' empty and
+// TMEM-full barriers; both epilogues arrive on the leader's TMEM-empty barrier.
+
+constexpr int kStages2 = 6;
+constexpr uint32_t kHalfBytes = 128 * BK * 2;          // A rows or B rows of one CTA, one K step
+constexpr uint32_t kStageBytes2 = 2 * kHalfBytes;      // per CTA
+constexpr int kNumBars2 = 2 * kStages2 + 5;
+constexpr size_t kGemmSmem2 = 1024 + (size_t)kStages2 * kStageBytes2 + (size_t)kEpiWarps * kEpiWords * 4 +
+                              kNumBars2 * 8 + 16;
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+    k_gemm_bf16_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                        const GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* epi = reinterpret_cast<float*>(smem + (size_t)kStages2 * kStageBytes2);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(epi + kEpiWarps * kEpiWords);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars2);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const uint32_t bar0 = smem_u32(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kStages2 + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kStages2 + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kStages2 + 2 + a); };
+    const uint32_t mma_done_bar = bar0 + 8u * (2 * kStages2 + 4);
+
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x / 32), 0);
+    const int lane = threadIdx.x % 32;
+    const uint32_t rank = cluster_ctarank();
+    const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages2; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 2 * kEpiWarps * 32);
+        }
+        mbar_init(mma_done_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();  // both CTAs' barriers are initialised before any remote arrival
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int num_tiles = p.m_tiles * p.n_tiles;  // 256 x 256 tiles
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer (each CTA, own halves)
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            bool ok = true;
+            int64_t issued = 0;
+            for (int tile = cluster; ok && tile < num_tiles; tile += nclusters) {
+                int mt, nt;
+                tile_coords(tile, p.m_tiles, p.n_tiles, &mt, &nt);
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, p.wait_ns, abort_flag, p.status,
+                                           kCodeProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    const bool withhold = p.withhold_first_load && blockIdx.x == 0 && issued == 0;
+                    ++issued;
+                    if (!withhold) {
+                        const uint32_t sa = smem_u32(smem + (size_t)stage * kStageBytes2);
+                        const uint32_t leader_full = mapa_shared(full_bar(stage), 0);
+                        if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * kStageBytes2);
+                        tma_load_2d_pair(sa, &tmA, kb * BK, mt * 256 + (int)rank * 128, leader_full);
+                        tma_load_2d_pair(sa + kHalfBytes, &tmB, kb * BK, nt * 256 + (int)rank * 128, leader_full);
+                    }
+                    if (++stage == kStages2) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer (leader CTA only)
+        if (lane == 0 && rank == 0) {
+            uint32_t stage = 0, phase = 0;
+            int local = 0;
+            bool ok = true;
+            const uint32_t idesc = idesc_bf16_f32(256, 256);
+            for (int tile = cluster; ok && tile < num_tiles; tile += nclusters, ++local) {
+                const int acc = local & 1;
+                const uint32_t use = (uint32_t)(local >> 1);
+                if (!mbar_wait_bounded(tempty_bar(acc), (use & 1u) ^ 1u, p.wait_ns, abort_flag, p.status,
+                                       kCodeMma)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait_bounded(full_bar(stage), phase, p.wait_ns, abort_flag, p.status, kCodeMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int k_rem = p.K - kb * BK;
+                    const int k_steps = k_rem >= BK ? BK / 16 : (k_rem + 15) / 16;
+                    const uint32_t sa = smem_u32(smem + (size_t)stage * kStageBytes2);
+                    const uint32_t sb = sa + kHalfBytes;
+                    for (int ks = 0; ks < k_steps; ++ks) {
+                        tc_mma_f16_pair(d_tmem, smem_desc_sw128(sa + 32u * ks), smem_desc_sw128(sb + 32u * ks),
+                                        idesc, (kb | ks) != 0 ? 1u : 0u);
+                    }
+                    tc_commit_pair_multicast(empty_bar(stage), 0x3);
+                    if (++stage == kStages2) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (ok) tc_commit_pair_multicast(tfull_bar(acc), 0x3);
+            }
+            tc_commit_pair_multicast(mma_done_bar, 0x1);
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(mma_done_bar, 0)) {
+                if (globaltimer() - t0 > p.wait_ns) {
+                    atomicOr(p.status, (unsigned int)kCodeTeardown);
+                    break;
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue (warps 2..5 of each CTA)
+        const int q = warp & 3;
+        float* buf = epi + (warp - 2) * kEpiWords;
+        const uint32_t leader_tempty0 = mapa_shared(tempty_bar(0), 0);
+        int local = 0;
+        for (int tile = cluster; tile < num_tiles; tile += nclusters, ++local) {
+            const int acc = local & 1;
+            const uint32_t use = (uint32_t)(local >> 1);
+            int mt, nt;
+                tile_coords(tile, p.m_tiles, p.n_tiles, &mt, &nt);
+            if (!mbar_wait_bounded(tfull_bar(acc), use & 1u, p.wait_ns, abort_flag, p.status, kCodeEpilogue)) break;
+            tc_fence_after();
+            epilogue_tile(p, tmem_base + (uint32_t)(acc * BN), q, lane, buf, mt * 256 + (int)rank * 128 + q * 32,
+                          nt * BN);
+            tc_fence_before();
+            mbar_arrive_cluster(leader_tempty0 + 8u * acc);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // the leader's MMAs into the peer's TMEM are complete before either CTA frees it
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, kTmemCols);
     }
 }
 
@@ -328,7 +524,7 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 GemmDims gemm_dims(int64_t M, int64_t N, int64_t K) {
     GemmDims d;
-    d.Mp = sbt_cdiv(M, BM) * BM;
+    d.Mp = sbt_cdiv(M, 256) * 256;  // whole 256-row tiles for the CTA-pair kernel
     d.Np = sbt_cdiv(N, BN) * BN;
     d.Kp = sbt_cdiv(K, BK) * BK;
     d.a_bytes = round_up((size_t)d.Mp * d.Kp * 2, 256);
@@ -387,10 +583,12 @@ sbt_status sbt_launch_gemm(sbt_context* ctx, const void* A, int64_t lda, const v
     }
 
     // 2. tensor-core main kernel
+    // CTA pairs for large problems; single CTAs when M or N is small.
+    const bool pair = M >= 512 && N >= 512 && ctx->sm_count >= 2;
     CUtensorMap tmA, tmB;
     sbt_status st = encode_kmajor(ctx, &tmA, Ap, d.Mp, d.Kp, BM);
     if (st) return st;
-    if ((st = encode_kmajor(ctx, &tmB, Bp, d.Np, d.Kp, BN))) return st;
+    if ((st = encode_kmajor(ctx, &tmB, Bp, d.Np, d.Kp, pair ? 128 : BN))) return st;
     GemmParams p;
     p.C = (char*)C;
     p.ldc = ldc;
@@ -408,7 +606,37 @@ sbt_status sbt_launch_gemm(sbt_context* ctx, const void* A, int64_t lda, const v
     if (!attr_set[ctx->device & 63]) {
         cudaError_t e = cudaFuncSetAttribute(k_gemm_bf16_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
         if (e != cudaSuccess) return sbt_cuda_check(e, "cudaFuncSetAttribute(gemm smem)");
+        e = cudaFuncSetAttribute(k_gemm_bf16_tc_pair, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem2);
+        if (e != cudaSuccess) return sbt_cuda_check(e, "cudaFuncSetAttribute(gemm pair smem)");
         attr_set[ctx->device & 63] = true;
+    }
+    if (pair) {
+        p.m_tiles = (int)(d.Mp / 256);
+        const int tiles = p.m_tiles * p.n_tiles;
+        // as many CTA pairs as can be resident at once (queried once per device)
+        static int max_clusters[64] = {0};
+        if (!max_clusters[ctx->device & 63]) {
+            cudaLaunchConfig_t cfg = {};
+            cudaLaunchAttribute attr;
+            attr.id = cudaLaunchAttributeClusterDimension;
+            attr.val.clusterDim.x = 2;
+            attr.val.clusterDim.y = 1;
+            attr.val.clusterDim.z = 1;
+            cfg.gridDim = dim3(2 * (unsigned)(ctx->sm_count / 2), 1, 1);
+            cfg.blockDim = dim3(kGemmThreads, 1, 1);
+            cfg.dynamicSmemBytes = kGemmSmem2;
+            cfg.attrs = &attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, k_gemm_bf16_tc_pair, &cfg) != cudaSuccess || n < 1) {
+                (void)cudaGetLastError();
+                n = ctx->sm_count / 2;
+            }
+            max_clusters[ctx->device & 63] = n;
+        }
+        const int clusters = std::min(tiles, max_clusters[ctx->device & 63]);
+        k_gemm_bf16_tc_pair<<<2 * clusters, kGemmThreads, kGemmSmem2, stream>>>(tmA, tmB, p);
+        return sbt_after_launch(ctx, "gemm_bounded (tcgen05, CTA pairs)");
     }
     const int tiles = p.m_tiles * p.n_tiles;
     const int grid = std::min(tiles, ctx->sm_count);

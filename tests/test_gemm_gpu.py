@@ -84,8 +84,20 @@ def test_integer_inputs_exact(ctx, mnk):
     np.testing.assert_array_equal(got32, want.astype(np.float64))
 
 
+def test_many_tiles_single_cta_kernel(ctx):
+    """M < 512 selects the single-CTA kernel; 4 x 118 tiles exceed the SM count, so its
+    persistent loop and both TMEM accumulators are used."""
+    M, N, K = 384, 30000, 96
+    g = wl.gemm_bf16(M=M, N=N, K=K, tag=9)
+    got, _ = run_gemm(ctx, g, "bf16")
+    ref = oracle.gemm_f64(g["A"], g["lda"], g["B"], g["ldb"], M, N, K)
+    ref_b = synth.bf16_bits_to_f32(oracle.round_bf16(ref)).astype(np.float64)
+    assert rel_fro(got, ref_b) <= TOL
+
+
 def test_many_tiles_per_block(ctx):
-    """More tiles than SMs: the persistent loop and both TMEM accumulators are used."""
+    """CTA-pair kernel (M, N >= 512) with more 256 x 256 tiles than CTA pairs: the persistent
+    loop and both TMEM accumulators are used."""
     M, N, K = 4096, 2560, 128
     g = wl.gemm_bf16(M=M, N=N, K=K, tag=8)
     got, _ = run_gemm(ctx, g, "bf16")
