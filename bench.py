@@ -202,6 +202,29 @@ def time_launches(fn, reps: int, warmup: int = 3, flush=None):
     return statistics.median(times), statistics.fmean(times), min(times)
 
 
+def kernel_split(fn, reps: int):
+    """Mean device time (ms) per launch of each kernel fn() launches, from CUPTI kernel
+    records (torch.profiler); {} if the profiler is unavailable."""
+    try:
+        import torch
+        from torch.profiler import ProfilerActivity, profile
+        fn()
+        torch.cuda.synchronize()
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            for _ in range(reps):
+                fn()
+            torch.cuda.synchronize()
+        out = {}
+        for ev in prof.events():
+            if getattr(ev, "device_type", None) is not None and "CUDA" in str(ev.device_type):
+                name = ev.name.replace("(anonymous namespace)::", "").replace("void ", "")
+                name = name.split("(")[0].split("<")[0].strip()
+                out[name] = out.get(name, 0.0) + ev.device_time / 1e3 / reps
+        return out
+    except Exception:
+        return {}
+
+
 def gather_bytes(idx: np.ndarray, n_rows: int, cols: int, es: int) -> int:
     valid = int(np.count_nonzero((idx >= 0) & (idx < n_rows)))
     return valid * cols * es + idx.size * cols * es + idx.size * 4
@@ -316,8 +339,19 @@ def run_ops(ctx, pk):
             ws = torch.empty(max(ws_n, 1), dtype=torch.uint8, device="cuda")
             fn = lambda: sbt.gemm_bounded(ctx, A, g["lda"], B, g["ldb"], C, g["ldc"], M, N, K, ws, ws_n)
             med, _, _ = time_launches(fn, 10 if M > 4000 else 30)
-            tf = 2.0 * M * N * K / med / 1e9
-            ops[f"gemm_bounded_{M}x{N}x{K}"] = {"ms": med, "TFLOP/s": tf, "frac_bf16": tf / pk["bf16_tflops"]}
+            flops = 2.0 * M * N * K
+            tf = flops / med / 1e9
+            entry = {"ms": med, "TFLOP/s": tf, "frac_bf16": tf / pk["bf16_tflops"],
+                     "frac_bf16_sustained": tf / pk["bf16_tflops_sustained"], "flops": flops,
+                     "note": "whole call: operand staging + tensor-core kernel"}
+            split = kernel_split(fn, 5)
+            if split:
+                entry["kernels_ms"] = split
+                main = sum(v for k, v in split.items() if "k_gemm" in k)
+                if main > 0:
+                    entry["tensor_kernel_TFLOP/s"] = flops / main / 1e9
+                    entry["tensor_kernel_frac_bf16"] = flops / main / 1e9 / pk["bf16_tflops"]
+            ops[f"gemm_bounded_{M}x{N}x{K}"] = entry
             del A, B, C, ws
     except Exception as e:  # the GEMM may be unavailable in this build
         ops["gemm_bounded"] = {"unavailable": str(e).splitlines()[0][:200]}

@@ -583,8 +583,9 @@ sbt_status sbt_launch_gemm(sbt_context* ctx, const void* A, int64_t lda, const v
     }
 
     // 2. tensor-core main kernel
-    // CTA pairs for large problems; single CTAs when M or N is small.
-    const bool pair = M >= 512 && N >= 512 && ctx->sm_count >= 2;
+    // CTA pairs when there are at least as many 256 x 256 tiles as SM pairs;
+    // single CTAs (128 x 256 tiles) for smaller problems.
+    const bool pair = ctx->sm_count >= 2 && (d.Mp / 256) * (d.Np / 256) >= ctx->sm_count / 2;
     CUtensorMap tmA, tmB;
     sbt_status st = encode_kmajor(ctx, &tmA, Ap, d.Mp, d.Kp, BM);
     if (st) return st;

@@ -36,8 +36,9 @@ def expect_timeout(ctx, launch):
     ctx.check_status()  # the flag was cleared by the read above
 
 
-def test_gemm_wait_runs_out_then_recovers(ctx):
-    M, N, K = 1000, 1000, 1000
+@pytest.mark.parametrize("mnk", [(1000, 1000, 1000), (2048, 2560, 256)], ids=["single_cta", "cta_pair"])
+def test_gemm_wait_runs_out_then_recovers(ctx, mnk):
+    M, N, K = mnk
     g = wl.gemm_bf16(M=M, N=N, K=K, tag=21)
     A, B = dev(g["A"]), dev(g["B"])
     C = torch.empty(M * g["ldc"] * 2, dtype=torch.uint8, device="cuda")

@@ -84,9 +84,10 @@ def test_integer_inputs_exact(ctx, mnk):
     np.testing.assert_array_equal(got32, want.astype(np.float64))
 
 
-def test_many_tiles_single_cta_kernel(ctx):
-    """M < 512 selects the single-CTA kernel; 4 x 118 tiles exceed the SM count, so its
-    persistent loop and both TMEM accumulators are used."""
+def test_many_tiles_with_m_tail(ctx):
+    """M = 384 fills one and a half 256-row tiles; 2 x 118 tiles run on CTA pairs, each pair
+    taking several tiles, so the persistent loop, both TMEM accumulators and the masked
+    M tail are all exercised."""
     M, N, K = 384, 30000, 96
     g = wl.gemm_bf16(M=M, N=N, K=K, tag=9)
     got, _ = run_gemm(ctx, g, "bf16")
