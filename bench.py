@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=8.0, help="CPU-baseline sample budget")
     ap.add_argument("--profile", default=None,
-                    choices=["gather", "scatter", "ragged", "tile_load", "tile_store", "tile_load_unaligned",
+                    choices=["gather", "scatter", "ragged", "ragged_store", "tile_load", "tile_store", "tile_load_unaligned",
                              "tile_store_unaligned", "gemm"],
                     help="only launch one operation's workload (warmup + steps launches) for ncu")
     ap.add_argument("--scale", type=float, default=1.0, help="--profile: fraction of the workload's rows")
@@ -305,7 +305,15 @@ def run_ops(ctx, pk):
     ops["ragged_tile_load"] = {"workload": "bf16 batch 64, len U[1,4096], 8 heads, depth 128 -> [64][8][4096][128]",
                                "ms": med, "GB/s": nbytes / med / 1e6, "frac_hbm": nbytes / med / 1e6 / hbm,
                                "algorithmic_bytes": nbytes}
-    del out, x, cu, d
+    # ragged 3D tile store: the padded tiles back into the packed array (valid rows only)
+    xs = torch.empty(d["total_rows"] * 8 * 128 * 2, dtype=torch.uint8, device="cuda")
+    fn = lambda: sbt.ragged_tile_store(ctx, out, 64, 8, 128, 4096, cu, xs, d["total_rows"], 1024, 128, dtype="bf16")
+    med, mean, best = time_launches(fn, 20)
+    nbytes = 2 * d["total_rows"] * 8 * 128 * 2 + 65 * 4
+    ops["ragged_tile_store"] = {"workload": "bf16 [64][8][4096][128] tiles -> packed [sum(len)][8][128], len U[1,4096]",
+                                "ms": med, "GB/s": nbytes / med / 1e6, "frac_hbm": nbytes / med / 1e6 / hbm,
+                                "algorithmic_bytes": nbytes}
+    del out, x, cu, d, xs
 
     # tile load / store over a 16381 x 16411 fp32 array, 64 x 32 tiles (aligned and unaligned rows)
     import synth
@@ -525,6 +533,14 @@ def run_profile(args):
         x, cu = dev_bytes(d["x"]), dev_bytes(d["cu_seqlens"])
         fn = lambda: sbt.ragged_tile_load(ctx, x, d["total_rows"], 8, 128, 1024, 128, cu, b, 4096, out,
                                           dtype="bf16")
+    elif op == "ragged_store":
+        d = wl.ragged_bf16(batch=max(1, int(64 * f)))
+        b = d["cu_seqlens"].size - 1
+        tiles = torch.empty(b * 8 * 4096 * 128 * 2, dtype=torch.uint8, device="cuda")
+        xs = torch.empty(d["total_rows"] * 8 * 128 * 2, dtype=torch.uint8, device="cuda")
+        cu = dev_bytes(d["cu_seqlens"])
+        fn = lambda: sbt.ragged_tile_store(ctx, tiles, b, 8, 128, 4096, cu, xs, d["total_rows"], 1024, 128,
+                                           dtype="bf16")
     elif op.startswith("tile"):
         r_, c_ = max(64, int(16381 * f)), 16411
         ld = 16411 if op.endswith("unaligned") else 16416

@@ -188,6 +188,25 @@ SBT_API sbt_status sbt_ragged_tile_load(sbt_context* ctx, sbt_dtype dtype, const
                                 int32_t batch, int32_t t_pad, void* out, void* stream);
 
 /*
+ * Ragged 3D tile store: the inverse of sbt_ragged_tile_load.
+ * Mojo "RaggedTMA3DTile", async_copy_from_col / async_copy_batched: tiles go
+ * back to the packed ragged array, only the first `dynamic_dim` rows of a tile
+ * (valid sequence positions) are written, and what overhangs is masked off.
+ *
+ *   x[(cu[b]+r)*ld_row + h*ld_head + d] = tiles[((b*heads + h)*t_pad + r)*depth + d]
+ *     for r < min(cu[b+1]-cu[b], t_pad) with 0 <= cu[b]+r < total_rows;
+ *   every other element of x keeps its bits.
+ *
+ * tiles: device, dense [batch][heads][t_pad][depth]; cu_seqlens: device
+ * int32[batch+1]; x: device packed [total_rows] rows with strides (ld_row,
+ * ld_head), both positive.  Sequences whose packed rows overlap get one of the
+ * candidate values (undefined which).
+ */
+SBT_API sbt_status sbt_ragged_tile_store(sbt_context* ctx, sbt_dtype dtype, const void* tiles, int32_t batch,
+                                         int32_t heads, int32_t depth, int32_t t_pad, const int32_t* cu_seqlens,
+                                         void* x, int64_t total_rows, int64_t ld_row, int64_t ld_head, void* stream);
+
+/*
  * Boundary-tile GEMM  C = A * B.
  * cuTile.jl "Operations", muladd: (M,K) x (K,N) -> (M,N) with bf16 inputs
  * accumulating in fp32.  Tylo.jl "Boundary tiles", section "Accumulator

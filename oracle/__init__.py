@@ -45,13 +45,14 @@ def _load():
             lib.oracle_scatter_rows_masked.argtypes = [ci, p, i64, i64, i64, p, i64, i64, i64, p, i64, i32,
                                                        p, i64]
             lib.oracle_ragged_tile_load.argtypes = [ci, p, i64, i32, i32, i64, i64, p, i32, i32, p]
+            lib.oracle_ragged_tile_store.argtypes = [ci, p, i32, i32, i32, i32, p, p, i64, i64, i64]
             lib.oracle_gemm_f64.argtypes = [p, i64, p, i64, i64, i64, i64, p, i64]
             lib.oracle_gemm_f64_at.argtypes = [p, i64, p, i64, i64, p, p, i64, p]
             lib.oracle_bf16_rne.argtypes = [ctypes.c_double]
             lib.oracle_bf16_rne.restype = ctypes.c_uint16
             lib.oracle_round_bf16.argtypes = [p, i64, p]
             for f in (lib.oracle_tile_load_padded, lib.oracle_tile_store_clipped, lib.oracle_gather_rows,
-                      lib.oracle_scatter_rows_masked, lib.oracle_ragged_tile_load, lib.oracle_gemm_f64,
+                      lib.oracle_scatter_rows_masked, lib.oracle_ragged_tile_load, lib.oracle_ragged_tile_store, lib.oracle_gemm_f64,
                       lib.oracle_gemm_f64_at, lib.oracle_round_bf16):
                 f.restype = None
             _lib = lib
@@ -139,6 +140,18 @@ def ragged_tile_load(x, total_rows, heads, depth, ld_row, ld_head, cu_seqlens, t
     _load().oracle_ragged_tile_load(_es(x), _p(x), total_rows, heads, depth, ld_row, ld_head, _p(cu), batch,
                                     t_pad, _p(out))
     return out
+
+
+def ragged_tile_store(tiles, x, total_rows, ld_row, ld_head, cu_seqlens):
+    """Ragged 3D store of dense tiles [batch][heads][t_pad][depth] into packed ``x`` (in place)."""
+    tiles, x = _flat_buffer(tiles), _flat_buffer(x)
+    assert tiles.dtype == x.dtype and tiles.ndim == 4
+    cu = np.ascontiguousarray(cu_seqlens, np.int32)
+    batch, heads, t_pad, depth = tiles.shape
+    assert batch == cu.size - 1
+    _load().oracle_ragged_tile_store(_es(x), _p(tiles), batch, heads, depth, t_pad, _p(cu), _p(x), total_rows,
+                                     ld_row, ld_head)
+    return x
 
 
 def gemm_f64(A, lda, B, ldb, M, N, K):

@@ -148,6 +148,32 @@ void oracle_ragged_tile_load(int es, const void* x, int64_t total_rows, int32_t 
     }
 }
 
+/* Ragged 3D tile store, the inverse of the ragged load.
+ * Mojo "RaggedTMA3DTile", async_copy_from_col / async_copy_batched: tiles
+ * are copied from shared memory back to the packed ragged array, only the
+ * first `dynamic_dim` rows (valid sequence positions) of a tile are written
+ * and a box that overhangs the array is masked off.  Here: for b < batch,
+ * h < heads, r < t_pad, d < depth, when r < cu[b+1]-cu[b] and the packed row
+ * cu[b]+r lies in [0, total_rows):
+ *   x[(cu[b]+r)*ld_row + h*ld_head + d] = tiles[((b*heads + h)*t_pad + r)*depth + d];
+ * nothing else of x is written. */
+void oracle_ragged_tile_store(int es, const void* tiles, int32_t batch, int32_t heads, int32_t depth, int32_t t_pad,
+                              const int32_t* cu_seqlens, void* x, int64_t total_rows, int64_t ld_row,
+                              int64_t ld_head) {
+    for (int32_t b = 0; b < batch; ++b) {
+        int64_t off = cu_seqlens[b];
+        int64_t len = (int64_t)cu_seqlens[b + 1] - cu_seqlens[b];
+        for (int32_t h = 0; h < heads; ++h)
+            for (int32_t r = 0; r < t_pad; ++r)
+                for (int32_t d = 0; d < depth; ++d) {
+                    int64_t row = off + r;
+                    if (r < len && row >= 0 && row < total_rows)
+                        put(x, row * ld_row + (int64_t)h * ld_head + d, es,
+                            at(tiles, (((int64_t)b * heads + h) * t_pad + r) * depth + d, es));
+                }
+    }
+}
+
 /* bf16 bits -> double (exact: bf16 is the top half of an IEEE binary32). */
 static double bf16_to_f64(uint16_t b) {
     uint32_t u = (uint32_t)b << 16;

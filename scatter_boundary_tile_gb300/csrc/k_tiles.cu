@@ -11,7 +11,7 @@
 // vector of the tile; cuTile.jl "Memory", "Bounds checking" fixes padding on
 // load and clipping on store.
 //
-// Ragged load: one block per (sequence, head, 128-row tile) work unit, the
+// Ragged load: one block per (sequence, 128-row tile, head) work unit, the
 // unit's valid-row count taken once from cu_seqlens (Mojo "RaggedTMA3DTile":
 // only `dynamic_dim` rows of a tile are valid); rows past the sequence are
 // written as zeros, so the padded output is defined everywhere.
@@ -244,10 +244,12 @@ __global__ void __launch_bounds__(kThreads) k_ragged_load(const RaggedParams p) 
     constexpr int V = VEC ? 16 / ES : 1;
     typedef typename sbt_elem<ES>::T T;
     for (int64_t unit = blockIdx.x; unit < p.units; unit += gridDim.x) {
-        const int rt = (int)(unit % p.n_rt);
-        const int64_t bh = unit / p.n_rt;
-        const int h = (int)(bh % p.heads);
-        const int b = (int)(bh / p.heads);
+        // heads vary fastest, so blocks running together cover whole packed rows
+        const int h = (int)(unit % p.heads);
+        const int64_t brt = unit / p.heads;
+        const int rt = (int)(brt % p.n_rt);
+        const int b = (int)(brt / p.n_rt);
+        const int64_t bh = (int64_t)b * p.heads + h;
         const int64_t off = __ldg(p.cu + b);
         const int64_t len = (int64_t)__ldg(p.cu + b + 1) - off;
         const int r0 = rt * kRaggedRows;
@@ -301,6 +303,67 @@ sbt_status launch_tiles(sbt_context* ctx, Kern kern, TileParams p, int64_t ntile
         if (st) return st;
     }
     return SBT_OK;
+}
+
+// Inverse of k_ragged_load: only the unit's valid rows are read from the
+// tiles and written to the packed array; rows past the sequence are skipped.
+template <int ES, bool VEC>
+__global__ void __launch_bounds__(kThreads) k_ragged_store(const RaggedParams p) {
+    constexpr int V = VEC ? 16 / ES : 1;
+    typedef typename sbt_elem<ES>::T T;
+    for (int64_t unit = blockIdx.x; unit < p.units; unit += gridDim.x) {
+        // heads vary fastest, so blocks running together cover whole packed rows
+        const int h = (int)(unit % p.heads);
+        const int64_t brt = unit / p.heads;
+        const int rt = (int)(brt % p.n_rt);
+        const int b = (int)(brt / p.n_rt);
+        const int64_t bh = (int64_t)b * p.heads + h;
+        const int64_t off = __ldg(p.cu + b);
+        const int64_t len = (int64_t)__ldg(p.cu + b + 1) - off;
+        const int r0 = rt * kRaggedRows;
+        const int nrows = p.t_pad - r0 < kRaggedRows ? p.t_pad - r0 : kRaggedRows;
+        int64_t nvalid = len - r0;
+        nvalid = nvalid < 0 ? 0 : (nvalid > nrows ? nrows : nvalid);
+        if (nvalid == 0) continue;
+        const char* in_tile = p.x + ((bh * p.t_pad + r0) * (int64_t)p.depth) * ES;
+        const int ntask = (int)nvalid * p.per_row;
+        for (int base = threadIdx.x; base < ntask; base += kThreads * kRaggedUnroll) {
+            uint4 vv[kRaggedUnroll];
+            T sv[kRaggedUnroll];
+#pragma unroll
+            for (int u = 0; u < kRaggedUnroll; ++u) {
+                const int t = base + u * kThreads;
+                if (t < ntask) {
+                    if (VEC)
+                        vv[u] = sbt_ld_nc_v4(in_tile + (int64_t)t * 16);
+                    else
+                        sv[u] = ld_elem<ES>(in_tile, t);
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kRaggedUnroll; ++u) {
+                const int t = base + u * kThreads;
+                if (t >= ntask) continue;
+                const int i = t / p.per_row;
+                const int j = (t - i * p.per_row) * V;
+                const int64_t row = off + r0 + i;
+                if (row < 0 || row >= p.total_rows) continue;
+                const int64_t dst = row * p.ld_row + (int64_t)h * p.ld_head + j;
+                if (VEC)
+                    sbt_st_v4(p.out + dst * ES, vv[u]);
+                else
+                    st_elem<ES>(p.out, dst, sv[u]);
+            }
+        }
+    }
+}
+
+template <int ES, bool VEC>
+sbt_status launch_ragged_store_t(sbt_context* ctx, const RaggedParams& p, cudaStream_t s) {
+    auto kern = k_ragged_store<ES, VEC>;
+    const int grid = sbt_persistent_grid(ctx, (const void*)kern, kThreads, 0, p.units);
+    kern<<<grid, kThreads, 0, s>>>(p);
+    return sbt_after_launch(ctx, "ragged_tile_store");
 }
 
 template <int ES, bool VEC>
@@ -442,4 +505,30 @@ sbt_status sbt_launch_ragged(sbt_context* ctx, int es, const void* x, int64_t to
     p.units = (int64_t)batch * heads * p.n_rt;
     if (es == 4) return vec ? launch_ragged_t<4, true>(ctx, p, stream) : launch_ragged_t<4, false>(ctx, p, stream);
     return vec ? launch_ragged_t<2, true>(ctx, p, stream) : launch_ragged_t<2, false>(ctx, p, stream);
+}
+
+sbt_status sbt_launch_ragged_store(sbt_context* ctx, int es, const void* tiles, int32_t batch, int32_t heads,
+                                   int32_t depth, int32_t t_pad, const int32_t* cu_seqlens, void* x,
+                                   int64_t total_rows, int64_t ld_row, int64_t ld_head, cudaStream_t stream) {
+    const int V = 16 / es;
+    bool vec = (depth % V) == 0 && sbt_aligned16(tiles) && sbt_aligned16(x) && sbt_mul16(ld_row, es) &&
+               sbt_mul16(ld_head, es);
+    if (ctx->path == SBT_PATH_SCALAR) vec = false;
+    RaggedParams p;
+    p.x = (const char*)tiles;  // the dense side is read here
+    p.out = (char*)x;          // and the packed side written
+    p.cu = cu_seqlens;
+    p.total_rows = total_rows;
+    p.ld_row = ld_row;
+    p.ld_head = ld_head;
+    p.heads = heads;
+    p.depth = depth;
+    p.batch = batch;
+    p.t_pad = t_pad;
+    p.n_rt = (int32_t)sbt_cdiv(t_pad, kRaggedRows);
+    p.per_row = vec ? depth / V : depth;
+    p.units = (int64_t)batch * heads * p.n_rt;
+    if (es == 4)
+        return vec ? launch_ragged_store_t<4, true>(ctx, p, stream) : launch_ragged_store_t<4, false>(ctx, p, stream);
+    return vec ? launch_ragged_store_t<2, true>(ctx, p, stream) : launch_ragged_store_t<2, false>(ctx, p, stream);
 }

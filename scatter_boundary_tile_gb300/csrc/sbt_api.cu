@@ -256,6 +256,23 @@ sbt_status sbt_ragged_tile_load(sbt_context* ctx, sbt_dtype dtype, const void* x
                              (cudaStream_t)stream);
 }
 
+sbt_status sbt_ragged_tile_store(sbt_context* ctx, sbt_dtype dtype, const void* tiles, int32_t batch, int32_t heads,
+                                 int32_t depth, int32_t t_pad, const int32_t* cu_seqlens, void* x, int64_t total_rows,
+                                 int64_t ld_row, int64_t ld_head, void* stream) {
+    SBT_REQUIRE(ctx, "ctx is NULL");
+    int es;
+    sbt_status st = check_dtype_move(dtype, &es);
+    if (st) return st;
+    SBT_REQUIRE(total_rows >= 0 && heads >= 0 && depth >= 0 && batch >= 0 && t_pad >= 0,
+                "ragged_tile_store: negative extent");
+    if ((int64_t)batch * heads * t_pad * depth == 0 || total_rows == 0) return SBT_OK;
+    SBT_REQUIRE(tiles && cu_seqlens && x, "ragged_tile_store: NULL pointer");
+    SBT_REQUIRE(ld_row > 0 && ld_head > 0, "ragged_tile_store: strides must be positive");
+    if ((st = sbt_use_device(ctx))) return st;
+    return sbt_launch_ragged_store(ctx, es, tiles, batch, heads, depth, t_pad, cu_seqlens, x, total_rows, ld_row,
+                                   ld_head, (cudaStream_t)stream);
+}
+
 sbt_status sbt_gemm_bounded_workspace_size(sbt_context* ctx, int64_t M, int64_t N, int64_t K, int64_t lda,
                                            int64_t ldb, size_t* bytes) {
     SBT_REQUIRE(ctx && bytes, "NULL argument");

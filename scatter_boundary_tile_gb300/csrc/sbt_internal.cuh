@@ -76,6 +76,9 @@ sbt_status sbt_launch_scatter(sbt_context* ctx, int es, void* dst, int64_t rows,
 sbt_status sbt_launch_ragged(sbt_context* ctx, int es, const void* x, int64_t total_rows, int32_t heads,
                              int32_t depth, int64_t ld_row, int64_t ld_head, const int32_t* cu_seqlens,
                              int32_t batch, int32_t t_pad, void* out, cudaStream_t stream);
+sbt_status sbt_launch_ragged_store(sbt_context* ctx, int es, const void* tiles, int32_t batch, int32_t heads,
+                                   int32_t depth, int32_t t_pad, const int32_t* cu_seqlens, void* x,
+                                   int64_t total_rows, int64_t ld_row, int64_t ld_head, cudaStream_t stream);
 sbt_status sbt_launch_gemm(sbt_context* ctx, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
                            int64_t ldc, sbt_dtype c_dtype, int64_t M, int64_t N, int64_t K, void* workspace,
                            size_t workspace_bytes, cudaStream_t stream);

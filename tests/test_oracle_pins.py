@@ -291,6 +291,36 @@ def test_ragged_empty_and_out_of_range_metadata():
     assert not out[2, :, 2:].any()
 
 
+def test_ragged_store_inverts_the_load_and_writes_nothing_else():
+    d = synth.workloads.ragged_bf16(batch=7, max_len=60, heads=3, depth=8)
+    x, cu, lens, total = d["x"], d["cu_seqlens"], d["lens"], d["total_rows"]
+    t_pad = 64
+    tiles = synth.normal_bf16(43, (7, 3, t_pad, 8))
+    canvas = np.full((total, 3, 8), 0xDEAD, np.uint16)
+    oracle.ragged_tile_store(tiles, canvas, total, 24, 8, cu)
+    for b in range(7):
+        L = int(lens[b])
+        # numpy slicing: packed rows of sequence b are the first L rows of its tiles
+        np.testing.assert_array_equal(canvas[cu[b]:cu[b] + L], tiles[b, :, :L].transpose(1, 0, 2))
+    # every packed row belongs to one sequence, so nothing keeps the canary
+    assert not np.any(canvas == 0xDEAD)
+    # load then store reproduces the packed array exactly
+    back = np.zeros_like(x)
+    oracle.ragged_tile_store(oracle.ragged_tile_load(x, total, 3, 8, 24, 8, cu, t_pad), back, total, 24, 8, cu)
+    np.testing.assert_array_equal(back, x)
+
+
+def test_ragged_store_clips_long_sequences_and_bad_metadata():
+    tiles = synth.normal_bf16(44, (3, 2, 4, 4))
+    x = np.full((12, 2, 4), 0x1234, np.uint16)
+    cu = np.array([0, 6, 6, 14], np.int32)  # len 6 > t_pad 4; an empty sequence; len 8 > t_pad
+    oracle.ragged_tile_store(tiles, x, 12, 8, 4, cu)
+    np.testing.assert_array_equal(x[0:4], tiles[0].transpose(1, 0, 2))
+    assert np.all(x[4:6] == 0x1234)          # rows past t_pad of sequence 0: not written
+    np.testing.assert_array_equal(x[6:10], tiles[2].transpose(1, 0, 2))
+    assert np.all(x[10:12] == 0x1234)        # sequence 2's rows 4.. are past t_pad
+
+
 # ----------------------------------------------------------------------------- GEMM and bf16 rounding
 
 def _bits_of(vals):

@@ -73,3 +73,62 @@ def test_full_size_workload_bit_exact(ctx):
     got = host(out, np.uint16, (64, 8, 4096, 128))
     want = oracle.ragged_tile_load(x, d["total_rows"], 8, 128, 1024, 128, cu, 4096)
     assert np.array_equal(got, want)
+
+
+# ----------------------------------------------------------------------------- ragged store (the inverse)
+
+def gpu_ragged_store(ctx, tiles, x_init, total_rows, ld_row, ld_head, cu, dtype, path="auto"):
+    batch, heads, t_pad, depth = tiles.shape
+    canvas = Canvas(x_init.nbytes, fill=x_init)
+    td, cd = dev(tiles), dev(cu.astype(np.int32))
+    ctx.set_path(path)
+    sbt.ragged_tile_store(ctx, td, batch, heads, depth, t_pad, cd, canvas.ptr, total_rows, ld_row, ld_head,
+                          dtype=dtype)
+    sync()
+    assert canvas.guards_intact()
+    return canvas.inner(x_init.dtype, x_init.shape)
+
+
+@pytest.mark.parametrize("t_pad", [300, 256, 100, 129])
+@pytest.mark.parametrize("depth", [128, 24, 20])
+def test_store_small_batches(ctx, t_pad, depth):
+    d = wl.ragged_bf16(batch=5, max_len=300, heads=3, depth=depth)
+    cu, total = d["cu_seqlens"], d["total_rows"]
+    tiles = synth.normal_bf16(404, (5, 3, t_pad, depth))
+    x0 = np.full((total, 3, depth), 0xDEAD, np.uint16)
+    want = oracle.ragged_tile_store(tiles, x0.copy(), total, 3 * depth, depth, cu)
+    for path in ("auto", "scalar"):
+        got = gpu_ragged_store(ctx, tiles, x0, total, 3 * depth, depth, cu, "bf16", path=path)
+        assert np.array_equal(got, want), path
+
+
+def test_store_fp32_strided_heads_and_bad_metadata(ctx):
+    total, H, D, ldh, ldr = 90, 4, 32, 40, 168
+    # negative start (rows -3..4), an empty sequence, one running past total_rows; none overlap
+    cu = np.array([-3, 5, 10, 10, 70, 90, 95], np.int32)
+    tiles = synth.uniform_f32(405, (6, H, 64, D), 1.0, 2.0)
+    x0 = np.full((total, ldr), wl.F32_CANARY_BITS, np.uint32).view(np.float32)
+    want = oracle.ragged_tile_store(tiles, x0.copy(), total, ldr, ldh, cu)
+    got = gpu_ragged_store(ctx, tiles, x0, total, ldr, ldh, cu, "f32")
+    assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
+
+
+def test_store_round_trip(ctx):
+    d = wl.ragged_bf16(batch=9, max_len=700, heads=8, depth=128)
+    x, cu, total = d["x"], d["cu_seqlens"], d["total_rows"]
+    tiles = gpu_ragged(ctx, x, total, 8, 128, 1024, 128, cu, 700, "bf16")
+    back = gpu_ragged_store(ctx, tiles, np.zeros_like(x), total, 1024, 128, cu, "bf16")
+    assert np.array_equal(back, x)
+
+
+def test_store_full_size_workload_bit_exact(ctx):
+    """batch 64, lengths uniform in [1, 4096], 8 heads, depth 128: [64][8][4096][128] bf16 tiles
+    stored back into the packed array; the whole packed array is compared."""
+    d = wl.ragged_bf16()
+    cu, total = d["cu_seqlens"], d["total_rows"]
+    tiles = synth.normal_bf16(406, (64, 8, 4096, 128))
+    xd = torch.zeros(total * 1024 * 2, dtype=torch.uint8, device="cuda")
+    sbt.ragged_tile_store(ctx, dev(tiles), 64, 8, 128, 4096, dev(cu), xd, total, 1024, 128, dtype="bf16")
+    got = host(xd, np.uint16, (total, 8, 128))
+    want = oracle.ragged_tile_store(tiles, np.zeros((total, 8, 128), np.uint16), total, 1024, 128, cu)
+    assert np.array_equal(got, want)
