@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=8.0, help="CPU-baseline sample budget")
     ap.add_argument("--profile", default=None,
-                    choices=["gather", "scatter", "ragged", "ragged_store", "tile_load", "tile_store", "tile_load_unaligned",
+                    choices=["gather", "scatter", "scatter_add", "ragged", "ragged_store", "tile_load", "tile_store", "tile_load_unaligned",
                              "tile_store_unaligned", "gemm"],
                     help="only launch one operation's workload (warmup + steps launches) for ncu")
     ap.add_argument("--scale", type=float, default=1.0, help="--profile: fraction of the workload's rows")
@@ -295,6 +295,25 @@ def run_ops(ctx, pk):
                                   "algorithmic_bytes": nbytes}
     del dst, s, i, m, d
 
+    # row scatter-add: the backward of the headline gather (bf16 gradients into a zero table)
+    import synth
+    g = wl.gather_rows_bf16()
+    n = g["idx"].size
+    grad = synth.normal_bf16(0x5B7102, (n, 512))
+    table = torch.zeros(1_000_000 * 512 * 2, dtype=torch.uint8, device="cuda")
+    gi, gg = dev_bytes(g["idx"]), dev_bytes(grad)
+    fn = lambda: sbt.scatter_add_rows(ctx, table, 1_000_000, 512, 512, gi, n, gg, 512, 512, dtype="bf16")
+    med, mean, best = time_launches(fn, 20)
+    valid = (g["idx"] >= 0) & (g["idx"] < 1_000_000)
+    uniq = int(np.unique(g["idx"][valid]).size)
+    nbytes = n * 1024 + n * 4 + 2 * uniq * 1024
+    ops["scatter_add_rows"] = {"workload": "bf16 gradients 1,048,576x512 added into a 1,000,000x512 table through "
+                                           "the gather's indices (repeats accumulate)",
+                               "ms": med, "GB/s": nbytes / med / 1e6, "frac_hbm": nbytes / med / 1e6 / hbm,
+                               "algorithmic_bytes": nbytes,
+                               "note": "bytes = gradients + indices + each distinct target row read and written once"}
+    del table, gi, gg, grad, g
+
     # ragged 3D tile load
     d = wl.ragged_bf16()
     out = torch.empty(64 * 8 * 4096 * 128 * 2, dtype=torch.uint8, device="cuda")
@@ -533,6 +552,13 @@ def run_profile(args):
         x, cu = dev_bytes(d["x"]), dev_bytes(d["cu_seqlens"])
         fn = lambda: sbt.ragged_tile_load(ctx, x, d["total_rows"], 8, 128, 1024, 128, cu, b, 4096, out,
                                           dtype="bf16")
+    elif op == "scatter_add":
+        d = wl.gather_rows_bf16(n_rows=max(1, int(1_000_000 * f)), n_idx=max(1, int(1_048_576 * f)))
+        n, rows = d["idx"].size, d["n_rows"]
+        grad = synth.normal_bf16(0x5B7102, (n, 512))
+        table = torch.zeros(rows * 512 * 2, dtype=torch.uint8, device="cuda")
+        gi, gg = dev_bytes(d["idx"]), dev_bytes(grad)
+        fn = lambda: sbt.scatter_add_rows(ctx, table, rows, 512, 512, gi, n, gg, 512, 512, dtype="bf16")
     elif op == "ragged_store":
         d = wl.ragged_bf16(batch=max(1, int(64 * f)))
         b = d["cu_seqlens"].size - 1

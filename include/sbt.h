@@ -168,6 +168,27 @@ SBT_API sbt_status sbt_scatter_rows_masked(sbt_context* ctx, sbt_dtype dtype, vo
                                    const uint8_t* mask, int64_t ld_mask, void* stream);
 
 /*
+ * Row scatter-add: the adjoint (backward) of sbt_gather_rows.
+ * warp.tile_load_indexed, description: in a backward pass the adjoint of the
+ * gathered tile is accumulated atomically into the array's gradient at the
+ * gathered locations.
+ *
+ *   for k < n_idx, j < tile_c: if r = row_offset + idx[k] in [0, rows) and
+ *   c = col_offset + j in [0, cols):  dst[r*ld_dst + c] += src[k*ld_src + j]
+ *
+ * Each addition is done in the element type (SBT_F32, SBT_BF16 or SBT_F16)
+ * with one rounding to nearest even, by the memory system's atomic add, so
+ * repeated indices accumulate; their order is unspecified (results with
+ * repeats may differ in the last bits from run to run).  Elements that read
+ * padding in the forward pass contribute nothing.  Subnormal fp32 results
+ * are outside the contract (the GPU's fp32 atomic add may flush them).
+ */
+SBT_API sbt_status sbt_scatter_add_rows(sbt_context* ctx, sbt_dtype dtype, void* dst, int64_t rows, int64_t cols,
+                                        int64_t ld_dst, const int32_t* idx, int64_t n_idx, int64_t row_offset,
+                                        int64_t col_offset, const void* src, int64_t ld_src, int32_t tile_c,
+                                        void* stream);
+
+/*
  * Ragged 3D tile load.
  * Mojo "RaggedTMA3DTile", struct description: a packed array
  * [total_rows][heads][depth] whose leading dimension concatenates sequences,

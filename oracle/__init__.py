@@ -45,6 +45,8 @@ def _load():
             lib.oracle_scatter_rows_masked.argtypes = [ci, p, i64, i64, i64, p, i64, i64, i64, p, i64, i32,
                                                        p, i64]
             lib.oracle_ragged_tile_load.argtypes = [ci, p, i64, i32, i32, i64, i64, p, i32, i32, p]
+            lib.oracle_scatter_add_rows.argtypes = [ci, p, i64, i64, i64, p, i64, i64, i64, p, i64, i32]
+            lib.oracle_scatter_add_rows.restype = None
             lib.oracle_ragged_tile_store.argtypes = [ci, p, i32, i32, i32, i32, p, p, i64, i64, i64]
             lib.oracle_gemm_f64.argtypes = [p, i64, p, i64, i64, i64, i64, p, i64]
             lib.oracle_gemm_f64_at.argtypes = [p, i64, p, i64, i64, p, p, i64, p]
@@ -140,6 +142,20 @@ def ragged_tile_load(x, total_rows, heads, depth, ld_row, ld_head, cu_seqlens, t
     _load().oracle_ragged_tile_load(_es(x), _p(x), total_rows, heads, depth, ld_row, ld_head, _p(cu), batch,
                                     t_pad, _p(out))
     return out
+
+
+def scatter_add_rows(dst, rows, cols, ld_dst, idx, src, ld_src, tile_c, row_offset=0, col_offset=0, kind=None):
+    """Row scatter-add into ``dst`` (in place).  kind: 'f32', 'bf16' or 'f16' (2-byte arrays
+    default to bf16)."""
+    dst, src = _flat_buffer(dst), _flat_buffer(src)
+    assert dst.dtype == src.dtype
+    if kind is None:
+        kind = "f32" if dst.dtype.itemsize == 4 else "bf16"
+    code = {"f32": 4, "bf16": 2, "f16": 3}[kind]
+    idx = np.ascontiguousarray(idx, np.int32)
+    _load().oracle_scatter_add_rows(code, _p(dst), rows, cols, ld_dst, _p(idx), idx.size, row_offset, col_offset,
+                                    _p(src), ld_src, tile_c)
+    return dst
 
 
 def ragged_tile_store(tiles, x, total_rows, ld_row, ld_head, cu_seqlens):

@@ -148,6 +148,72 @@ void oracle_ragged_tile_load(int es, const void* x, int64_t total_rows, int32_t 
     }
 }
 
+static float f32_of(const void* p) { float f; memcpy(&f, p, 4); return f; }
+static double bf16_bits_f64(uint16_t b) { uint32_t u = (uint32_t)b << 16; float f; memcpy(&f, &u, 4); return (double)f; }
+static double f16_bits_f64(uint16_t h) {
+    int e = (h >> 10) & 0x1F, m = h & 0x3FF;
+    double v = e == 0 ? ldexp((double)m, -24) : (e == 31 ? (m ? NAN : INFINITY) : ldexp((double)(m | 0x400), e - 25));
+    return (h & 0x8000) ? -v : v;
+}
+uint16_t oracle_bf16_rne(double x);
+/* double -> binary16 bits, round to nearest even (spacing 2^(e-11) for normals, 2^-24 below 2^-14). */
+static uint16_t f16_rne(double x) {
+    if (isnan(x)) return 0x7E00;
+    uint16_t sign = signbit(x) ? 0x8000 : 0;
+    double a = fabs(x);
+    if (a == 0.0) return sign;
+    int e;
+    frexp(a, &e);
+    int q_exp = e - 11 > -24 ? e - 11 : -24;
+    double q = rint(ldexp(a, -q_exp));
+    double y = ldexp(q, q_exp);
+    if (y >= 65520.0 || isinf(a)) return sign | 0x7C00;
+    if (y < 0x1p-14) return sign | (uint16_t)rint(ldexp(y, 24));
+    frexp(y, &e);
+    int m = (int)rint(ldexp(y, 11 - e)) - 0x400;
+    return sign | (uint16_t)(((e + 14) << 10) | m);
+}
+
+/* Row scatter-add, the adjoint of the row gather.
+ * warp.tile_load_indexed, description: in a backward pass the adjoint of the
+ * gathered tile is accumulated atomically into the array's gradient at the
+ * gathered locations.  Source element (k, j) is added to dst row
+ * row_offset + idx[k], column col_offset + j, when that coordinate is inside
+ * the array; elements that read padding in the forward pass have no location
+ * and add nothing.  Each addition happens in the element type with one
+ * rounding to nearest even (the exact sum of two values of the type is formed
+ * in double first: double has more than 2p+2 significand bits for p = 24, 11
+ * or 8, so rounding it again to the type is the correctly rounded sum).
+ * es/kind: 4 = fp32, 2 = bf16, 3 = fp16 (2-byte storage). */
+void oracle_scatter_add_rows(int kind, void* dst, int64_t rows, int64_t cols, int64_t ld_dst, const int32_t* idx,
+                             int64_t n_idx, int64_t row_offset, int64_t col_offset, const void* src, int64_t ld_src,
+                             int32_t tile_c) {
+    int es = kind == 4 ? 4 : 2;
+    for (int64_t k = 0; k < n_idx; ++k) {
+        int64_t r = (int64_t)idx[k] + row_offset;
+        if (r < 0 || r >= rows) continue;
+        for (int32_t j = 0; j < tile_c; ++j) {
+            int64_t c = col_offset + j;
+            if (c < 0 || c >= cols) continue;
+            char* d = (char*)dst + (r * ld_dst + c) * es;
+            const char* s = (const char*)src + (k * ld_src + j) * es;
+            if (kind == 4) {
+                float v = (float)((double)f32_of(d) + (double)f32_of(s));
+                memcpy(d, &v, 4);
+            } else {
+                uint16_t a, b, out;
+                memcpy(&a, d, 2);
+                memcpy(&b, s, 2);
+                if (kind == 2)
+                    out = oracle_bf16_rne(bf16_bits_f64(a) + bf16_bits_f64(b));
+                else
+                    out = f16_rne(f16_bits_f64(a) + f16_bits_f64(b));
+                memcpy(d, &out, 2);
+            }
+        }
+    }
+}
+
 /* Ragged 3D tile store, the inverse of the ragged load.
  * Mojo "RaggedTMA3DTile", async_copy_from_col / async_copy_batched: tiles
  * are copied from shared memory back to the packed ragged array, only the

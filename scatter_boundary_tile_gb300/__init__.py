@@ -7,7 +7,7 @@ an op raises.
 
 Op names match the C ABI in ``include/sbt.h`` without the ``sbt_`` prefix:
 ``tile_load_padded``, ``tile_store_clipped``, ``gather_rows``,
-``scatter_rows_masked``, ``ragged_tile_load``, ``ragged_tile_store``, ``gemm_bounded`` (plus
+``scatter_rows_masked``, ``scatter_add_rows``, ``ragged_tile_load``, ``ragged_tile_store``, ``gemm_bounded`` (plus
 ``gemm_bounded_workspace_size``).  Arrays are torch tensors on the device
 (only their data pointer is used; shapes and strides are the explicit
 arguments, in elements).
@@ -32,7 +32,7 @@ PATHS = {"auto": 0, "scalar": 1, "vector": 2, "tma": 3}
 # Every symbol include/sbt.h declares.
 EXPORTS = ("sbt_create", "sbt_destroy", "sbt_set_path", "sbt_set_wait_limit_ns", "sbt_set_test_hook", "sbt_launch_count",
            "sbt_check_status", "sbt_last_error_message", "sbt_tile_load_padded", "sbt_tile_store_clipped",
-           "sbt_gather_rows", "sbt_scatter_rows_masked", "sbt_ragged_tile_load", "sbt_ragged_tile_store", "sbt_gemm_bounded_workspace_size",
+           "sbt_gather_rows", "sbt_scatter_rows_masked", "sbt_scatter_add_rows", "sbt_ragged_tile_load", "sbt_ragged_tile_store", "sbt_gemm_bounded_workspace_size",
            "sbt_gemm_bounded", "sbt_gemm_bounded_noalloc")
 GEMM_NOALLOC_SCRATCH_BYTES = 16 << 20  # SBT_GEMM_NOALLOC_SCRATCH_BYTES in include/sbt.h
 
@@ -68,6 +68,7 @@ def load_library(path: str = LIB_PATH):
             "sbt_tile_store_clipped": [p, ci, p, i32, i32, i32, i32, p, i64, i64, i64, i64, i64, i64, i64, i64, p],
             "sbt_gather_rows": [p, ci, p, i64, i64, i64, p, i64, i64, i64, i32, p, i64, p, i64, p, p],
             "sbt_scatter_rows_masked": [p, ci, p, i64, i64, i64, p, i64, i64, i64, p, i64, i32, p, i64, p],
+            "sbt_scatter_add_rows": [p, ci, p, i64, i64, i64, p, i64, i64, i64, p, i64, i32, p],
             "sbt_ragged_tile_load": [p, ci, p, i64, i32, i32, i64, i64, p, i32, i32, p, p],
             "sbt_ragged_tile_store": [p, ci, p, i32, i32, i32, i32, p, p, i64, i64, i64, p],
             "sbt_gemm_bounded_workspace_size": [p, i64, i64, i64, i64, i64, ctypes.POINTER(ctypes.c_size_t)],
@@ -210,6 +211,13 @@ def scatter_rows_masked(ctx, dst, rows, cols, ld_dst, idx, n_idx, src, ld_src, t
     _check(load_library().sbt_scatter_rows_masked(ctx.handle, code, _ptr(dst), rows, cols, ld_dst, _ptr(idx), n_idx,
                                                   row_offset, col_offset, _ptr(src), ld_src, tile_c, _ptr(mask),
                                                   ld_mask, _stream(stream)))
+
+
+def scatter_add_rows(ctx, dst, rows, cols, ld_dst, idx, n_idx, src, ld_src, tile_c, row_offset=0, col_offset=0,
+                     dtype=None, stream=None):
+    code = _dtype_code(dst, dtype)
+    _check(load_library().sbt_scatter_add_rows(ctx.handle, code, _ptr(dst), rows, cols, ld_dst, _ptr(idx), n_idx,
+                                               row_offset, col_offset, _ptr(src), ld_src, tile_c, _stream(stream)))
 
 
 def ragged_tile_load(ctx, x, total_rows, heads, depth, ld_row, ld_head, cu_seqlens, batch, t_pad, out, dtype=None,

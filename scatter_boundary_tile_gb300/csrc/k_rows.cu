@@ -305,6 +305,112 @@ __global__ void __launch_bounds__(kThreads) k_scatter_rows(const RowParams p) {
     }
 }
 
+// ---------------------------------------------------------------------------- scatter-add (gather backward)
+
+// Element-type additions done by the L2 (red = reduction without a return value).
+// KIND: 4 = fp32, 2 = bf16, 3 = fp16; rounding to nearest even, no flush of subnormals
+// for the 16-bit types.
+template <int KIND>
+__device__ __forceinline__ void red_add_v4(char* p, const uint4& v) {
+    if (KIND == 4)
+        asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(__uint_as_float(v.x)),
+                     "f"(__uint_as_float(v.y)), "f"(__uint_as_float(v.z)), "f"(__uint_as_float(v.w))
+                     : "memory");
+    else if (KIND == 2)
+        asm volatile("red.global.add.noftz.v4.bf16x2 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                     "r"(v.z), "r"(v.w)
+                     : "memory");
+    else
+        asm volatile("red.global.add.noftz.v4.f16x2 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+                     "r"(v.z), "r"(v.w)
+                     : "memory");
+}
+
+template <int KIND>
+__device__ __forceinline__ void red_add_elem(char* p, uint32_t bits) {
+    if (KIND == 4)
+        asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(__uint_as_float(bits)) : "memory");
+    else if (KIND == 2)
+        asm volatile("red.global.add.noftz.bf16 [%0], %1;" ::"l"(p), "h"((unsigned short)bits) : "memory");
+    else
+        asm volatile("red.global.add.noftz.f16 [%0], %1;" ::"l"(p), "h"((unsigned short)bits) : "memory");
+}
+
+template <int KIND, bool VEC>
+__global__ void __launch_bounds__(kThreads) k_scatter_add_rows(const RowParams p) {
+    __shared__ int64_t s_row[2][kChunkRows];
+    __shared__ uint32_t s_valid[2];
+    constexpr int ES = KIND == 4 ? 4 : 2;
+    constexpr int V = 16 / ES;
+    typedef typename sbt_elem<ES>::T T;
+    const int64_t nchunks = (p.n_idx + kChunkRows - 1) / kChunkRows;
+    const bool stager = threadIdx.x < 32;
+    if (stager) finish_index_stage(p, blockIdx.x, nchunks, issue_index_load(p, blockIdx.x, nchunks), s_row[0], &s_valid[0]);
+    __syncthreads();
+    int buf = 0;
+    for (int64_t chunk = blockIdx.x; chunk < nchunks; chunk += gridDim.x, buf ^= 1) {
+        const int64_t next = chunk + gridDim.x;
+        const int32_t next_raw = stager ? issue_index_load(p, next, nchunks) : 0;
+        const int64_t k0 = chunk * kChunkRows;
+        const int nrows = (int)(p.n_idx - k0 < kChunkRows ? p.n_idx - k0 : kChunkRows);
+        const uint32_t valid = s_valid[buf];
+        const int64_t* rows_of = s_row[buf];
+        const int per_row = VEC ? p.nvec : p.tile_c;
+        const int ntask = nrows * per_row;
+        for (int base = threadIdx.x; base < ntask; base += kThreads * kUnroll) {
+            uint4 val[kUnroll];
+            T sv[kUnroll];
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int t = base + u * kThreads;
+                if (t < ntask) {
+                    const int row = t / per_row;
+                    const int j = (t - row * per_row) * (VEC ? V : 1);
+                    if ((valid >> row) & 1u) {
+                        if (VEC)
+                            val[u] = sbt_ld_nc_v4(p.src + ((k0 + row) * p.ld_dense + j) * ES);
+                        else
+                            sv[u] = ld_elem<ES>(p.src, (k0 + row) * p.ld_dense + j);
+                    }
+                }
+            }
+#pragma unroll
+            for (int u = 0; u < kUnroll; ++u) {
+                const int t = base + u * kThreads;
+                if (t >= ntask) continue;
+                const int row = t / per_row;
+                if (!((valid >> row) & 1u)) continue;
+                const int j = (t - row * per_row) * (VEC ? V : 1);
+                const int64_t c0 = p.col_offset + j;
+                char* drow = p.dst + rows_of[row] * p.ld_arr * ES;
+                if (VEC) {
+                    if (c0 >= 0 && c0 + V <= p.cols) {
+                        red_add_v4<KIND>(drow + c0 * ES, val[u]);
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < V; ++e) {
+                            const int64_t c = c0 + e;
+                            if (c >= 0 && c < p.cols) red_add_elem<KIND>(drow + c * ES, sbt_vec_get<ES>(val[u], e));
+                        }
+                    }
+                } else if (c0 >= 0 && c0 < p.cols) {
+                    red_add_elem<KIND>(drow + c0 * ES, (uint32_t)sv[u]);
+                }
+            }
+        }
+        if (stager) finish_index_stage(p, next, nchunks, next_raw, s_row[buf ^ 1], &s_valid[buf ^ 1]);
+        __syncthreads();
+    }
+}
+
+template <int KIND, bool VEC>
+sbt_status launch_scatter_add_t(sbt_context* ctx, const RowParams& p, cudaStream_t stream) {
+    auto kern = k_scatter_add_rows<KIND, VEC>;
+    const int grid = sbt_persistent_grid(ctx, (const void*)kern, kThreads, 0, sbt_cdiv(p.n_idx, kChunkRows));
+    kern<<<grid, kThreads, 0, stream>>>(p);
+    return sbt_after_launch(ctx, "scatter_add_rows");
+}
+
 template <int ES, bool VEC, int MM>
 sbt_status launch_gather_t(sbt_context* ctx, const RowParams& p, cudaStream_t stream) {
     auto kern = k_gather_rows<ES, VEC, MM>;
@@ -420,4 +526,33 @@ sbt_status sbt_launch_scatter(sbt_context* ctx, int es, void* dst, int64_t rows,
     const int mm = pick_mask_mode(es, vec, mask, ld_mask);
     return es == 4 ? dispatch_rows<4>(ctx, false, vec, mm, p, stream)
                    : dispatch_rows<2>(ctx, false, vec, mm, p, stream);
+}
+
+sbt_status sbt_launch_scatter_add(sbt_context* ctx, int kind, void* dst, int64_t rows, int64_t cols, int64_t ld_dst,
+                                  const int32_t* idx, int64_t n_idx, int64_t row_offset, int64_t col_offset,
+                                  const void* src, int64_t ld_src, int32_t tile_c, cudaStream_t stream) {
+    const int es = kind == 4 ? 4 : 2;
+    RowParams p;
+    p.src = (const char*)src;
+    p.dst = (char*)dst;
+    p.idx = idx;
+    p.mask = nullptr;
+    p.rows = rows;
+    p.cols = cols;
+    p.ld_arr = ld_dst;
+    p.ld_dense = ld_src;
+    p.ld_mask = 0;
+    p.n_idx = n_idx;
+    p.row_offset = row_offset;
+    p.col_offset = col_offset;
+    p.tile_c = tile_c;
+    p.pad_word = 0;
+    bool vec = rows_vector_ok(es, dst, ld_dst, col_offset, src, ld_src, tile_c);
+    if (ctx->path == SBT_PATH_SCALAR) vec = false;
+    p.nvec = vec ? tile_c / (16 / es) : 0;
+#define SBT_SA(K_) return vec ? launch_scatter_add_t<K_, true>(ctx, p, stream) : launch_scatter_add_t<K_, false>(ctx, p, stream)
+    if (kind == 4) SBT_SA(4);
+    if (kind == 2) SBT_SA(2);
+    SBT_SA(3);
+#undef SBT_SA
 }

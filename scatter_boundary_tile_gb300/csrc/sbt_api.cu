@@ -256,6 +256,24 @@ sbt_status sbt_ragged_tile_load(sbt_context* ctx, sbt_dtype dtype, const void* x
                              (cudaStream_t)stream);
 }
 
+sbt_status sbt_scatter_add_rows(sbt_context* ctx, sbt_dtype dtype, void* dst, int64_t rows, int64_t cols,
+                                int64_t ld_dst, const int32_t* idx, int64_t n_idx, int64_t row_offset,
+                                int64_t col_offset, const void* src, int64_t ld_src, int32_t tile_c, void* stream) {
+    SBT_REQUIRE(ctx, "ctx is NULL");
+    const int kind = dtype == SBT_F32 ? 4 : dtype == SBT_BF16 ? 2 : dtype == SBT_F16 ? 3 : 0;
+    if (!kind) return sbt_fail(SBT_ERR_UNSUPPORTED, "scatter_add_rows: dtype must be SBT_F32, SBT_BF16 or SBT_F16");
+    SBT_REQUIRE(rows >= 0 && cols >= 0 && n_idx >= 0, "scatter_add_rows: negative extent");
+    SBT_REQUIRE(tile_c >= 1 && tile_c <= 65536, "scatter_add_rows: tile_c must be in [1, 65536]");
+    if (n_idx == 0 || rows * cols == 0) return SBT_OK;
+    SBT_REQUIRE(dst && idx && src, "scatter_add_rows: NULL pointer");
+    SBT_REQUIRE(ld_dst >= cols, "scatter_add_rows: ld_dst < cols");
+    SBT_REQUIRE(ld_src >= tile_c, "scatter_add_rows: ld_src < tile_c");
+    sbt_status st = sbt_use_device(ctx);
+    if (st) return st;
+    return sbt_launch_scatter_add(ctx, kind, dst, rows, cols, ld_dst, idx, n_idx, row_offset, col_offset, src, ld_src,
+                                  tile_c, (cudaStream_t)stream);
+}
+
 sbt_status sbt_ragged_tile_store(sbt_context* ctx, sbt_dtype dtype, const void* tiles, int32_t batch, int32_t heads,
                                  int32_t depth, int32_t t_pad, const int32_t* cu_seqlens, void* x, int64_t total_rows,
                                  int64_t ld_row, int64_t ld_head, void* stream) {

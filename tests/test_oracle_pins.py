@@ -260,6 +260,57 @@ def test_scatter_duplicates_take_a_candidate():
         assert float(dst[2, j]) in cands
 
 
+# ----------------------------------------------------------------------------- scatter-add (gather backward)
+
+def test_scatter_add_unique_fp32_equals_numpy_rounding():
+    rows, cols, n = 300, 40, 120
+    dst = synth.uniform_f32(61, (rows, cols), -1.0, 1.0)
+    before = dst.copy()
+    idx = synth.permutation_prefix(62, rows, n)
+    src = synth.uniform_f32(63, (n, cols), -1.0, 1.0)
+    oracle.scatter_add_rows(dst, rows, cols, cols, idx, src, cols, cols)
+    want = before.copy()
+    want[idx] = (before[idx].astype(np.float64) + src.astype(np.float64)).astype(np.float32)
+    np.testing.assert_array_equal(dst, want)
+
+
+def test_scatter_add_duplicates_integer_values_equal_numpy_add_at():
+    rows, cols, n = 10, 16, 500
+    dst = synth.int_below(64, rows * cols, 9, lo=-4).astype(np.float32).reshape(rows, cols)
+    idx = synth.int_below(65, n, 14, lo=-2).astype(np.int32)   # duplicates and out-of-range rows
+    src = synth.int_below(66, n * cols, 7, lo=-3).astype(np.float32).reshape(n, cols)
+    want = dst.astype(np.int64)
+    ok = (idx >= 0) & (idx < rows)
+    np.add.at(want, idx[ok], src[ok].astype(np.int64))
+    oracle.scatter_add_rows(dst, rows, cols, cols, idx, src, cols, cols)
+    np.testing.assert_array_equal(dst, want.astype(np.float32))
+
+
+@pytest.mark.parametrize("kind,tdt", [("bf16", torch.bfloat16), ("f16", torch.float16)])
+def test_scatter_add_half_types_equal_torch(kind, tdt):
+    rows, cols, n = 200, 24, 90
+    base = torch.from_numpy(synth.normal_f32(67, (rows, cols))).to(tdt)
+    add = torch.from_numpy(synth.normal_f32(68, (n, cols)) * np.float32(3.0)).to(tdt)
+    idx = synth.permutation_prefix(69, rows, n)
+    dst = base.view(torch.int16).numpy().view(np.uint16).copy()
+    src = add.view(torch.int16).numpy().view(np.uint16).copy()
+    oracle.scatter_add_rows(dst, rows, cols, cols, idx, src, cols, cols, kind=kind)
+    want = base.clone()
+    want[torch.from_numpy(idx.astype(np.int64))] = (base[torch.from_numpy(idx.astype(np.int64))].float()
+                                                   + add.float()).to(tdt)
+    np.testing.assert_array_equal(dst, want.view(torch.int16).numpy().view(np.uint16))
+
+
+def test_scatter_add_clips_rows_and_columns():
+    dst = np.zeros((6, 5), np.float32)
+    idx = np.array([-1, 6, 2, np.iinfo(np.int32).max], np.int32)
+    src = np.ones((4, 7), np.float32)
+    oracle.scatter_add_rows(dst, 6, 5, 5, idx, src, 7, 7, col_offset=-1)
+    want = np.zeros((6, 5), np.float32)
+    want[2, :] = 1.0   # window columns -1..5 -> 0..4 inside
+    np.testing.assert_array_equal(dst, want)
+
+
 # ----------------------------------------------------------------------------- ragged
 
 def test_ragged_equal_lengths_is_a_transpose():
