@@ -336,8 +336,8 @@ def run_ops(ctx, pk):
 
     # tile load / store over a 16381 x 16411 fp32 array, 64 x 32 tiles (aligned and unaligned rows)
     import synth
-    for ld, tag in ((16416, "aligned_ld"), (16411, "unaligned_ld")):
-        r_, c_ = 16381, 16411
+    # 16,384 x 16,416 with ld 16,416 (16-byte rows) and 16,381 x 16,411 with ld 16,411 (unaligned rows)
+    for r_, c_, ld, tag in ((16384, 16416, 16416, "aligned_ld"), (16381, 16411, 16411, "unaligned_ld")):
         a = synth.uniform_f32(0x5B7101, (r_, ld), -1.0, 1.0)
         gr, gc = -(-r_ // 64), -(-c_ // 32)
         ad = dev_bytes(a)
@@ -345,13 +345,13 @@ def run_ops(ctx, pk):
         fn = lambda: sbt.tile_load_padded(ctx, ad, r_, c_, ld, 1, 0, 0, 64, 32, gr, gc, 64, 32, tiles, dtype="f32")
         med, _, _ = time_launches(fn, 20)
         nbytes = r_ * c_ * 4 + tiles.numel()
-        ops[f"tile_load_padded_{tag}"] = {"workload": f"fp32 16381x16411 ld {ld}, 64x32 tile grid {gr}x{gc}",
+        ops[f"tile_load_padded_{tag}"] = {"workload": f"fp32 {r_}x{c_} ld {ld}, 64x32 tile grid {gr}x{gc}",
                                           "ms": med, "GB/s": nbytes / med / 1e6, "frac_hbm": nbytes / med / 1e6 / hbm,
                                           "algorithmic_bytes": nbytes}
         fn = lambda: sbt.tile_store_clipped(ctx, tiles, gr, gc, 64, 32, ad, r_, c_, ld, 1, 0, 0, 64, 32, dtype="f32")
         med, _, _ = time_launches(fn, 20)
         nbytes = 2 * r_ * c_ * 4
-        ops[f"tile_store_clipped_{tag}"] = {"workload": f"fp32 16381x16411 ld {ld}, 64x32 tile grid {gr}x{gc}",
+        ops[f"tile_store_clipped_{tag}"] = {"workload": f"fp32 {r_}x{c_} ld {ld}, 64x32 tile grid {gr}x{gc}",
                                             "ms": med, "GB/s": nbytes / med / 1e6,
                                             "frac_hbm": nbytes / med / 1e6 / hbm, "algorithmic_bytes": nbytes}
         del ad, tiles, a
@@ -568,8 +568,9 @@ def run_profile(args):
         fn = lambda: sbt.ragged_tile_store(ctx, tiles, b, 8, 128, 4096, cu, xs, d["total_rows"], 1024, 128,
                                            dtype="bf16")
     elif op.startswith("tile"):
-        r_, c_ = max(64, int(16381 * f)), 16411
-        ld = 16411 if op.endswith("unaligned") else 16416
+        unal = op.endswith("unaligned")
+        r_, c_ = max(64, int((16381 if unal else 16384) * f)), (16411 if unal else 16416)
+        ld = c_
         a = synth.uniform_f32(0x5B7101, (r_, ld), -1.0, 1.0)
         gr, gc = -(-r_ // 64), -(-c_ // 32)
         ad = dev_bytes(a)

@@ -431,6 +431,14 @@ sbt_status sbt_launch_tile_load(sbt_context* ctx, int es, const void* src, int64
                                 int64_t step_r, int64_t step_c, int32_t grid_r, int32_t grid_c, int32_t tile_r,
                                 int32_t tile_c, void* dst, uint32_t pad_word, cudaStream_t stream) {
     if (!src) rows = cols = 0;  // an empty array: every element is padding
+    // TMA tiles when asked, or by default for tiles of 16 KiB and more (measured: even with the
+    // vector path at 8 KiB, ~2% ahead at 32 KiB on a 16,384 x 16,416 fp32 array).
+    const bool big_tile = (int64_t)tile_r * tile_c * es >= 16384;
+    if ((ctx->path == SBT_PATH_TMA || (ctx->path == SBT_PATH_AUTO && big_tile)) &&
+        sbt_tile_tma_ok(es, src, rows, cols, stride_r, stride_c, origin_r, origin_c, step_r, step_c, grid_r, grid_c,
+                        tile_r, tile_c, dst, false))
+        return sbt_launch_tile_load_tma(ctx, es, src, rows, cols, stride_r, origin_r, origin_c, step_r, step_c, grid_r,
+                                        grid_c, tile_r, tile_c, dst, pad_word, stream);
     int mode = tiles_vector_ok(es, src, stride_r, stride_c, origin_c, step_c, grid_c, tile_c, dst) ? kAligned
                : (src && tiles_realign_ok(es, stride_r, stride_c, tile_c, dst)) ? kRealign
                                                                                 : kElem;
@@ -464,6 +472,12 @@ sbt_status sbt_launch_tile_store(sbt_context* ctx, int es, const void* src_tiles
                                  int32_t tile_r, int32_t tile_c, void* dst, int64_t rows, int64_t cols,
                                  int64_t stride_r, int64_t stride_c, int64_t origin_r, int64_t origin_c,
                                  int64_t step_r, int64_t step_c, cudaStream_t stream) {
+    const bool big_tile = (int64_t)tile_r * tile_c * es >= 16384;
+    if ((ctx->path == SBT_PATH_TMA || (ctx->path == SBT_PATH_AUTO && big_tile)) &&
+        sbt_tile_tma_ok(es, dst, rows, cols, stride_r, stride_c, origin_r, origin_c, step_r, step_c, grid_r, grid_c,
+                        tile_r, tile_c, src_tiles, true))
+        return sbt_launch_tile_store_tma(ctx, es, src_tiles, grid_r, grid_c, tile_r, tile_c, dst, rows, cols, stride_r,
+                                         origin_r, origin_c, step_r, step_c, stream);
     int mode = tiles_vector_ok(es, dst, stride_r, stride_c, origin_c, step_c, grid_c, tile_c, src_tiles) ? kAligned
                                                                                                          : kElem;
     if (ctx->path == SBT_PATH_SCALAR) mode = kElem;

@@ -87,6 +87,18 @@ sbt_status sbt_launch_gemm(sbt_context* ctx, const void* A, int64_t lda, const v
                            int64_t ldc, sbt_dtype c_dtype, int64_t M, int64_t N, int64_t K, void* workspace,
                            size_t workspace_bytes, cudaStream_t stream);
 size_t sbt_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
+// TMA tensor-copy variants of the tile load / store (k_tiles_tma.cu) and their preconditions.
+bool sbt_tile_tma_ok(int es, const void* arr, int64_t rows, int64_t cols, int64_t stride_r, int64_t stride_c,
+                     int64_t origin_r, int64_t origin_c, int64_t step_r, int64_t step_c, int32_t grid_r,
+                     int32_t grid_c, int32_t tile_r, int32_t tile_c, const void* tiles, bool store);
+sbt_status sbt_launch_tile_load_tma(sbt_context* ctx, int es, const void* src, int64_t rows, int64_t cols,
+                                    int64_t stride_r, int64_t origin_r, int64_t origin_c, int64_t step_r,
+                                    int64_t step_c, int32_t grid_r, int32_t grid_c, int32_t tile_r, int32_t tile_c,
+                                    void* dst, uint32_t pad_word, cudaStream_t stream);
+sbt_status sbt_launch_tile_store_tma(sbt_context* ctx, int es, const void* src_tiles, int32_t grid_r, int32_t grid_c,
+                                     int32_t tile_r, int32_t tile_c, void* dst, int64_t rows, int64_t cols,
+                                     int64_t stride_r, int64_t origin_r, int64_t origin_c, int64_t step_r,
+                                     int64_t step_c, cudaStream_t stream);
 // TMA bulk-copy variants of the row gather / scatter (k_bulk.cu) and their preconditions.
 bool sbt_gather_bulk_ok(int es, const void* src, int64_t cols, int64_t ld_src, int64_t col_offset, int32_t tile_c,
                         const uint8_t* mask, const void* out, int64_t ld_out);

@@ -41,7 +41,7 @@ def same_bits(a, b):
     return a.shape == b.shape and np.array_equal(a.view(np.uint8), b.view(np.uint8))
 
 
-@pytest.mark.parametrize("path", ["auto", "scalar"])
+@pytest.mark.parametrize("path", ["auto", "tma", "scalar"])
 def test_small_fp32_grid_load_and_store(ctx, path):
     a = wl.tiles_small()["a"]
     got = gpu_load(ctx, a, 65, 73, 73, 1, 0, 0, 64, 32, 2, 3, 64, 32, "f32", pad=0.0, path=path)
@@ -83,6 +83,8 @@ CASES = [
     (40, 37, 90, 2, (-3, 5), (8, 8), (6, 5), (8, 8)),           # column stride 2
     (30, 20, 20, 1, (0, 0), (0, 0), (1, 1), (256, 256)),        # tile larger than the array
     (1, 1, 1, 1, (0, 0), (1, 1), (3, 3), (1, 1)),               # 1x1
+    (70, 72, 80, 1, (0, 0), (64, 32), (2, 3), (64, 32)),        # 16-byte row width: TMA tiles, edge tiles
+    (70, 72, 80, 1, (-6, -8), (30, 24), (4, 4), (32, 16)),      # TMA with negative origins and gaps
 ]
 
 
@@ -95,7 +97,7 @@ def test_load_edge_cases(ctx, case, dtype):
     pad = 7.5 if dtype == "f32" else 0x40F0
     pad_np = np.float32(7.5) if dtype == "f32" else 0x40F0
     want = oracle.tile_load_padded(buf, rows, cols, ld, sc, r0, c0, str_, stc, gr, gc, tr, tc, pad=pad_np)
-    for path in ("auto", "scalar"):
+    for path in ("auto", "tma", "scalar"):
         got = gpu_load(ctx, buf, rows, cols, ld, sc, r0, c0, str_, stc, gr, gc, tr, tc, dtype, pad=pad, path=path)
         assert same_bits(got, want), path
 
@@ -106,6 +108,8 @@ STORE_CASES = [
     (65, 73, 73, 1, (3, 7), (13, 11), (6, 8), (13, 11)),
     (40, 37, 90, 2, (-3, 5), (8, 8), (6, 5), (8, 8)),
     (30, 20, 24, 1, (-100, -100), (64, 64), (2, 2), (8, 8)),  # wholly outside: writes nothing
+    (70, 72, 80, 1, (0, 0), (64, 32), (2, 3), (64, 32)),        # TMA store, partial edge tiles
+    (70, 72, 80, 1, (3, 40), (34, 24), (3, 2), (32, 16)),       # TMA store, gaps, rows and columns past the end
 ]
 
 
@@ -121,7 +125,7 @@ def test_store_edge_cases(ctx, case, dtype):
         dst = np.full((rows, ld), 0xDEAD, np.uint16)
     want = dst.copy()
     oracle.tile_store_clipped(tiles, want, rows, cols, ld, sc, r0, c0, str_, stc)
-    for path in ("auto", "scalar"):
+    for path in ("auto", "tma", "scalar"):
         got = gpu_store(ctx, tiles, dst, rows, cols, ld, sc, r0, c0, str_, stc, dtype, path=path)
         assert same_bits(got, want), path
 
@@ -148,15 +152,19 @@ def test_validation(ctx):
     assert ctx.launch_count == before
 
 
-@pytest.mark.parametrize("ld", [16411, 16416])
-def test_large_fp32_grid(ctx, ld):
-    """16381 x 16411 fp32 over a ceil-div grid of 64 x 32 tiles; ld 16411 (unaligned rows,
-    element path at the vectors) or 16416 (16-byte aligned rows, vector path)."""
-    rows, cols = 16381, 16411
+@pytest.mark.parametrize("shape,path", [((16381, 16411, 16411), "auto"), ((16384, 16416, 16416), "auto"),
+                                        ((16384, 16416, 16416), "tma"), ((16384, 16416, 16416), "vector"),
+                                        ((16381, 16411, 16416), "auto")])
+def test_large_fp32_grid(ctx, shape, path):
+    """fp32 arrays over a ceil-div grid of 64 x 32 tiles: 16,381 x 16,411 with ld 16,411
+    (unaligned rows: realigned loads, element stores), 16,384 x 16,416 with ld 16,416 (16-byte
+    rows: vector or TMA tiles), and 16,381 x 16,411 with ld 16,416 (aligned rows, ragged edge)."""
+    rows, cols, ld = shape
     a = synth.uniform_f32(205, (rows, ld), -1.0, 1.0)
     gr, gc = -(-rows // 64), -(-cols // 32)
     a_dev = dev(a)
     tiles = torch.empty(gr * gc * 64 * 32 * 4, dtype=torch.uint8, device="cuda")
+    ctx.set_path(path)
     sbt.tile_load_padded(ctx, a_dev, rows, cols, ld, 1, 0, 0, 64, 32, gr, gc, 64, 32, tiles, dtype="f32")
     want = oracle.tile_load_padded(a, rows, cols, ld, 1, 0, 0, 64, 32, gr, gc, 64, 32, pad=np.float32(0))
     assert same_bits(host(tiles, np.float32, want.shape), want)
