@@ -46,7 +46,7 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=5)
     ap.add_argument("--cpu-seconds", type=float, default=8.0, help="CPU-baseline sample budget")
     ap.add_argument("--profile", default=None,
-                    choices=["gather", "scatter", "scatter_add", "ragged", "ragged_store", "tile_load", "tile_store", "tile_load_unaligned",
+                    choices=["gather", "scatter", "scatter_add", "ragged", "ragged_store", "tile_load_tma", "tile_load", "tile_store", "tile_load_unaligned",
                              "tile_store_unaligned", "gemm"],
                     help="only launch one operation's workload (warmup + steps launches) for ncu")
     ap.add_argument("--scale", type=float, default=1.0, help="--profile: fraction of the workload's rows")
@@ -354,6 +354,24 @@ def run_ops(ctx, pk):
         ops[f"tile_store_clipped_{tag}"] = {"workload": f"fp32 {r_}x{c_} ld {ld}, 64x32 tile grid {gr}x{gc}",
                                             "ms": med, "GB/s": nbytes / med / 1e6,
                                             "frac_hbm": nbytes / med / 1e6 / hbm, "algorithmic_bytes": nbytes}
+        if tag == "aligned_ld":  # 128 x 64 tiles (32 KiB): the TMA tensor-copy path
+            gr2, gc2 = -(-r_ // 128), -(-c_ // 64)
+            t2 = torch.empty(gr2 * gc2 * 128 * 64 * 4, dtype=torch.uint8, device="cuda")
+            fn = lambda: sbt.tile_load_padded(ctx, ad, r_, c_, ld, 1, 0, 0, 128, 64, gr2, gc2, 128, 64, t2,
+                                              dtype="f32")
+            med, _, _ = time_launches(fn, 20)
+            nbytes = r_ * c_ * 4 + t2.numel()
+            ops["tile_load_padded_tma_128x64"] = {"workload": f"fp32 {r_}x{c_} ld {ld}, 128x64 tile grid {gr2}x{gc2}",
+                                                  "ms": med, "GB/s": nbytes / med / 1e6,
+                                                  "frac_hbm": nbytes / med / 1e6 / hbm, "algorithmic_bytes": nbytes}
+            fn = lambda: sbt.tile_store_clipped(ctx, t2, gr2, gc2, 128, 64, ad, r_, c_, ld, 1, 0, 0, 128, 64,
+                                                dtype="f32")
+            med, _, _ = time_launches(fn, 20)
+            nbytes = 2 * r_ * c_ * 4
+            ops["tile_store_clipped_tma_128x64"] = {"workload": f"fp32 {r_}x{c_} ld {ld}, 128x64 tile grid {gr2}x{gc2}",
+                                                    "ms": med, "GB/s": nbytes / med / 1e6,
+                                                    "frac_hbm": nbytes / med / 1e6 / hbm, "algorithmic_bytes": nbytes}
+            del t2
         del ad, tiles, a
 
     # bounded GEMM
@@ -567,6 +585,13 @@ def run_profile(args):
         cu = dev_bytes(d["cu_seqlens"])
         fn = lambda: sbt.ragged_tile_store(ctx, tiles, b, 8, 128, 4096, cu, xs, d["total_rows"], 1024, 128,
                                            dtype="bf16")
+    elif op == "tile_load_tma":
+        r_, c_ = max(128, int(16384 * f)), 16416
+        a = synth.uniform_f32(0x5B7101, (r_, c_), -1.0, 1.0)
+        gr, gc = -(-r_ // 128), -(-c_ // 64)
+        ad = dev_bytes(a)
+        tiles = torch.empty(gr * gc * 128 * 64 * 4, dtype=torch.uint8, device="cuda")
+        fn = lambda: sbt.tile_load_padded(ctx, ad, r_, c_, c_, 1, 0, 0, 128, 64, gr, gc, 128, 64, tiles, dtype="f32")
     elif op.startswith("tile"):
         unal = op.endswith("unaligned")
         r_, c_ = max(64, int((16381 if unal else 16384) * f)), (16411 if unal else 16416)
