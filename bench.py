@@ -314,6 +314,20 @@ def run_ops(ctx, pk):
                                "note": "bytes = gradients + indices + each distinct target row read and written once"}
     del table, gi, gg, grad, g
 
+    # column gather (axis 1): 4,096 random columns of every row of a 2,048 x 100,003 bf16 matrix
+    a = synth.normal_bf16(0x5B7103, (2048, 100_003))
+    ci = synth.int_below(0x5B7104, 4096, 100_003).astype(np.int32)
+    ad, cid = dev_bytes(a), dev_bytes(ci)
+    outc = torch.empty(2048 * 4096 * 2, dtype=torch.uint8, device="cuda")
+    fn = lambda: sbt.gather_cols(ctx, ad, 2048, 100_003, 100_003, cid, 4096, outc, 4096, 2048, dtype="bf16")
+    med, _, _ = time_launches(fn, 20)
+    nbytes = 2 * 2048 * 4096 * 2 + 4096 * 4
+    ops["gather_cols"] = {"workload": "bf16 2,048 x 100,003, 4,096 random columns gathered from every row",
+                          "ms": med, "GB/s": nbytes / med / 1e6, "frac_hbm": nbytes / med / 1e6 / hbm,
+                          "algorithmic_bytes": nbytes,
+                          "note": "each 2-byte element read costs a 32-byte sector: random columns are sector-bound"}
+    del a, ad, cid, outc
+
     # ragged 3D tile load
     d = wl.ragged_bf16()
     out = torch.empty(64 * 8 * 4096 * 128 * 2, dtype=torch.uint8, device="cuda")

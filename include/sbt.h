@@ -150,6 +150,24 @@ SBT_API sbt_status sbt_gather_rows(sbt_context* ctx, sbt_dtype dtype, const void
                            int64_t ld_out, const void* pad_value, void* stream);
 
 /*
+ * Column gather: the gather along axis 1.
+ * warp.tile_load_indexed, description and "Parameters" with axis = 1: element
+ * (i, k) reads row row_offset + i and column col_offset + idx[k] (the offset
+ * added before the check, in 64-bit); every coordinate is checked against both
+ * bounds and an element outside reads the padding value.
+ *
+ *   out[i*ld_out + k] = src[(row_offset+i)*ld_src + col_offset + idx[k]] or *pad_value,
+ *   for i < tile_r, k < n_idx.
+ *
+ * src: device rows x cols, row stride ld_src >= cols.  idx: device int32[n_idx].
+ * out: device [tile_r][ld_out], ld_out >= n_idx.  1 <= tile_r <= 65536.
+ */
+SBT_API sbt_status sbt_gather_cols(sbt_context* ctx, sbt_dtype dtype, const void* src, int64_t rows, int64_t cols,
+                                   int64_t ld_src, const int32_t* idx, int64_t n_idx, int64_t row_offset,
+                                   int64_t col_offset, int32_t tile_r, void* out, int64_t ld_out,
+                                   const void* pad_value, void* stream);
+
+/*
  * Masked row scatter.
  * cuTile.jl "Memory": scatter writes only where the mask is true and is
  * bounds-checked like every tile memory operation (out-of-range elements are

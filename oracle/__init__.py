@@ -42,6 +42,8 @@ def _load():
             lib.oracle_tile_store_clipped.argtypes = [ci, p, i32, i32, i32, i32, p, i64, i64, i64, i64,
                                                       i64, i64, i64, i64]
             lib.oracle_gather_rows.argtypes = [ci, p, i64, i64, i64, p, i64, i64, i64, i32, p, i64, p, i64, p]
+            lib.oracle_gather_cols.argtypes = [ci, p, i64, i64, i64, p, i64, i64, i64, i32, p, i64, p]
+            lib.oracle_gather_cols.restype = None
             lib.oracle_scatter_rows_masked.argtypes = [ci, p, i64, i64, i64, p, i64, i64, i64, p, i64, i32,
                                                        p, i64]
             lib.oracle_ragged_tile_load.argtypes = [ci, p, i64, i32, i32, i64, i64, p, i32, i32, p]
@@ -116,6 +118,19 @@ def gather_rows(src, rows, cols, ld_src, idx, tile_c, row_offset=0, col_offset=0
     padb = _pad_bits(pad, src.dtype)
     _load().oracle_gather_rows(_es(src), _p(src), rows, cols, ld_src, _p(idx), n, row_offset, col_offset,
                                tile_c, _p(mask), ld_mask or 0, _p(out), ld_out, _p(padb))
+    return out
+
+
+def gather_cols(src, rows, cols, ld_src, idx, tile_r, row_offset=0, col_offset=0, pad=0, ld_out=None):
+    """Column gather; returns out[tile_r][ld_out] (columns >= n_idx left as zero)."""
+    src = _flat_buffer(src)
+    idx = np.ascontiguousarray(idx, np.int32)
+    n = idx.size
+    ld_out = n if ld_out is None else ld_out
+    out = np.zeros((tile_r, ld_out), src.dtype)
+    padb = _pad_bits(pad, src.dtype)
+    _load().oracle_gather_cols(_es(src), _p(src), rows, cols, ld_src, _p(idx), n, row_offset, col_offset, tile_r,
+                               _p(out), ld_out, _p(padb))
     return out
 
 

@@ -99,6 +99,27 @@ void oracle_gather_rows(int es, const void* src, int64_t rows, int64_t cols, int
     }
 }
 
+/* Column gather (gather along axis 1).
+ * warp.tile_load_indexed, description, with axis = 1: element (i, k) of the
+ * tile reads row row_offset + i and column col_offset + idx[k] (the offset is
+ * added before the check, in 64-bit); every coordinate is checked against both
+ * bounds and an element outside reads the padding value.
+ * Output element (i, k) is out[i*ld_out + k], i < tile_r, k < n_idx. */
+void oracle_gather_cols(int es, const void* src, int64_t rows, int64_t cols, int64_t ld_src, const int32_t* idx,
+                        int64_t n_idx, int64_t row_offset, int64_t col_offset, int32_t tile_r, void* out,
+                        int64_t ld_out, const void* pad) {
+    for (int32_t i = 0; i < tile_r; ++i) {
+        int64_t r = row_offset + i;
+        for (int64_t k = 0; k < n_idx; ++k) {
+            int64_t c = (int64_t)idx[k] + col_offset;
+            if (r >= 0 && r < rows && c >= 0 && c < cols)
+                put(out, i * ld_out + k, es, at(src, r * ld_src + c, es));
+            else
+                put(out, i * ld_out + k, es, pad);
+        }
+    }
+}
+
 /* Masked row scatter.
  * cuTile.jl "Memory": scatter writes only where the mask is true and, like
  * every memory operation there, is bounds-checked (out-of-range elements are

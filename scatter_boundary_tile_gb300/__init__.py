@@ -6,7 +6,7 @@ There is no fallback: if ``libsbt.so`` is missing or fails to load, importing
 an op raises.
 
 Op names match the C ABI in ``include/sbt.h`` without the ``sbt_`` prefix:
-``tile_load_padded``, ``tile_store_clipped``, ``gather_rows``,
+``tile_load_padded``, ``tile_store_clipped``, ``gather_rows``, ``gather_cols``,
 ``scatter_rows_masked``, ``scatter_add_rows``, ``ragged_tile_load``, ``ragged_tile_store``, ``gemm_bounded`` (plus
 ``gemm_bounded_workspace_size``).  Arrays are torch tensors on the device
 (only their data pointer is used; shapes and strides are the explicit
@@ -32,7 +32,7 @@ PATHS = {"auto": 0, "scalar": 1, "vector": 2, "tma": 3}
 # Every symbol include/sbt.h declares.
 EXPORTS = ("sbt_create", "sbt_destroy", "sbt_set_path", "sbt_set_wait_limit_ns", "sbt_set_test_hook", "sbt_launch_count",
            "sbt_check_status", "sbt_last_error_message", "sbt_tile_load_padded", "sbt_tile_store_clipped",
-           "sbt_gather_rows", "sbt_scatter_rows_masked", "sbt_scatter_add_rows", "sbt_ragged_tile_load", "sbt_ragged_tile_store", "sbt_gemm_bounded_workspace_size",
+           "sbt_gather_rows", "sbt_gather_cols", "sbt_scatter_rows_masked", "sbt_scatter_add_rows", "sbt_ragged_tile_load", "sbt_ragged_tile_store", "sbt_gemm_bounded_workspace_size",
            "sbt_gemm_bounded", "sbt_gemm_bounded_noalloc")
 GEMM_NOALLOC_SCRATCH_BYTES = 16 << 20  # SBT_GEMM_NOALLOC_SCRATCH_BYTES in include/sbt.h
 
@@ -68,6 +68,7 @@ def load_library(path: str = LIB_PATH):
             "sbt_tile_store_clipped": [p, ci, p, i32, i32, i32, i32, p, i64, i64, i64, i64, i64, i64, i64, i64, p],
             "sbt_gather_rows": [p, ci, p, i64, i64, i64, p, i64, i64, i64, i32, p, i64, p, i64, p, p],
             "sbt_scatter_rows_masked": [p, ci, p, i64, i64, i64, p, i64, i64, i64, p, i64, i32, p, i64, p],
+            "sbt_gather_cols": [p, ci, p, i64, i64, i64, p, i64, i64, i64, i32, p, i64, p, p],
             "sbt_scatter_add_rows": [p, ci, p, i64, i64, i64, p, i64, i64, i64, p, i64, i32, p],
             "sbt_ragged_tile_load": [p, ci, p, i64, i32, i32, i64, i64, p, i32, i32, p, p],
             "sbt_ragged_tile_store": [p, ci, p, i32, i32, i32, i32, p, p, i64, i64, i64, p],
@@ -203,6 +204,14 @@ def gather_rows(ctx, src, rows, cols, ld_src, idx, n_idx, out, ld_out, tile_c, r
     _check(load_library().sbt_gather_rows(ctx.handle, code, _ptr(src), rows, cols, ld_src, _ptr(idx), n_idx,
                                           row_offset, col_offset, tile_c, _ptr(mask), ld_mask, _ptr(out), ld_out,
                                           _pad_bytes(pad, code), _stream(stream)))
+
+
+def gather_cols(ctx, src, rows, cols, ld_src, idx, n_idx, out, ld_out, tile_r, row_offset=0, col_offset=0, pad=None,
+                dtype=None, stream=None):
+    code = _dtype_code(out, dtype)
+    _check(load_library().sbt_gather_cols(ctx.handle, code, _ptr(src), rows, cols, ld_src, _ptr(idx), n_idx, row_offset,
+                                          col_offset, tile_r, _ptr(out), ld_out, _pad_bytes(pad, code),
+                                          _stream(stream)))
 
 
 def scatter_rows_masked(ctx, dst, rows, cols, ld_dst, idx, n_idx, src, ld_src, tile_c, row_offset=0, col_offset=0,

@@ -305,6 +305,53 @@ __global__ void __launch_bounds__(kThreads) k_scatter_rows(const RowParams p) {
     }
 }
 
+// ---------------------------------------------------------------------------- column gather (axis 1)
+
+constexpr int kColChunk = 256;  // indices per unit (one output column per thread)
+constexpr int kColRows = 32;    // output rows per unit
+
+struct ColParams {
+    const char* src;
+    char* out;
+    const int32_t* idx;
+    int64_t rows, cols, ld_src, ld_out, n_idx, row_offset, col_offset;
+    int32_t tile_r;
+    int64_t n_kchunks, units;
+    uint32_t pad_word;
+};
+
+template <int ES>
+__global__ void __launch_bounds__(kThreads) k_gather_cols(const ColParams p) {
+    typedef typename sbt_elem<ES>::T T;
+    for (int64_t unit = blockIdx.x; unit < p.units; unit += gridDim.x) {
+        const int64_t kc = unit % p.n_kchunks, rb = unit / p.n_kchunks;
+        const int64_t k = kc * kColChunk + threadIdx.x;
+        int64_t c = -1;
+        if (k < p.n_idx) {
+            c = (int64_t)__ldg(p.idx + k) + p.col_offset;
+            if (c < 0 || c >= p.cols) c = -1;
+        }
+        const int i0 = (int)(rb * kColRows);
+        const int nr = p.tile_r - i0 < kColRows ? p.tile_r - i0 : kColRows;
+        if (k < p.n_idx) {
+            const int64_t col = c;  // this thread's column, checked once for all its rows
+            for (int ib = 0; ib < nr; ib += 8) {
+                T v[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int64_t r = p.row_offset + i0 + ib + u;
+                    v[u] = (T)p.pad_word;
+                    if (ib + u < nr && col >= 0 && r >= 0 && r < p.rows)
+                        v[u] = __ldg(reinterpret_cast<const T*>(p.src) + r * p.ld_src + col);
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u)
+                    if (ib + u < nr) reinterpret_cast<T*>(p.out)[(int64_t)(i0 + ib + u) * p.ld_out + k] = v[u];
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------------------- scatter-add (gather backward)
 
 // Element-type additions done by the L2 (red = reduction without a return value).
@@ -555,4 +602,32 @@ sbt_status sbt_launch_scatter_add(sbt_context* ctx, int kind, void* dst, int64_t
     if (kind == 2) SBT_SA(2);
     SBT_SA(3);
 #undef SBT_SA
+}
+
+sbt_status sbt_launch_gather_cols(sbt_context* ctx, int es, const void* src, int64_t rows, int64_t cols, int64_t ld_src,
+                                  const int32_t* idx, int64_t n_idx, int64_t row_offset, int64_t col_offset,
+                                  int32_t tile_r, void* out, int64_t ld_out, uint32_t pad_word, cudaStream_t stream) {
+    ColParams p;
+    p.src = (const char*)src;
+    p.out = (char*)out;
+    p.idx = idx;
+    p.rows = (src && cols > 0) ? rows : 0;
+    p.cols = cols;
+    p.ld_src = ld_src;
+    p.ld_out = ld_out;
+    p.n_idx = n_idx;
+    p.row_offset = row_offset;
+    p.col_offset = col_offset;
+    p.tile_r = tile_r;
+    p.n_kchunks = sbt_cdiv(n_idx, kColChunk);
+    p.units = p.n_kchunks * sbt_cdiv(tile_r, kColRows);
+    p.pad_word = pad_word;
+    if (es == 4) {
+        const int grid = sbt_persistent_grid(ctx, (const void*)k_gather_cols<4>, kThreads, 0, p.units);
+        k_gather_cols<4><<<grid, kThreads, 0, stream>>>(p);
+    } else {
+        const int grid = sbt_persistent_grid(ctx, (const void*)k_gather_cols<2>, kThreads, 0, p.units);
+        k_gather_cols<2><<<grid, kThreads, 0, stream>>>(p);
+    }
+    return sbt_after_launch(ctx, "gather_cols");
 }

@@ -218,6 +218,25 @@ sbt_status sbt_gather_rows(sbt_context* ctx, sbt_dtype dtype, const void* src, i
                              ld_mask, out, ld_out, sbt_pad_word(pad_value, es), (cudaStream_t)stream);
 }
 
+sbt_status sbt_gather_cols(sbt_context* ctx, sbt_dtype dtype, const void* src, int64_t rows, int64_t cols,
+                           int64_t ld_src, const int32_t* idx, int64_t n_idx, int64_t row_offset, int64_t col_offset,
+                           int32_t tile_r, void* out, int64_t ld_out, const void* pad_value, void* stream) {
+    SBT_REQUIRE(ctx, "ctx is NULL");
+    int es;
+    sbt_status st = check_dtype_move(dtype, &es);
+    if (st) return st;
+    SBT_REQUIRE(rows >= 0 && cols >= 0 && n_idx >= 0, "gather_cols: negative extent");
+    SBT_REQUIRE(tile_r >= 1 && tile_r <= 65536, "gather_cols: tile_r must be in [1, 65536]");
+    SBT_REQUIRE(ld_out >= n_idx, "gather_cols: ld_out < n_idx");
+    if (n_idx == 0) return SBT_OK;
+    SBT_REQUIRE(idx && out, "gather_cols: NULL idx or out");
+    SBT_REQUIRE(rows * cols == 0 || src, "gather_cols: src is NULL");
+    SBT_REQUIRE(rows * cols == 0 || ld_src >= cols, "gather_cols: ld_src < cols");
+    if ((st = sbt_use_device(ctx))) return st;
+    return sbt_launch_gather_cols(ctx, es, src, rows, cols, ld_src, idx, n_idx, row_offset, col_offset, tile_r, out,
+                                  ld_out, sbt_pad_word(pad_value, es), (cudaStream_t)stream);
+}
+
 sbt_status sbt_scatter_rows_masked(sbt_context* ctx, sbt_dtype dtype, void* dst, int64_t rows, int64_t cols,
                                    int64_t ld_dst, const int32_t* idx, int64_t n_idx, int64_t row_offset,
                                    int64_t col_offset, const void* src, int64_t ld_src, int32_t tile_c,

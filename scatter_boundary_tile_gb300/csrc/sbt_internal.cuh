@@ -76,6 +76,9 @@ sbt_status sbt_launch_scatter(sbt_context* ctx, int es, void* dst, int64_t rows,
 sbt_status sbt_launch_ragged(sbt_context* ctx, int es, const void* x, int64_t total_rows, int32_t heads,
                              int32_t depth, int64_t ld_row, int64_t ld_head, const int32_t* cu_seqlens,
                              int32_t batch, int32_t t_pad, void* out, cudaStream_t stream);
+sbt_status sbt_launch_gather_cols(sbt_context* ctx, int es, const void* src, int64_t rows, int64_t cols, int64_t ld_src,
+                                  const int32_t* idx, int64_t n_idx, int64_t row_offset, int64_t col_offset,
+                                  int32_t tile_r, void* out, int64_t ld_out, uint32_t pad_word, cudaStream_t stream);
 // kind: 4 = fp32, 2 = bf16, 3 = fp16
 sbt_status sbt_launch_scatter_add(sbt_context* ctx, int kind, void* dst, int64_t rows, int64_t cols, int64_t ld_dst,
                                   const int32_t* idx, int64_t n_idx, int64_t row_offset, int64_t col_offset,

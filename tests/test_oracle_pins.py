@@ -117,6 +117,32 @@ def test_gather_general_equals_numpy_pad_and_clip():
         np.testing.assert_array_equal(out, want)
 
 
+def test_gather_cols_equals_numpy_fancy_indexing_and_pad_clip():
+    rows, cols, ld = 30, 50, 53
+    a = synth.uniform_f32(71, (rows, ld), -1.0, 1.0)
+    logical = a[:, :cols]
+    idx = synth.int_below(72, 40, 50).astype(np.int32)
+    out = oracle.gather_cols(a, rows, cols, ld, idx, tile_r=25, row_offset=3)
+    np.testing.assert_array_equal(out, logical[3:28][:, idx])  # numpy: all coordinates valid
+    # out-of-range rows and columns (both sides), via np.pad with one pad row/column around the array
+    idx = np.array([-1, 0, 49, 50, np.iinfo(np.int32).min, 7, 52], np.int32)
+    pad = np.float32(-2.0)
+    out = oracle.gather_cols(a, rows, cols, ld, idx, tile_r=34, row_offset=-2, col_offset=1, pad=pad)
+    big = padded_reference(logical, pad, 1)
+    r = np.clip(np.arange(34) - 2, -1, rows) + 1
+    c = np.clip(idx.astype(np.int64) + 1, -1, cols) + 1
+    np.testing.assert_array_equal(out, big[r][:, c])
+
+
+def test_gather_cols_is_row_gather_of_the_transpose():
+    a = synth.uniform_f32(73, (12, 9), -1.0, 1.0)
+    idx = np.array([8, -1, 3, 3, 9, 0], np.int32)
+    by_cols = oracle.gather_cols(a, 12, 9, 9, idx, tile_r=12, pad=5.0)
+    at = np.ascontiguousarray(a.T)
+    by_rows = oracle.gather_rows(at, 9, 12, 12, idx, tile_c=12, pad=np.float32(5.0))
+    np.testing.assert_array_equal(by_cols, by_rows.T)
+
+
 def test_gather_bf16_raw_bits_nan_negzero():
     a = np.array([[0x7FC1, 0x8000, 0x3F80, 0xFF81]], np.uint16)  # NaN payload, -0.0, 1.0, -NaN
     out = oracle.gather_rows(a, 1, 4, 4, np.array([0, -1], np.int32), tile_c=4, pad=0xBF80)
