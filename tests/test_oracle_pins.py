@@ -358,6 +358,23 @@ def test_ragged_prefix_and_zero_rows():
         assert not out[b, :, L:].any()
 
 
+def test_grouped_ragged_is_the_ragged_load_with_merged_depth():
+    # Mojo "RaggedTMA3DTile", group > 1: the packed array is [rows][middle][group][depth] and a
+    # tile holds (sequence position, group member) rows.  The grouped tile, written out directly
+    # with numpy, equals the ragged load with depth' = group * depth.
+    B, M, G, D, t_pad = 4, 3, 2, 8, 12
+    lens = np.array([5, 12, 0, 9])
+    cu = np.zeros(B + 1, np.int32)
+    cu[1:] = np.cumsum(lens)
+    x = synth.normal_bf16(45, (int(cu[-1]), M, G, D))
+    want = np.zeros((B, M, t_pad, G, D), np.uint16)
+    for b in range(B):
+        L = min(int(lens[b]), t_pad)
+        want[b, :, :L] = x[cu[b]:cu[b] + L].transpose(1, 0, 2, 3)
+    got = oracle.ragged_tile_load(x, int(cu[-1]), M, G * D, M * G * D, G * D, cu, t_pad)
+    np.testing.assert_array_equal(got.reshape(B, M, t_pad, G, D), want)
+
+
 def test_ragged_empty_and_out_of_range_metadata():
     x = synth.normal_bf16(42, (10, 2, 4))
     cu = np.array([0, 0, 8, 14], np.int32)  # empty sequence; the last one runs past total_rows=10

@@ -132,3 +132,18 @@ def test_store_full_size_workload_bit_exact(ctx):
     got = host(xd, np.uint16, (total, 8, 128))
     want = oracle.ragged_tile_store(tiles, np.zeros((total, 8, 128), np.uint16), total, 1024, 128, cu)
     assert np.array_equal(got, want)
+
+
+def test_grouped_ragged_tiles(ctx):
+    """group > 1: packed [rows][middle=8][group=4][depth=32] read as tiles of (position, group member)
+    rows, i.e. the ragged load with depth' = group * depth."""
+    d = wl.ragged_bf16(batch=6, max_len=500, heads=8, depth=128)  # 128 = group 4 x depth 32
+    x, cu = d["x"], d["cu_seqlens"]
+    got = gpu_ragged(ctx, x, d["total_rows"], 8, 128, 1024, 128, cu, 512, "bf16")
+    want = oracle.ragged_tile_load(x, d["total_rows"], 8, 128, 1024, 128, cu, 512)
+    assert np.array_equal(got, want)
+    g = got.reshape(6, 8, 512, 4, 32)
+    xg = x.reshape(-1, 8, 4, 32)
+    b, m, s, gi = 2, 5, 3, 1
+    if s < d["lens"][b]:
+        np.testing.assert_array_equal(g[b, m, s, gi], xg[cu[b] + s, m, gi])
