@@ -52,6 +52,11 @@ def _load():
             lib.oracle_ragged_tile_store.argtypes = [ci, p, i32, i32, i32, i32, p, p, i64, i64, i64]
             lib.oracle_gemm_f64.argtypes = [p, i64, p, i64, i64, i64, i64, p, i64]
             lib.oracle_gemm_f64_at.argtypes = [p, i64, p, i64, i64, p, p, i64, p]
+            lib.oracle_fp8_decode.argtypes = [ci, ctypes.c_uint8]
+            lib.oracle_fp8_decode.restype = ctypes.c_double
+            lib.oracle_gemm_block_scaled_f64.argtypes = [ci, ci, ci, p, i64, p, i64, p, i64, p, i64, i64, i64, i64,
+                                                         i64, p, i64]
+            lib.oracle_gemm_block_scaled_f64.restype = None
             lib.oracle_bf16_rne.argtypes = [ctypes.c_double]
             lib.oracle_bf16_rne.restype = ctypes.c_uint16
             lib.oracle_round_bf16.argtypes = [p, i64, p]
@@ -203,6 +208,24 @@ def gemm_f64_at(A, lda, B, ldb, K, ms, ns):
     out = np.empty(ms.size, np.float64)
     _load().oracle_gemm_f64_at(_p(A), lda, _p(B), ldb, K, _p(ms), _p(ns), ms.size, _p(out))
     return out
+
+
+FP8_FORMATS = {"e4m3": 0, "e5m2": 1, "e8m0": 2}
+
+
+def fp8_decode(fmt: str, code: int) -> float:
+    return float(_load().oracle_fp8_decode(FP8_FORMATS[fmt], code))
+
+
+def gemm_block_scaled_f64(A, lda, SA, ldsa, B, ldb, SB, ldsb, M, N, K, block, afmt="e4m3", bfmt="e4m3",
+                          sfmt="e8m0"):
+    """(A .* scale_a)(B .* scale_b) in double from 8-bit codes; returns (M, N) float64."""
+    arrs = [_flat_buffer(np.ascontiguousarray(x, np.uint8)) for x in (A, SA, B, SB)]
+    C = np.empty((M, N), np.float64)
+    _load().oracle_gemm_block_scaled_f64(FP8_FORMATS[afmt], FP8_FORMATS[bfmt], FP8_FORMATS[sfmt], _p(arrs[0]), lda,
+                                         _p(arrs[1]), ldsa, _p(arrs[2]), ldb, _p(arrs[3]), ldsb, M, N, K, block,
+                                         _p(C), N)
+    return C
 
 
 def bf16_rne(x: float) -> int:

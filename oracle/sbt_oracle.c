@@ -269,6 +269,51 @@ static double bf16_to_f64(uint16_t b) {
     return (double)f;
 }
 
+/* 8-bit formats, decoded from their definitions (OCP 8-bit floating point and
+ * microscaling formats): fmt 0 = E4M3 (bias 7, subnormals, no infinities,
+ * S.1111.111 is NaN), 1 = E5M2 (bias 15, IEEE-style infinities and NaNs),
+ * 2 = E8M0 (unsigned exponent: 2^(e-127), 0xFF is NaN). */
+double oracle_fp8_decode(int fmt, uint8_t b) {
+    if (fmt == 2) return b == 0xFF ? NAN : ldexp(1.0, (int)b - 127);
+    int sign = b >> 7;
+    int e, m;
+    double v;
+    if (fmt == 0) {
+        e = (b >> 3) & 15;
+        m = b & 7;
+        if (e == 15 && m == 7) return NAN;
+        v = e == 0 ? ldexp((double)m, -9) : ldexp((double)(8 + m), e - 10);
+    } else {
+        e = (b >> 2) & 31;
+        m = b & 3;
+        if (e == 31) return m ? NAN : (sign ? -INFINITY : INFINITY);
+        v = e == 0 ? ldexp((double)m, -16) : ldexp((double)(4 + m), e - 17);
+    }
+    return sign ? -v : v;
+}
+
+/* Block-scaled GEMM reference.
+ * cuTile.jl "Operations", muladd_scaled: (a .* a_scale) * (b .* b_scale) + acc
+ * where each scale element multiplies a contiguous block of `block` = K / K_s
+ * elements along K; a_scale is (M, K_s), b_scale is (K_s, N).  Operands in
+ * E4M3 or E5M2 (afmt, bfmt), scales in E8M0 or E4M3 (sfmt).  Every scaled
+ * operand and every product is exact in double; the sum runs in double,
+ * k = 0..K-1. */
+void oracle_gemm_block_scaled_f64(int afmt, int bfmt, int sfmt, const uint8_t* A, int64_t lda, const uint8_t* SA,
+                                  int64_t ldsa, const uint8_t* B, int64_t ldb, const uint8_t* SB, int64_t ldsb,
+                                  int64_t M, int64_t N, int64_t K, int64_t block, double* C, int64_t ldc) {
+    for (int64_t m = 0; m < M; ++m)
+        for (int64_t n = 0; n < N; ++n) {
+            double s = 0.0;
+            for (int64_t k = 0; k < K; ++k) {
+                double a = oracle_fp8_decode(afmt, A[m * lda + k]) * oracle_fp8_decode(sfmt, SA[m * ldsa + k / block]);
+                double b = oracle_fp8_decode(bfmt, B[k * ldb + n]) * oracle_fp8_decode(sfmt, SB[(k / block) * ldsb + n]);
+                s += a * b;
+            }
+            C[m * ldc + n] = s;
+        }
+}
+
 /* GEMM reference, full matrix.
  * cuTile.jl "Operations", muladd: (M,K) x (K,N) -> (M,N), and bf16 inputs
  * accumulate in a wider type; Tylo.jl "Boundary tiles", section "Accumulator

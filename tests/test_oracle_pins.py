@@ -473,3 +473,43 @@ def test_bf16_rne_matches_torch_on_binary32_values():
     want = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
     got = oracle.round_bf16(f.astype(np.float64))
     np.testing.assert_array_equal(got, want)
+
+
+# ----------------------------------------------------------------------------- block-scaled GEMM
+
+@pytest.mark.parametrize("fmt,tdt", [("e4m3", torch.float8_e4m3fn), ("e5m2", torch.float8_e5m2),
+                                     ("e8m0", torch.float8_e8m0fnu)])
+def test_fp8_decode_all_codes_equal_torch(fmt, tdt):
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    want = codes.view(tdt).to(torch.float64).numpy()
+    got = np.array([oracle.fp8_decode(fmt, c) for c in range(256)])
+    assert np.array_equal(np.isnan(got), np.isnan(want))
+    ok = ~np.isnan(want)
+    np.testing.assert_array_equal(got[ok], want[ok])
+
+
+def test_block_scaled_unit_scales_equal_numpy_matmul():
+    M, N, K, bs = 7, 9, 64, 32
+    A = synth.int_below(81, M * K, 256).astype(np.uint8).reshape(M, K)
+    B = synth.int_below(82, K * N, 256).astype(np.uint8).reshape(K, N)
+    A[(A & 0x7F) == 0x7F] = 0x38  # keep NaN codes out (0x38 = 1.0)
+    B[(B & 0x7F) == 0x7F] = 0x38
+    SA = np.full((M, K // bs), 127, np.uint8)
+    SB = np.full((K // bs, N), 127, np.uint8)
+    C = oracle.gemm_block_scaled_f64(A, K, SA, K // bs, B, N, SB, N, M, N, K, bs)
+    a = torch.from_numpy(A).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    b = torch.from_numpy(B).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_allclose(C, a @ b, rtol=1e-12, atol=1e-9)
+
+
+def test_block_scaled_closed_form():
+    # ones times ones with scale_a[m][j] = 2^(m % 3) and scale_b[j][n] = 2^(j % 2):
+    # C[m][n] = bs * 2^(m % 3) * (#even blocks + 2 * #odd blocks)
+    M, N, K, bs = 5, 4, 96, 32   # 3 blocks: j = 0, 1, 2
+    A = np.full((M, K), 0x38, np.uint8)
+    B = np.full((K, N), 0x38, np.uint8)
+    SA = np.array([[127 + (m % 3)] * 3 for m in range(M)], np.uint8)
+    SB = np.array([[127 + (j % 2)] * N for j in range(3)], np.uint8)
+    C = oracle.gemm_block_scaled_f64(A, K, SA, 3, B, N, SB, N, M, N, K, bs)
+    want = np.array([[bs * 2.0 ** (m % 3) * (2 + 2 * 1)] * N for m in range(M)])
+    np.testing.assert_array_equal(C, want)
