@@ -54,8 +54,8 @@ def _load():
             lib.oracle_gemm_f64_at.argtypes = [p, i64, p, i64, i64, p, p, i64, p]
             lib.oracle_fp8_decode.argtypes = [ci, ctypes.c_uint8]
             lib.oracle_fp8_decode.restype = ctypes.c_double
-            lib.oracle_gemm_block_scaled_f64.argtypes = [ci, ci, ci, p, i64, p, i64, p, i64, p, i64, i64, i64, i64,
-                                                         i64, p, i64]
+            lib.oracle_gemm_block_scaled_f64.argtypes = [ci, ci, ci, p, i64, p, i64, p, i64, p, i64, p, i64, i64,
+                                                         i64, i64, i64, p, i64]
             lib.oracle_gemm_block_scaled_f64.restype = None
             lib.oracle_bf16_rne.argtypes = [ctypes.c_double]
             lib.oracle_bf16_rne.restype = ctypes.c_uint16
@@ -210,21 +210,29 @@ def gemm_f64_at(A, lda, B, ldb, K, ms, ns):
     return out
 
 
-FP8_FORMATS = {"e4m3": 0, "e5m2": 1, "e8m0": 2}
+LOWP_FORMATS = {"e4m3": 0, "e5m2": 1, "e8m0": 2, "e2m1": 3}
 
 
 def fp8_decode(fmt: str, code: int) -> float:
-    return float(_load().oracle_fp8_decode(FP8_FORMATS[fmt], code))
+    """Value of one code of a low-precision format (E2M1: the low 4 bits)."""
+    return float(_load().oracle_fp8_decode(LOWP_FORMATS[fmt], code))
 
 
 def gemm_block_scaled_f64(A, lda, SA, ldsa, B, ldb, SB, ldsb, M, N, K, block, afmt="e4m3", bfmt="e4m3",
-                          sfmt="e8m0"):
-    """(A .* scale_a)(B .* scale_b) in double from 8-bit codes; returns (M, N) float64."""
+                          sfmt="e8m0", acc=None, ld_acc=0):
+    """(A .* scale_a)(B .* scale_b) + acc in double from raw codes; returns (M, N) float64.
+
+    A, B: uint8 buffers of codes (E2M1: two per byte, even element in the low
+    nibble, element index row * ld + col).  acc: optional float32 buffer."""
     arrs = [_flat_buffer(np.ascontiguousarray(x, np.uint8)) for x in (A, SA, B, SB)]
+    accp = None
+    if acc is not None:
+        acc = _flat_buffer(np.ascontiguousarray(acc, np.float32))
+        accp = _p(acc)
     C = np.empty((M, N), np.float64)
-    _load().oracle_gemm_block_scaled_f64(FP8_FORMATS[afmt], FP8_FORMATS[bfmt], FP8_FORMATS[sfmt], _p(arrs[0]), lda,
-                                         _p(arrs[1]), ldsa, _p(arrs[2]), ldb, _p(arrs[3]), ldsb, M, N, K, block,
-                                         _p(C), N)
+    _load().oracle_gemm_block_scaled_f64(LOWP_FORMATS[afmt], LOWP_FORMATS[bfmt], LOWP_FORMATS[sfmt], _p(arrs[0]),
+                                         lda, _p(arrs[1]), ldsa, _p(arrs[2]), ldb, _p(arrs[3]), ldsb, accp, ld_acc,
+                                         M, N, K, block, _p(C), N)
     return C
 
 

@@ -269,15 +269,25 @@ static double bf16_to_f64(uint16_t b) {
     return (double)f;
 }
 
-/* 8-bit formats, decoded from their definitions (OCP 8-bit floating point and
- * microscaling formats): fmt 0 = E4M3 (bias 7, subnormals, no infinities,
- * S.1111.111 is NaN), 1 = E5M2 (bias 15, IEEE-style infinities and NaNs),
- * 2 = E8M0 (unsigned exponent: 2^(e-127), 0xFF is NaN). */
+/* Low-precision formats, decoded from their definitions (OCP 8-bit floating
+ * point and microscaling formats):
+ *   fmt 0 = E4M3 (bias 7, subnormals, no infinities, S.1111.111 is NaN)
+ *   fmt 1 = E5M2 (bias 15, IEEE-style infinities and NaNs)
+ *   fmt 2 = E8M0 (unsigned exponent: 2^(e-127), 0xFF is NaN)
+ *   fmt 3 = E2M1 (4-bit: bias 1, one subnormal 0.5, no infinities or NaNs;
+ *           the code is the low 4 bits of b) */
 double oracle_fp8_decode(int fmt, uint8_t b) {
     if (fmt == 2) return b == 0xFF ? NAN : ldexp(1.0, (int)b - 127);
-    int sign = b >> 7;
-    int e, m;
+    int sign, e, m;
     double v;
+    if (fmt == 3) {
+        sign = (b >> 3) & 1;
+        e = (b >> 1) & 3;
+        m = b & 1;
+        v = e == 0 ? 0.5 * m : ldexp((double)(2 + m), e - 2);
+        return sign ? -v : v;
+    }
+    sign = b >> 7;
     if (fmt == 0) {
         e = (b >> 3) & 15;
         m = b & 7;
@@ -292,25 +302,34 @@ double oracle_fp8_decode(int fmt, uint8_t b) {
     return sign ? -v : v;
 }
 
+/* Element i (row * ld + col) of a row-major low-precision matrix.  E2M1
+ * elements are packed two per byte, element i in byte i / 2, the even one in
+ * the low nibble. */
+static double lowp_at(int fmt, const uint8_t* p, int64_t i) {
+    if (fmt == 3) return oracle_fp8_decode(3, (uint8_t)(p[i >> 1] >> (4 * (i & 1))));
+    return oracle_fp8_decode(fmt, p[i]);
+}
+
 /* Block-scaled GEMM reference.
- * cuTile.jl "Operations", muladd_scaled: (a .* a_scale) * (b .* b_scale) + acc
+ * cuTile.jl "Operations", muladd_scaled: D = (a .* a_scale) * (b .* b_scale) + acc
  * where each scale element multiplies a contiguous block of `block` = K / K_s
  * elements along K; a_scale is (M, K_s), b_scale is (K_s, N).  Operands in
- * E4M3 or E5M2 (afmt, bfmt), scales in E8M0 or E4M3 (sfmt).  Every scaled
- * operand and every product is exact in double; the sum runs in double,
- * k = 0..K-1. */
+ * E4M3, E5M2 or E2M1 (afmt, bfmt), scales in E8M0 or E4M3 (sfmt), acc fp32
+ * (NULL: zero).  Every scaled operand and every product is exact in double;
+ * the sum runs in double over k = 0..K-1, then acc is added. */
 void oracle_gemm_block_scaled_f64(int afmt, int bfmt, int sfmt, const uint8_t* A, int64_t lda, const uint8_t* SA,
                                   int64_t ldsa, const uint8_t* B, int64_t ldb, const uint8_t* SB, int64_t ldsb,
-                                  int64_t M, int64_t N, int64_t K, int64_t block, double* C, int64_t ldc) {
+                                  const float* acc, int64_t ld_acc, int64_t M, int64_t N, int64_t K, int64_t block,
+                                  double* D, int64_t ldd) {
     for (int64_t m = 0; m < M; ++m)
         for (int64_t n = 0; n < N; ++n) {
             double s = 0.0;
             for (int64_t k = 0; k < K; ++k) {
-                double a = oracle_fp8_decode(afmt, A[m * lda + k]) * oracle_fp8_decode(sfmt, SA[m * ldsa + k / block]);
-                double b = oracle_fp8_decode(bfmt, B[k * ldb + n]) * oracle_fp8_decode(sfmt, SB[(k / block) * ldsb + n]);
+                double a = lowp_at(afmt, A, m * lda + k) * oracle_fp8_decode(sfmt, SA[m * ldsa + k / block]);
+                double b = lowp_at(bfmt, B, k * ldb + n) * oracle_fp8_decode(sfmt, SB[(k / block) * ldsb + n]);
                 s += a * b;
             }
-            C[m * ldc + n] = s;
+            D[m * ldd + n] = s + (acc ? (double)acc[m * ld_acc + n] : 0.0);
         }
 }
 

@@ -476,6 +476,11 @@ def test_bf16_rne_matches_torch_on_binary32_values():
 
 
 # ----------------------------------------------------------------------------- block-scaled GEMM
+# Formats: OCP 8-bit floating point / microscaling formats; the GEMM is
+# cuTile.jl "Operations", muladd_scaled.
+
+E2M1_VALUES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]  # the format's whole positive value set
+
 
 @pytest.mark.parametrize("fmt,tdt", [("e4m3", torch.float8_e4m3fn), ("e5m2", torch.float8_e5m2),
                                      ("e8m0", torch.float8_e8m0fnu)])
@@ -486,30 +491,90 @@ def test_fp8_decode_all_codes_equal_torch(fmt, tdt):
     assert np.array_equal(np.isnan(got), np.isnan(want))
     ok = ~np.isnan(want)
     np.testing.assert_array_equal(got[ok], want[ok])
+    np.testing.assert_array_equal(np.signbit(got[ok]), np.signbit(want[ok]))
+
+
+def test_e2m1_decode_is_the_format_table():
+    got = [oracle.fp8_decode("e2m1", c) for c in range(16)]
+    assert got[:8] == E2M1_VALUES
+    assert got[8:] == [-v for v in E2M1_VALUES]
+    assert np.signbit(got[8])  # code 0b1000 is -0
+
+
+def _fp8_codes(seed, shape):
+    """Uniform E4M3 codes with the two NaN codes replaced by 1.0 (0x38)."""
+    c = synth.int_below(seed, int(np.prod(shape)), 256).astype(np.uint8).reshape(shape)
+    c[(c & 0x7F) == 0x7F] = 0x38
+    return c
+
+
+def _e4m3(codes):
+    return torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
 
 
 def test_block_scaled_unit_scales_equal_numpy_matmul():
     M, N, K, bs = 7, 9, 64, 32
-    A = synth.int_below(81, M * K, 256).astype(np.uint8).reshape(M, K)
-    B = synth.int_below(82, K * N, 256).astype(np.uint8).reshape(K, N)
-    A[(A & 0x7F) == 0x7F] = 0x38  # keep NaN codes out (0x38 = 1.0)
-    B[(B & 0x7F) == 0x7F] = 0x38
+    A, B = _fp8_codes(81, (M, K)), _fp8_codes(82, (K, N))
     SA = np.full((M, K // bs), 127, np.uint8)
     SB = np.full((K // bs, N), 127, np.uint8)
     C = oracle.gemm_block_scaled_f64(A, K, SA, K // bs, B, N, SB, N, M, N, K, bs)
-    a = torch.from_numpy(A).view(torch.float8_e4m3fn).to(torch.float64).numpy()
-    b = torch.from_numpy(B).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_allclose(C, _e4m3(A) @ _e4m3(B), rtol=1e-12, atol=1e-9)
+
+
+def test_block_scaled_e4m3_scales_equal_broadcast_matmul():
+    # Scales E4M3 over blocks of 16 along K, odd leading dimensions everywhere:
+    # (A * repeat(SA, 16, axis=1)) @ (B * repeat(SB, 16, axis=0)) in numpy.
+    M, N, K, bs = 11, 13, 80, 16
+    Ks = K // bs
+    lda, ldb, ldsa, ldsb = K + 3, N + 5, Ks + 1, N + 2
+    A, B = _fp8_codes(83, (M, lda)), _fp8_codes(84, (K, ldb))
+    SA = (0x30 + synth.int_below(85, M * ldsa, 16)).astype(np.uint8).reshape(M, ldsa)  # scales in [0.5, 1.875]
+    SB = (0x30 + synth.int_below(86, Ks * ldsb, 16)).astype(np.uint8).reshape(Ks, ldsb)
+    C = oracle.gemm_block_scaled_f64(A, lda, SA, ldsa, B, ldb, SB, ldsb, M, N, K, bs, sfmt="e4m3")
+    a = _e4m3(A[:, :K]) * np.repeat(_e4m3(SA[:, :Ks]), bs, axis=1)
+    b = _e4m3(B[:, :N]) * np.repeat(_e4m3(SB[:, :N]), bs, axis=0)
     np.testing.assert_allclose(C, a @ b, rtol=1e-12, atol=1e-9)
 
 
-def test_block_scaled_closed_form():
-    # ones times ones with scale_a[m][j] = 2^(m % 3) and scale_b[j][n] = 2^(j % 2):
-    # C[m][n] = bs * 2^(m % 3) * (#even blocks + 2 * #odd blocks)
+def test_block_scaled_e2m1_packed_equal_table_matmul():
+    # E2M1 operands, two per byte along each row, even element in the low nibble.
+    M, N, K, bs = 6, 10, 64, 32
+    ca = synth.int_below(87, M * K, 16).astype(np.uint8).reshape(M, K)
+    cb = synth.int_below(88, K * N, 16).astype(np.uint8).reshape(K, N)
+    pack = lambda c: (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
+    table = np.array(E2M1_VALUES + [-v for v in E2M1_VALUES])
+    SA = np.full((M, K // bs), 128, np.uint8)   # 2.0
+    SB = np.full((K // bs, N), 126, np.uint8)   # 0.5
+    C = oracle.gemm_block_scaled_f64(pack(ca), K, SA, K // bs, pack(cb), N, SB, N, M, N, K, bs,
+                                     afmt="e2m1", bfmt="e2m1")
+    np.testing.assert_array_equal(C, table[ca] @ table[cb])
+
+
+def test_block_scaled_closed_form_with_acc():
+    # ones times ones with scale_a[m][j] = 2^(m % 3) and scale_b[j][n] = 2^(j % 2), plus acc:
+    # D[m][n] = bs * 2^(m % 3) * (1 + 2 + 1) + acc[m][n]
     M, N, K, bs = 5, 4, 96, 32   # 3 blocks: j = 0, 1, 2
     A = np.full((M, K), 0x38, np.uint8)
     B = np.full((K, N), 0x38, np.uint8)
     SA = np.array([[127 + (m % 3)] * 3 for m in range(M)], np.uint8)
     SB = np.array([[127 + (j % 2)] * N for j in range(3)], np.uint8)
-    C = oracle.gemm_block_scaled_f64(A, K, SA, 3, B, N, SB, N, M, N, K, bs)
-    want = np.array([[bs * 2.0 ** (m % 3) * (2 + 2 * 1)] * N for m in range(M)])
+    acc = np.arange(M * N, dtype=np.float32).reshape(M, N) - 7.5
+    C = oracle.gemm_block_scaled_f64(A, K, SA, 3, B, N, SB, N, M, N, K, bs, acc=acc, ld_acc=N)
+    want = np.array([[bs * 2.0 ** (m % 3) * 4 for n in range(N)] for m in range(M)]) + acc
     np.testing.assert_array_equal(C, want)
+
+
+def test_block_scaled_nan_stays_in_its_row_and_column():
+    M, N, K, bs = 4, 5, 32, 32
+    A = np.full((M, K), 0x38, np.uint8)
+    B = np.full((K, N), 0x38, np.uint8)
+    A[2, 7] = 0x7F            # E4M3 NaN
+    SA = np.full((M, 1), 127, np.uint8)
+    SB = np.full((1, N), 127, np.uint8)
+    SB[0, 3] = 0xFF           # E8M0 NaN
+    C = oracle.gemm_block_scaled_f64(A, K, SA, 1, B, N, SB, N, M, N, K, bs)
+    nan = np.zeros((M, N), bool)
+    nan[2, :] = True
+    nan[:, 3] = True
+    np.testing.assert_array_equal(np.isnan(C), nan)
+    np.testing.assert_array_equal(C[~nan], 32.0)
