@@ -268,6 +268,53 @@ SBT_API sbt_status sbt_gemm_bounded(sbt_context* ctx, const void* A, int64_t lda
                             size_t workspace_bytes, void* stream);
 
 /*
+ * Block-scaled GEMM  D = (A .* a_scale) * (B .* b_scale) + acc.
+ * cuTile.jl "Operations", muladd_scaled: A (M x K) and B (K x N) in a
+ * low-precision float format, a_scale (M x K_s) and b_scale (K_s x N) in
+ * E8M0 or E4M3; scale element j of a row of a_scale (of a column of b_scale)
+ * multiplies the contiguous block of K / K_s elements k = j*K/K_s ..
+ * (j+1)*K/K_s - 1 of that row of A (column of B).  fp32 accumulator, fp32
+ * acc and D.
+ *
+ * Formats (OCP 8-bit floating point and microscaling formats):
+ *   SBT_FMT_E4M3  1-4-3, bias 7, no infinities, S.1111.111 is NaN
+ *   SBT_FMT_E5M2  1-5-2, bias 15, IEEE infinities and NaNs
+ *   SBT_FMT_E8M0  unsigned power of two 2^(e-127), 0xFF is NaN (scales only)
+ *   SBT_FMT_E2M1  4-bit 1-2-1, bias 1, values 0, 0.5, 1, 1.5, 2, 3, 4, 6
+ *                 (operands only); two per byte, element i of a row-major
+ *                 array (i = row * ld + col) in byte i / 2, the even element
+ *                 in the low nibble; ld must be even.
+ *
+ * a_fmt, b_fmt: E4M3, E5M2 or E2M1 (they may differ).  s_fmt: E8M0 or E4M3,
+ * both scale arrays.  A: device, row stride lda >= K (elements).  B: device,
+ * row stride ldb >= N.  a_scale: device bytes, row stride ld_sa >= K_s.
+ * b_scale: device bytes, row stride ld_sb >= N.  K_s >= 1 must divide K
+ * (K_s is ignored when K = 0).  acc: device fp32, row stride ld_acc >= N, or
+ * NULL for zero; it may be D itself (then ld_acc == ldd) but may not
+ * otherwise overlap D.  D: device fp32, row stride ldd >= N; elements outside
+ * M x N are never written.
+ *
+ * Accuracy: each scaled operand value (code value times its scale) is formed
+ * exactly and the products are summed in fp32, provided every scaled operand
+ * lies in the normal range of bf16/fp32 (E8M0 scale exponents from 2^-124 to
+ * 2^119 with E4M3 operands; any E4M3 scale).  NaN codes propagate to the row
+ * (A, a_scale) or column (B, b_scale) of D they feed.
+ *
+ * workspace: device scratch of at least sbt_gemm_block_scaled_workspace_size()
+ * bytes, 256-byte aligned, owned by the caller (bf16 copies of the scaled
+ * operands).
+ */
+typedef enum { SBT_FMT_E4M3 = 0, SBT_FMT_E5M2 = 1, SBT_FMT_E8M0 = 2, SBT_FMT_E2M1 = 3 } sbt_lowp_format;
+SBT_API sbt_status sbt_gemm_block_scaled_workspace_size(sbt_context* ctx, int64_t M, int64_t N, int64_t K,
+                                                        size_t* bytes);
+SBT_API sbt_status sbt_gemm_block_scaled(sbt_context* ctx, sbt_lowp_format a_fmt, const void* A, int64_t lda,
+                                         sbt_lowp_format b_fmt, const void* B, int64_t ldb, sbt_lowp_format s_fmt,
+                                         const void* a_scale, int64_t ld_sa, const void* b_scale, int64_t ld_sb,
+                                         int64_t K_s, const float* acc, int64_t ld_acc, float* D, int64_t ldd,
+                                         int64_t M, int64_t N, int64_t K, void* workspace, size_t workspace_bytes,
+                                         void* stream);
+
+/*
  * Boundary-tile GEMM without any device allocation.
  * The pages have no counterpart to this call; it exists for callers that
  * cannot allocate device memory when they multiply: code running while a

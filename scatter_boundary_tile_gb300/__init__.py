@@ -8,7 +8,8 @@ an op raises.
 Op names match the C ABI in ``include/sbt.h`` without the ``sbt_`` prefix:
 ``tile_load_padded``, ``tile_store_clipped``, ``gather_rows``, ``gather_cols``,
 ``scatter_rows_masked``, ``scatter_add_rows``, ``ragged_tile_load``, ``ragged_tile_store``, ``gemm_bounded`` (plus
-``gemm_bounded_workspace_size``).  Arrays are torch tensors on the device
+``gemm_bounded_workspace_size``), ``gemm_bounded_noalloc``, ``gemm_block_scaled`` (plus
+``gemm_block_scaled_workspace_size``).  Arrays are torch tensors on the device
 (only their data pointer is used; shapes and strides are the explicit
 arguments, in elements).
 """
@@ -33,7 +34,9 @@ PATHS = {"auto": 0, "scalar": 1, "vector": 2, "tma": 3}
 EXPORTS = ("sbt_create", "sbt_destroy", "sbt_set_path", "sbt_set_wait_limit_ns", "sbt_set_test_hook", "sbt_launch_count",
            "sbt_check_status", "sbt_last_error_message", "sbt_tile_load_padded", "sbt_tile_store_clipped",
            "sbt_gather_rows", "sbt_gather_cols", "sbt_scatter_rows_masked", "sbt_scatter_add_rows", "sbt_ragged_tile_load", "sbt_ragged_tile_store", "sbt_gemm_bounded_workspace_size",
-           "sbt_gemm_bounded", "sbt_gemm_bounded_noalloc")
+           "sbt_gemm_bounded", "sbt_gemm_block_scaled_workspace_size", "sbt_gemm_block_scaled",
+           "sbt_gemm_bounded_noalloc")
+LOWP_FORMATS = {"e4m3": 0, "e5m2": 1, "e8m0": 2, "e2m1": 3}  # sbt_lowp_format
 GEMM_NOALLOC_SCRATCH_BYTES = 16 << 20  # SBT_GEMM_NOALLOC_SCRATCH_BYTES in include/sbt.h
 
 
@@ -75,6 +78,9 @@ def load_library(path: str = LIB_PATH):
             "sbt_gemm_bounded_workspace_size": [p, i64, i64, i64, i64, i64, ctypes.POINTER(ctypes.c_size_t)],
             "sbt_gemm_bounded": [p, p, i64, p, i64, p, i64, ci, i64, i64, i64, p, ctypes.c_size_t, p],
             "sbt_gemm_bounded_noalloc": [p, p, i64, p, i64, p, i64, ci, i64, i64, i64, p],
+            "sbt_gemm_block_scaled_workspace_size": [p, i64, i64, i64, ctypes.POINTER(ctypes.c_size_t)],
+            "sbt_gemm_block_scaled": [p, ci, p, i64, ci, p, i64, ci, p, i64, p, i64, i64, p, i64, p, i64, i64, i64,
+                                      i64, p, ctypes.c_size_t, p],
         }
         for name, args in sig.items():
             f = getattr(lib, name)
@@ -255,6 +261,22 @@ def gemm_bounded(ctx, A, lda, B, ldb, C, ldc, M, N, K, workspace=None, workspace
     code = {"bf16": SBT_BF16, "f32": SBT_F32}[c_dtype] if isinstance(c_dtype, str) else int(c_dtype)
     _check(load_library().sbt_gemm_bounded(ctx.handle, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, code, M, N, K,
                                            _ptr(workspace), workspace_bytes, _stream(stream)))
+
+
+def gemm_block_scaled_workspace_size(ctx, M, N, K) -> int:
+    n = ctypes.c_size_t()
+    _check(load_library().sbt_gemm_block_scaled_workspace_size(ctx.handle, M, N, K, ctypes.byref(n)))
+    return int(n.value)
+
+
+def gemm_block_scaled(ctx, A, lda, B, ldb, a_scale, ld_sa, b_scale, ld_sb, K_s, D, ldd, M, N, K, acc=None, ld_acc=0,
+                      workspace=None, workspace_bytes=0, a_fmt="e4m3", b_fmt="e4m3", s_fmt="e8m0", stream=None):
+    """sbt_gemm_block_scaled: D = (A .* a_scale)(B .* b_scale) + acc; formats by name (see LOWP_FORMATS)."""
+    fmt = lambda f: LOWP_FORMATS[f] if isinstance(f, str) else int(f)
+    _check(load_library().sbt_gemm_block_scaled(ctx.handle, fmt(a_fmt), _ptr(A), lda, fmt(b_fmt), _ptr(B), ldb,
+                                                fmt(s_fmt), _ptr(a_scale), ld_sa, _ptr(b_scale), ld_sb, K_s,
+                                                _ptr(acc), ld_acc, _ptr(D), ldd, M, N, K, _ptr(workspace),
+                                                workspace_bytes, _stream(stream)))
 
 
 def gemm_bounded_noalloc(ctx, A, lda, B, ldb, C, ldc, M, N, K, c_dtype="bf16", stream=None):

@@ -54,6 +54,8 @@ struct GemmParams {
     char* C;
     int64_t ldc;
     int c_f32;
+    const float* acc;  // fp32 C only: added to the product before the store (NULL: nothing added)
+    int64_t ld_acc;
     int M, N, K;
     int m_tiles, n_tiles, k_blocks;
     unsigned int* status;
@@ -94,8 +96,14 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tmem
         if (col < p.N) {
             if (p.c_f32) {
                 float* Cp = reinterpret_cast<float*>(p.C);
-                for (int rr = 0; rr < 32 && row0 + rr < p.M; ++rr)
-                    Cp[(int64_t)(row0 + rr) * p.ldc + col] = buf[rr * 33 + lane];
+                if (p.acc) {
+                    for (int rr = 0; rr < 32 && row0 + rr < p.M; ++rr)
+                        Cp[(int64_t)(row0 + rr) * p.ldc + col] =
+                            buf[rr * 33 + lane] + __ldg(p.acc + (int64_t)(row0 + rr) * p.ld_acc + col);
+                } else {
+                    for (int rr = 0; rr < 32 && row0 + rr < p.M; ++rr)
+                        Cp[(int64_t)(row0 + rr) * p.ldc + col] = buf[rr * 33 + lane];
+                }
             } else {
                 __nv_bfloat16* Cp = reinterpret_cast<__nv_bfloat16*>(p.C);
                 for (int rr = 0; rr < 32 && row0 + rr < p.M; ++rr)
@@ -503,27 +511,22 @@ __global__ void __launch_bounds__(256) k_stage_bt(const uint16_t* __restrict__ B
     }
 }
 
-// C[m][n] = 0 for m < M, n < N (the K = 0 product).
-__global__ void k_zero_c(char* C, int64_t ldc, int M, int N, int es) {
+// C[m][n] = acc[m][n] (fp32 C), or 0 without acc, for m < M, n < N: the K = 0 result.
+__global__ void k_zero_c(char* C, int64_t ldc, int M, int N, int es, const float* acc, int64_t ld_acc) {
     const int64_t total = (int64_t)M * N;
     for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total; i += (int64_t)gridDim.x * blockDim.x) {
         const int64_t m = i / N, n = i - m * N;
         if (es == 4)
-            reinterpret_cast<float*>(C)[m * ldc + n] = 0.f;
+            reinterpret_cast<float*>(C)[m * ldc + n] = acc ? acc[m * ld_acc + n] : 0.f;
         else
             reinterpret_cast<uint16_t*>(C)[m * ldc + n] = 0;
     }
 }
 
-struct GemmDims {
-    int64_t Mp, Np, Kp;
-    size_t a_bytes, b_bytes;
-};
-
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-GemmDims gemm_dims(int64_t M, int64_t N, int64_t K) {
-    GemmDims d;
+sbt_gemm_layout gemm_dims(int64_t M, int64_t N, int64_t K) {
+    sbt_gemm_layout d;
     d.Mp = sbt_cdiv(M, 256) * 256;  // whole 256-row tiles for the CTA-pair kernel
     d.Np = sbt_cdiv(N, BN) * BN;
     d.Kp = sbt_cdiv(K, BK) * BK;
@@ -548,23 +551,27 @@ sbt_status encode_kmajor(sbt_context* ctx, CUtensorMap* map, void* base, int64_t
 
 size_t sbt_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
     if (M <= 0 || N <= 0 || K <= 0) return 0;
-    const GemmDims d = gemm_dims(M, N, K);
+    const sbt_gemm_layout d = gemm_dims(M, N, K);
     return d.a_bytes + d.b_bytes;
+}
+
+sbt_gemm_layout sbt_gemm_layout_of(int64_t M, int64_t N, int64_t K) { return gemm_dims(M, N, K); }
+
+sbt_status sbt_launch_gemm_zero_k(sbt_context* ctx, void* C, int64_t ldc, bool c_f32, const float* acc,
+                                  int64_t ld_acc, int64_t M, int64_t N, cudaStream_t stream) {
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(sbt_cdiv(M * N, 256), (int64_t)ctx->sm_count * 8));
+    k_zero_c<<<grid, 256, 0, stream>>>((char*)C, ldc, (int)M, (int)N, c_f32 ? 4 : 2, acc, ld_acc);
+    return sbt_after_launch(ctx, "gemm (K=0)");
 }
 
 sbt_status sbt_launch_gemm(sbt_context* ctx, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
                            int64_t ldc, sbt_dtype c_dtype, int64_t M, int64_t N, int64_t K, void* workspace,
                            size_t workspace_bytes, cudaStream_t stream) {
     (void)workspace_bytes;
-    const int es_c = c_dtype == SBT_F32 ? 4 : 2;
     if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2)
         return sbt_fail(SBT_ERR_INVALID_ARG, "gemm_bounded: extents must be below 2^30");
-    if (K == 0) {
-        const int grid = (int)std::min<int64_t>(sbt_cdiv(M * N, 256), (int64_t)ctx->sm_count * 8);
-        k_zero_c<<<grid, 256, 0, stream>>>((char*)C, ldc, (int)M, (int)N, es_c);
-        return sbt_after_launch(ctx, "gemm_bounded (K=0)");
-    }
-    const GemmDims d = gemm_dims(M, N, K);
+    if (K == 0) return sbt_launch_gemm_zero_k(ctx, C, ldc, c_dtype == SBT_F32, nullptr, 0, M, N, stream);
+    const sbt_gemm_layout d = gemm_dims(M, N, K);
     if (d.Np / 64 > 65535 || d.Kp / 64 > INT32_MAX)
         return sbt_fail(SBT_ERR_INVALID_ARG, "gemm_bounded: N too large for the staging grid");
     uint16_t* Ap = (uint16_t*)workspace;
@@ -581,19 +588,26 @@ sbt_status sbt_launch_gemm(sbt_context* ctx, const void* A, int64_t lda, const v
         k_stage_bt<<<g2, 256, 0, stream>>>((const uint16_t*)B, ldb, (int)K, (int)N, Bp, (int)d.Kp);
         if ((st = sbt_after_launch(ctx, "gemm_bounded (stage B)"))) return st;
     }
+    return sbt_launch_gemm_main(ctx, Ap, Bp, d, C, ldc, c_dtype == SBT_F32, nullptr, 0, M, N, K, stream);
+}
 
+sbt_status sbt_launch_gemm_main(sbt_context* ctx, const uint16_t* Ap, const uint16_t* Bp, const sbt_gemm_layout& d,
+                                void* C, int64_t ldc, bool c_f32, const float* acc, int64_t ld_acc, int64_t M,
+                                int64_t N, int64_t K, cudaStream_t stream) {
     // 2. tensor-core main kernel
     // CTA pairs when there are at least as many 256 x 256 tiles as SM pairs;
     // single CTAs (128 x 256 tiles) for smaller problems.
     const bool pair = ctx->sm_count >= 2 && (d.Mp / 256) * (d.Np / 256) >= ctx->sm_count / 2;
     CUtensorMap tmA, tmB;
-    sbt_status st = encode_kmajor(ctx, &tmA, Ap, d.Mp, d.Kp, BM);
+    sbt_status st = encode_kmajor(ctx, &tmA, (void*)Ap, d.Mp, d.Kp, BM);
     if (st) return st;
-    if ((st = encode_kmajor(ctx, &tmB, Bp, d.Np, d.Kp, pair ? 128 : BN))) return st;
+    if ((st = encode_kmajor(ctx, &tmB, (void*)Bp, d.Np, d.Kp, pair ? 128 : BN))) return st;
     GemmParams p;
     p.C = (char*)C;
     p.ldc = ldc;
-    p.c_f32 = c_dtype == SBT_F32;
+    p.c_f32 = c_f32;
+    p.acc = acc;
+    p.ld_acc = ld_acc;
     p.M = (int)M;
     p.N = (int)N;
     p.K = (int)K;

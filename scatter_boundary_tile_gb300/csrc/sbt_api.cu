@@ -343,4 +343,52 @@ sbt_status sbt_gemm_bounded(sbt_context* ctx, const void* A, int64_t lda, const 
                            (cudaStream_t)stream);
 }
 
+static bool is_operand_format(sbt_lowp_format f) {
+    return f == SBT_FMT_E4M3 || f == SBT_FMT_E5M2 || f == SBT_FMT_E2M1;
+}
+
+sbt_status sbt_gemm_block_scaled_workspace_size(sbt_context* ctx, int64_t M, int64_t N, int64_t K, size_t* bytes) {
+    SBT_REQUIRE(ctx && bytes, "NULL argument");
+    SBT_REQUIRE(M >= 0 && N >= 0 && K >= 0, "gemm_block_scaled: negative extent");
+    *bytes = sbt_gemm_workspace_bytes(M, N, K);
+    return SBT_OK;
+}
+
+sbt_status sbt_gemm_block_scaled(sbt_context* ctx, sbt_lowp_format a_fmt, const void* A, int64_t lda,
+                                 sbt_lowp_format b_fmt, const void* B, int64_t ldb, sbt_lowp_format s_fmt,
+                                 const void* a_scale, int64_t ld_sa, const void* b_scale, int64_t ld_sb, int64_t K_s,
+                                 const float* acc, int64_t ld_acc, float* D, int64_t ldd, int64_t M, int64_t N,
+                                 int64_t K, void* workspace, size_t workspace_bytes, void* stream) {
+    SBT_REQUIRE(ctx, "ctx is NULL");
+    SBT_REQUIRE(M >= 0 && N >= 0 && K >= 0, "gemm_block_scaled: negative extent");
+    if (!is_operand_format(a_fmt) || !is_operand_format(b_fmt))
+        return sbt_fail(SBT_ERR_UNSUPPORTED, "gemm_block_scaled: operands must be E4M3, E5M2 or E2M1");
+    if (s_fmt != SBT_FMT_E8M0 && s_fmt != SBT_FMT_E4M3)
+        return sbt_fail(SBT_ERR_UNSUPPORTED, "gemm_block_scaled: scales must be E8M0 or E4M3");
+    SBT_REQUIRE(K == 0 || (K_s >= 1 && K % K_s == 0), "gemm_block_scaled: K_s must divide K");
+    SBT_REQUIRE(lda >= K && ldb >= N && ldd >= N, "gemm_block_scaled: leading dimension smaller than the extent");
+    SBT_REQUIRE(K == 0 || (ld_sa >= K_s && ld_sb >= N), "gemm_block_scaled: scale leading dimension too small");
+    SBT_REQUIRE(!acc || ld_acc >= N, "gemm_block_scaled: ld_acc smaller than N");
+    SBT_REQUIRE(a_fmt != SBT_FMT_E2M1 || lda % 2 == 0, "gemm_block_scaled: E2M1 A needs an even lda");
+    SBT_REQUIRE(b_fmt != SBT_FMT_E2M1 || ldb % 2 == 0, "gemm_block_scaled: E2M1 B needs an even ldb");
+    SBT_REQUIRE(!acc || (const void*)acc != (const void*)D || ld_acc == ldd,
+                "gemm_block_scaled: acc aliasing D needs ld_acc == ldd");
+    if (M == 0 || N == 0) return SBT_OK;
+    SBT_REQUIRE(D, "gemm_block_scaled: D is NULL");
+    SBT_REQUIRE(K == 0 || (A && B && a_scale && b_scale), "gemm_block_scaled: NULL operand or scale");
+    const size_t need = sbt_gemm_workspace_bytes(M, N, K);
+    if (need > 0) {
+        if (!workspace || workspace_bytes < need)
+            return sbt_fail(SBT_ERR_ALIGNMENT,
+                            "gemm_block_scaled: workspace smaller than sbt_gemm_block_scaled_workspace_size()");
+        if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+            return sbt_fail(SBT_ERR_ALIGNMENT, "gemm_block_scaled: workspace must be 256-byte aligned");
+    }
+    sbt_status st = sbt_use_device(ctx);
+    if (st) return st;
+    return sbt_launch_gemm_block_scaled(ctx, (int)a_fmt, A, lda, (int)b_fmt, B, ldb, (int)s_fmt, a_scale, ld_sa,
+                                        b_scale, ld_sb, K_s, acc, ld_acc, D, ldd, M, N, K, workspace,
+                                        (cudaStream_t)stream);
+}
+
 }  // extern "C"

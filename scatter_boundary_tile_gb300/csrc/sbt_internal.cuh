@@ -89,6 +89,27 @@ sbt_status sbt_launch_ragged_store(sbt_context* ctx, int es, const void* tiles, 
 sbt_status sbt_launch_gemm(sbt_context* ctx, const void* A, int64_t lda, const void* B, int64_t ldb, void* C,
                            int64_t ldc, sbt_dtype c_dtype, int64_t M, int64_t N, int64_t K, void* workspace,
                            size_t workspace_bytes, cudaStream_t stream);
+// K-major padded operand copies of the tensor-core GEMM: A' [Mp][Kp] and
+// B'^T [Np][Kp] bf16, zero past M, N, K; B' starts a_bytes into the workspace.
+struct sbt_gemm_layout {
+    int64_t Mp, Np, Kp;
+    size_t a_bytes, b_bytes;
+};
+sbt_gemm_layout sbt_gemm_layout_of(int64_t M, int64_t N, int64_t K);
+// The tensor-core kernel over already staged operands; C (fp32 or bf16) gets
+// A'B'^T (+ acc, fp32 C only) for m < M, n < N.
+sbt_status sbt_launch_gemm_main(sbt_context* ctx, const uint16_t* Ap, const uint16_t* Bp, const sbt_gemm_layout& d,
+                                void* C, int64_t ldc, bool c_f32, const float* acc, int64_t ld_acc, int64_t M,
+                                int64_t N, int64_t K, cudaStream_t stream);
+// C = acc (or 0): the K = 0 result.
+sbt_status sbt_launch_gemm_zero_k(sbt_context* ctx, void* C, int64_t ldc, bool c_f32, const float* acc,
+                                  int64_t ld_acc, int64_t M, int64_t N, cudaStream_t stream);
+// Block-scaled GEMM (formats as sbt_lowp_format); workspace as sbt_gemm_layout_of.
+sbt_status sbt_launch_gemm_block_scaled(sbt_context* ctx, int a_fmt, const void* A, int64_t lda, int b_fmt,
+                                        const void* B, int64_t ldb, int s_fmt, const void* SA, int64_t ld_sa,
+                                        const void* SB, int64_t ld_sb, int64_t Ks, const float* acc, int64_t ld_acc,
+                                        float* D, int64_t ldd, int64_t M, int64_t N, int64_t K, void* workspace,
+                                        cudaStream_t stream);
 size_t sbt_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K);
 // TMA tensor-copy variants of the tile load / store (k_tiles_tma.cu) and their preconditions.
 bool sbt_tile_tma_ok(int es, const void* arr, int64_t rows, int64_t cols, int64_t stride_r, int64_t stride_c,

@@ -84,3 +84,73 @@ def gemm_bf16(seed: int = SEED_GEMM, M: int = 65, N: int = 97, K: int = 73, tag:
 
 
 GEMM_SHAPES = [(65, 97, 73), (1000, 1000, 1000), (8191, 8193, 4097)]
+
+SEED_GEMM_SCALED = 0x5B7006
+
+
+def lowp_codes(seed: int, shape, fmt: str) -> np.ndarray:
+    """Uniformly drawn codes of a low-precision format with NaN/infinity codes
+    replaced by the code of 1.0, so that magnitudes are log-uniform over the
+    format's whole range (zeros and subnormals included).  E2M1 returns one
+    nibble per uint8 (unpacked)."""
+    n = int(np.prod(shape))
+    if fmt == "e2m1":
+        return int_below(seed, n, 16).astype(np.uint8).reshape(shape)
+    c = int_below(seed, n, 256).astype(np.uint8).reshape(shape)
+    if fmt == "e4m3":
+        c[(c & 0x7F) == 0x7F] = 0x38
+    elif fmt == "e5m2":
+        c[(c & 0x7C) == 0x7C] = 0x3C
+    else:
+        raise ValueError(fmt)
+    return c
+
+
+def pack_e2m1(nibbles: np.ndarray) -> np.ndarray:
+    """Two E2M1 codes per byte along each row (even column in the low nibble); columns must be even."""
+    assert nibbles.shape[-1] % 2 == 0
+    return (nibbles[..., 0::2] | (nibbles[..., 1::2] << 4)).astype(np.uint8)
+
+
+def scale_codes(seed: int, shape, fmt: str) -> np.ndarray:
+    """E8M0 scales 2^-4 .. 2^4 (codes 123..131), or positive normal E4M3 scales 0.125 .. 7.5 (codes 0x20..0x4F)."""
+    n = int(np.prod(shape))
+    if fmt == "e8m0":
+        return (123 + int_below(seed, n, 9)).astype(np.uint8).reshape(shape)
+    if fmt == "e4m3":
+        return (0x20 + int_below(seed, n, 0x30)).astype(np.uint8).reshape(shape)
+    raise ValueError(fmt)
+
+
+def gemm_block_scaled(seed: int = SEED_GEMM_SCALED, M: int = 65, N: int = 97, K: int = 96, block: int = 32,
+                      afmt: str = "e4m3", bfmt: str = "e4m3", sfmt: str = "e8m0", tag: int = 0):
+    """A (M,K) and B (K,N) codes (see lowp_codes), a_scale (M,K/block), b_scale (K/block,N).
+    Leading dimensions: the smallest odd >= the extent for byte formats and the
+    smallest even for E2M1 (packed, ld in elements); ld_sa = smallest odd >= K_s,
+    ld_sb = smallest odd >= N, ldd = smallest odd >= N.  Padding codes are NaN
+    (0x7F) for byte formats and 0xFF (NaN in E8M0 and E4M3) for scales, so that
+    any read past K, K_s or N shows."""
+    Ks = K // block
+    even = lambda n: n + (n % 2)
+    lda = even(K) if afmt == "e2m1" else smallest_odd_at_least(K)
+    ldb = even(N) if bfmt == "e2m1" else smallest_odd_at_least(N)
+    ld_sa, ld_sb = smallest_odd_at_least(Ks), smallest_odd_at_least(N)
+    a = lowp_codes(stream_seed(seed, 4 * tag + 1), (M, K), afmt)
+    b = lowp_codes(stream_seed(seed, 4 * tag + 2), (K, N), bfmt)
+    if afmt == "e2m1":
+        A = pack_e2m1(np.pad(a, ((0, 0), (0, lda - K))))
+    else:
+        A = np.full((M, lda), 0x7F, np.uint8)
+        A[:, :K] = a
+    if bfmt == "e2m1":
+        B = pack_e2m1(np.pad(b, ((0, 0), (0, ldb - N))))
+    else:
+        B = np.full((K, ldb), 0x7F, np.uint8)
+        B[:, :N] = b
+    SA = np.full((M, ld_sa), 0xFF, np.uint8)
+    SB = np.full((Ks, ld_sb), 0xFF, np.uint8)
+    SA[:, :Ks] = scale_codes(stream_seed(seed, 4 * tag + 3), (M, Ks), sfmt)
+    SB[:, :N] = scale_codes(stream_seed(seed, 4 * tag + 4), (Ks, N), sfmt)
+    return {"A": A, "B": B, "SA": SA, "SB": SB, "M": M, "N": N, "K": K, "Ks": Ks, "block": block,
+            "lda": lda, "ldb": ldb, "ld_sa": ld_sa, "ld_sb": ld_sb, "ldd": smallest_odd_at_least(N),
+            "afmt": afmt, "bfmt": bfmt, "sfmt": sfmt}
