@@ -47,7 +47,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=8.0, help="CPU-baseline sample budget")
     ap.add_argument("--profile", default=None,
                     choices=["gather", "scatter", "scatter_add", "ragged", "ragged_store", "tile_load_tma", "tile_load", "tile_store", "tile_load_unaligned",
-                             "tile_store_unaligned", "gemm"],
+                             "tile_store_unaligned", "gemm", "gemm_scaled"],
                     help="only launch one operation's workload (warmup + steps launches) for ncu")
     ap.add_argument("--scale", type=float, default=1.0, help="--profile: fraction of the workload's rows")
     return ap.parse_args()
@@ -414,6 +414,27 @@ def run_ops(ctx, pk):
             del A, B, C, ws
     except Exception as e:  # the GEMM may be unavailable in this build
         ops["gemm_bounded"] = {"unavailable": str(e).splitlines()[0][:200]}
+
+    # block-scaled GEMM: E4M3 operands, E8M0 scales over blocks of 32 along K, fp32 out
+    for (M, N, K) in [(8191, 8193, 4096)]:
+        g = wl.gemm_block_scaled(M=M, N=N, K=K, block=32)
+        A, B, SA, SB = (dev_bytes(g[k]) for k in ("A", "B", "SA", "SB"))
+        D = torch.empty(M * g["ldd"] * 4, dtype=torch.uint8, device="cuda")
+        ws_n = sbt.gemm_block_scaled_workspace_size(ctx, M, N, K)
+        ws = torch.empty(max(ws_n, 256), dtype=torch.uint8, device="cuda")
+        fn = lambda: sbt.gemm_block_scaled(ctx, A, g["lda"], B, g["ldb"], SA, g["ld_sa"], SB, g["ld_sb"], g["Ks"],
+                                           D, g["ldd"], M, N, K, workspace=ws, workspace_bytes=ws_n)
+        med, _, _ = time_launches(fn, 10)
+        flops = 2.0 * M * N * K
+        tf = flops / med / 1e9
+        entry = {"ms": med, "TFLOP/s": tf, "frac_bf16": tf / pk["bf16_tflops"],
+                 "workload": "E4M3 x E4M3, E8M0 scales per 32 along K, fp32 D, no acc",
+                 "note": "whole call: scaled staging to bf16 + bf16 tensor-core kernel; fraction of the bf16 peak"}
+        split = kernel_split(fn, 5)
+        if split:
+            entry["kernels_ms"] = split
+        ops[f"gemm_block_scaled_{M}x{N}x{K}"] = entry
+        del A, B, SA, SB, D, ws
     return ops
 
 
@@ -659,6 +680,15 @@ def run_profile(args):
         else:
             fn = lambda: sbt.tile_store_clipped(ctx, tiles, gr, gc, 64, 32, ad, r_, c_, ld, 1, 0, 0, 64, 32,
                                                 dtype="f32")
+    elif op == "gemm_scaled":  # (8191, 8193, 4096) E4M3 / E8M0 per 32, scaled along M
+        M, N, K = max(1, int(8191 * f)), 8193, 4096
+        g = wl.gemm_block_scaled(M=M, N=N, K=K, block=32)
+        A, B, SA, SB = (dev_bytes(g[k]) for k in ("A", "B", "SA", "SB"))
+        D = torch.empty(M * g["ldd"] * 4, dtype=torch.uint8, device="cuda")
+        ws_n = sbt.gemm_block_scaled_workspace_size(ctx, M, N, K)
+        ws = torch.empty(max(ws_n, 256), dtype=torch.uint8, device="cuda")
+        fn = lambda: sbt.gemm_block_scaled(ctx, A, g["lda"], B, g["ldb"], SA, g["ld_sa"], SB, g["ld_sb"], g["Ks"],
+                                           D, g["ldd"], M, N, K, workspace=ws, workspace_bytes=ws_n)
     else:  # gemm: (8191, 8193, 4097) scaled along M
         M, N, K = max(1, int(8191 * f)), 8193, 4097
         g = wl.gemm_bf16(M=M, N=N, K=K)

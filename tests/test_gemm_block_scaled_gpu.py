@@ -180,9 +180,9 @@ def test_rejected_before_launch(ctx, case, status):
         kw["workspace_bytes"] = ws_n - 1
     elif case == "acc_alias_other_ld":
         acc, ld_acc, ldd = D, N + 1, N
-    before = ctx.launch_count()
+    before = ctx.launch_count
     with pytest.raises(sbt.SbtError) as e:
         sbt.gemm_block_scaled(ctx, buf, lda, buf, N, buf, Ks, buf, N, Ks, D, ldd, M, N, K, acc=acc, ld_acc=ld_acc,
                               **kw)
     assert e.value.status == status
-    assert ctx.launch_count() == before
+    assert ctx.launch_count == before
