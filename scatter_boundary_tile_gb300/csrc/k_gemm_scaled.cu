@@ -24,46 +24,68 @@ namespace {
 constexpr int kFmtE4M3 = 0, kFmtE5M2 = 1, kFmtE8M0 = 2, kFmtE2M1 = 3;
 
 // Value of one code, from the format definitions (OCP 8-bit floating point
-// and microscaling formats).  Normal values are assembled as fp32 bit
-// patterns; subnormal ones as (integer significand) * 2^-bias', both exact.
-__device__ __forceinline__ float lowp_value(int fmt, uint32_t c) {
-    if (fmt == kFmtE8M0) {
-        if (c == 255u) return __uint_as_float(0x7FC00000u);
-        return __uint_as_float(c ? c << 23 : 0x00400000u);  // 2^(c-127); c = 0 is the fp32 subnormal 2^-127
-    }
-    float v;
-    uint32_t neg;
-    if (fmt == kFmtE2M1) {
-        neg = (c >> 3) & 1u;
-        const uint32_t e = (c >> 1) & 3u, m = c & 1u;
-        v = e ? __uint_as_float(((e + 126u) << 23) | (m << 22)) : 0.5f * (float)m;
-    } else if (fmt == kFmtE4M3) {
-        neg = c >> 7;
-        const uint32_t e = (c >> 3) & 15u, m = c & 7u;
-        if (e == 15u && m == 7u) return __uint_as_float(0x7FC00000u);
-        v = e ? __uint_as_float(((e + 120u) << 23) | (m << 20)) : (float)m * 0x1p-9f;
+// and microscaling formats).  The exponent and mantissa fields are placed at
+// the top of an fp32 bit pattern and the result is rescaled by the power of
+// two that turns the fp32 bias into the format's bias: the fields of a normal
+// code become a normal fp32 number and those of a subnormal code an fp32
+// subnormal with the same significand, so one exact multiply covers both.
+template <int FMT>
+__device__ __forceinline__ float lowp_value(uint32_t c) {
+    if constexpr (FMT == kFmtE8M0) {
+        return __uint_as_float(c == 255u ? 0x7FC00000u : c ? c << 23 : 0x00400000u);  // 2^(c-127)
+    } else if constexpr (FMT == kFmtE2M1) {
+        const float v = __uint_as_float((c & 7u) << 22) * 0x1p126f;  // bias 1
+        return __uint_as_float(__float_as_uint(v) | ((c & 8u) << 28));
+    } else if constexpr (FMT == kFmtE4M3) {
+        const float v = __uint_as_float((c & 0x7Fu) << 20) * 0x1p120f;  // bias 7
+        const uint32_t bits = (c & 0x7Fu) == 0x7Fu ? 0x7FC00000u : __float_as_uint(v);
+        return __uint_as_float(bits | ((c & 0x80u) << 24));
     } else {  // E5M2
-        neg = c >> 7;
-        const uint32_t e = (c >> 2) & 31u, m = c & 3u;
-        if (e == 31u) v = m ? __uint_as_float(0x7FC00000u) : __uint_as_float(0x7F800000u);
-        else v = e ? __uint_as_float(((e + 112u) << 23) | (m << 21)) : (float)m * 0x1p-16f;
+        const float v = __uint_as_float((c & 0x7Fu) << 21) * 0x1p112f;  // bias 15
+        uint32_t bits = __float_as_uint(v);
+        if ((c & 0x7Cu) == 0x7Cu) bits = (c & 3u) ? 0x7FC00000u : 0x7F800000u;
+        return __uint_as_float(bits | ((c & 0x80u) << 24));
     }
-    return neg ? -v : v;
 }
 
 // Code of element i (= row * ld + col) of a row-major operand; E2M1 packs two
 // per byte, the even element in the low nibble.
-__device__ __forceinline__ uint32_t lowp_code(int fmt, const uint8_t* __restrict__ p, int64_t i) {
-    if (fmt == kFmtE2M1) return (uint32_t)(__ldg(p + (i >> 1)) >> (4 * (int)(i & 1))) & 15u;
-    return __ldg(p + i);
+template <int FMT>
+__device__ __forceinline__ uint32_t lowp_code(const uint8_t* __restrict__ p, int64_t i) {
+    if constexpr (FMT == kFmtE2M1) return (uint32_t)(__ldg(p + (i >> 1)) >> (4 * (int)(i & 1))) & 15u;
+    else return __ldg(p + i);
 }
 
-__device__ __forceinline__ uint32_t bf16_bits(float x) {
-    return (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(x));
+// Eight bytes from p..p+7 (all inside the array) through aligned 8-byte loads.
+// The aligned word holding p, and when p is unaligned the one holding p+7,
+// each contain a byte of the array, so neither reaches past its pages.
+__device__ __forceinline__ uint64_t load8_any(const uint8_t* p) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    const int sh = (int)(a & 7u) * 8;
+    const uint64_t* w = reinterpret_cast<const uint64_t*>(a & ~(uintptr_t)7);
+    const uint64_t lo = __ldg(w);
+    if (sh == 0) return lo;
+    return (lo >> sh) | (__ldg(w + 1) << (64 - sh));
+}
+
+// Four bytes from p..p+3 (all inside the array), the same way.
+__device__ __forceinline__ uint32_t load4_any(const uint8_t* p) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    const int sh = (int)(a & 3u) * 8;
+    const uint32_t* w = reinterpret_cast<const uint32_t*>(a & ~(uintptr_t)3);
+    const uint32_t lo = __ldg(w);
+    if (sh == 0) return lo;
+    return (lo >> sh) | (__ldg(w + 1) << (32 - sh));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    const __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<const uint32_t*>(&v);
 }
 
 // A' [Mp][Kp] <- A .* a_scale, zero past M or K.  One 16-byte vector (8 k) of A' per task.
-__global__ void __launch_bounds__(256) k_stage_scaled_a(int fmt, int sfmt, const uint8_t* __restrict__ A, int64_t lda,
+template <int FMT, int SFMT>
+__global__ void __launch_bounds__(256) k_stage_scaled_a(const uint8_t* __restrict__ A, int64_t lda,
                                                         const uint8_t* __restrict__ SA, int64_t ld_sa, int block,
                                                         int M, int K, uint16_t* __restrict__ Ap, int Kp,
                                                         int64_t total_vecs) {
@@ -74,21 +96,35 @@ __global__ void __launch_bounds__(256) k_stage_scaled_a(int fmt, int sfmt, const
         const int k0 = (int)(v - m * kv) * 8;
         uint32_t w[4] = {0, 0, 0, 0};
         if (m < M && k0 < K) {
+            float x[8];
+            if (k0 + 8 <= K) {  // whole vector inside the row: word loads
+                if constexpr (FMT == kFmtE2M1) {
+                    const uint32_t c = load4_any(A + ((m * lda + k0) >> 1));
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x[e] = lowp_value<FMT>((c >> (4 * e)) & 15u);
+                } else {
+                    const uint64_t c = load8_any(A + m * lda + k0);
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) x[e] = lowp_value<FMT>((uint32_t)(c >> (8 * e)) & 255u);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = k0 + e < K ? lowp_value<FMT>(lowp_code<FMT>(A, m * lda + k0 + e)) : 0.f;
+            }
             int kb = k0 / block, kr = k0 - kb * block;
-            float s = lowp_value(sfmt, __ldg(SA + m * ld_sa + kb));
+            float s = lowp_value<SFMT>(__ldg(SA + m * ld_sa + kb));
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
-                const int k = k0 + e;
-                if (k < K) {
-                    if (kr == block) {  // next scale block
-                        ++kb;
-                        kr = 0;
-                        s = lowp_value(sfmt, __ldg(SA + m * ld_sa + kb));
-                    }
-                    w[e >> 1] |= bf16_bits(lowp_value(fmt, lowp_code(fmt, A, m * lda + k)) * s) << (16 * (e & 1));
-                    ++kr;
+                if (kr == block) {  // next scale block (only read while k < K)
+                    ++kb;
+                    kr = 0;
+                    if (k0 + e < K) s = lowp_value<SFMT>(__ldg(SA + m * ld_sa + kb));
                 }
+                x[e] *= s;
+                ++kr;
             }
+#pragma unroll
+            for (int e = 0; e < 4; ++e) w[e] = pack_bf16x2(x[2 * e], x[2 * e + 1]);
         }
         sbt_st_v4(Ap + m * Kp + k0, make_uint4(w[0], w[1], w[2], w[3]));
     }
@@ -96,22 +132,25 @@ __global__ void __launch_bounds__(256) k_stage_scaled_a(int fmt, int sfmt, const
 
 // B'^T [Np][Kp] <- transpose of B .* b_scale, zero past K or N.  64 x 64 tiles
 // through shared memory: reads along n, 16-byte writes along k.
-__global__ void __launch_bounds__(256) k_stage_scaled_bt(int fmt, int sfmt, const uint8_t* __restrict__ B, int64_t ldb,
+template <int FMT, int SFMT>
+__global__ void __launch_bounds__(256) k_stage_scaled_bt(const uint8_t* __restrict__ B, int64_t ldb,
                                                          const uint8_t* __restrict__ SB, int64_t ld_sb, int block,
                                                          int K, int N, uint16_t* __restrict__ Bp, int Kp) {
-    __shared__ uint16_t t[64][66];
+    __shared__ float t[64][65];
+    __shared__ int s_kb[64];
     const int k0 = blockIdx.x * 64, n0 = blockIdx.y * 64;
+    if (threadIdx.x < 64) s_kb[threadIdx.x] = (k0 + (int)threadIdx.x) / block;
+    __syncthreads();
 #pragma unroll 4
     for (int i = 0; i < 16; ++i) {
         const int idx = i * 256 + threadIdx.x;
         const int kk = idx >> 6, nn = idx & 63;
         const int k = k0 + kk, n = n0 + nn;
-        uint32_t x = 0;
-        if (k < K && n < N) {
-            const float s = lowp_value(sfmt, __ldg(SB + (int64_t)(k / block) * ld_sb + n));
-            x = bf16_bits(lowp_value(fmt, lowp_code(fmt, B, (int64_t)k * ldb + n)) * s);
-        }
-        t[kk][nn] = (uint16_t)x;
+        float x = 0.f;
+        if (k < K && n < N)
+            x = lowp_value<FMT>(lowp_code<FMT>(B, (int64_t)k * ldb + n)) *
+                lowp_value<SFMT>(__ldg(SB + (int64_t)s_kb[kk] * ld_sb + n));
+        t[kk][nn] = x;
     }
     __syncthreads();
 #pragma unroll
@@ -120,11 +159,48 @@ __global__ void __launch_bounds__(256) k_stage_scaled_bt(int fmt, int sfmt, cons
         const int nn = task >> 3, kv = task & 7;
         uint32_t w[4];
 #pragma unroll
-        for (int e = 0; e < 4; ++e)
-            w[e] = (uint32_t)t[kv * 8 + 2 * e][nn] | ((uint32_t)t[kv * 8 + 2 * e + 1][nn] << 16);
+        for (int e = 0; e < 4; ++e) w[e] = pack_bf16x2(t[kv * 8 + 2 * e][nn], t[kv * 8 + 2 * e + 1][nn]);
         sbt_st_v4(Bp + (int64_t)(n0 + nn) * Kp + k0 + kv * 8, make_uint4(w[0], w[1], w[2], w[3]));
     }
 }
+
+template <int FMT, int SFMT>
+void launch_stage_a(dim3 g, cudaStream_t st, const uint8_t* A, int64_t lda, const uint8_t* SA, int64_t ld_sa,
+                    int block, int M, int K, uint16_t* Ap, int Kp, int64_t vecs) {
+    k_stage_scaled_a<FMT, SFMT><<<g, 256, 0, st>>>(A, lda, SA, ld_sa, block, M, K, Ap, Kp, vecs);
+}
+
+template <int FMT, int SFMT>
+void launch_stage_bt(dim3 g, cudaStream_t st, const uint8_t* B, int64_t ldb, const uint8_t* SB, int64_t ld_sb,
+                     int block, int K, int N, uint16_t* Bp, int Kp) {
+    k_stage_scaled_bt<FMT, SFMT><<<g, 256, 0, st>>>(B, ldb, SB, ld_sb, block, K, N, Bp, Kp);
+}
+
+// One instantiation per (operand format, scale format) pair.
+template <template <int, int> class F, typename... Args>
+void dispatch_formats(int fmt, int sfmt, Args... args) {
+    if (sfmt == kFmtE8M0) {
+        if (fmt == kFmtE4M3) F<kFmtE4M3, kFmtE8M0>::run(args...);
+        else if (fmt == kFmtE5M2) F<kFmtE5M2, kFmtE8M0>::run(args...);
+        else F<kFmtE2M1, kFmtE8M0>::run(args...);
+    } else {
+        if (fmt == kFmtE4M3) F<kFmtE4M3, kFmtE4M3>::run(args...);
+        else if (fmt == kFmtE5M2) F<kFmtE5M2, kFmtE4M3>::run(args...);
+        else F<kFmtE2M1, kFmtE4M3>::run(args...);
+    }
+}
+
+template <int FMT, int SFMT>
+struct StageA {
+    template <typename... Args>
+    static void run(Args... args) { launch_stage_a<FMT, SFMT>(args...); }
+};
+
+template <int FMT, int SFMT>
+struct StageBt {
+    template <typename... Args>
+    static void run(Args... args) { launch_stage_bt<FMT, SFMT>(args...); }
+};
 
 }  // namespace
 
@@ -143,13 +219,13 @@ sbt_status sbt_launch_gemm_block_scaled(sbt_context* ctx, int a_fmt, const void*
     uint16_t* Bp = (uint16_t*)((char*)workspace + d.a_bytes);
     const int64_t vecs = d.Mp * (d.Kp / 8);
     const int grid = (int)std::min<int64_t>(sbt_cdiv(vecs, 256), (int64_t)ctx->sm_count * 8);
-    k_stage_scaled_a<<<grid, 256, 0, stream>>>(a_fmt, s_fmt, (const uint8_t*)A, lda, (const uint8_t*)SA, ld_sa, block,
-                                               (int)M, (int)K, Ap, (int)d.Kp, vecs);
+    dispatch_formats<StageA>(a_fmt, s_fmt, dim3((unsigned)grid), stream, (const uint8_t*)A, lda, (const uint8_t*)SA,
+                             ld_sa, block, (int)M, (int)K, Ap, (int)d.Kp, vecs);
     sbt_status st = sbt_after_launch(ctx, "gemm_block_scaled (stage A)");
     if (st) return st;
     dim3 g2((unsigned)(d.Kp / 64), (unsigned)(d.Np / 64));
-    k_stage_scaled_bt<<<g2, 256, 0, stream>>>(b_fmt, s_fmt, (const uint8_t*)B, ldb, (const uint8_t*)SB, ld_sb, block,
-                                              (int)K, (int)N, Bp, (int)d.Kp);
+    dispatch_formats<StageBt>(b_fmt, s_fmt, g2, stream, (const uint8_t*)B, ldb, (const uint8_t*)SB, ld_sb, block,
+                              (int)K, (int)N, Bp, (int)d.Kp);
     if ((st = sbt_after_launch(ctx, "gemm_block_scaled (stage B)"))) return st;
     return sbt_launch_gemm_main(ctx, Ap, Bp, d, D, ldd, true, acc, ld_acc, M, N, K, stream);
 }
