@@ -1,0 +1,544 @@
+// Block-scaled GEMM on the tensor cores' own block scaling.
+//
+// cuTile.jl "Operations", muladd_scaled with E4M3 / E5M2 operands and E8M0
+// scales over blocks of 32 along K: exactly the microscaling form that
+// tcgen05.mma.kind::mxf8f6f4.block_scale computes, one scale per row of A and
+// per column of B for each K = 32 step, fp32 accumulation in TMEM.
+//
+// Pipeline (all on the caller's stream):
+//  1. Staging (the bounded copy of Tylo.jl "Boundary tiles"): A -> A8 [Mp][Kp]
+//     and B -> B8^T [Np][Kp], 8-bit codes, K-major, zero past M, N, K; the
+//     scales are packed per (row tile, 128-deep K block) into 512-byte chunks
+//     in the order the tensor memory wants them (below), 2^0 past the extents.
+//  2. A persistent kernel on clusters of two CTAs (M = 256 per pair, N = 224
+//     per tile, 128 K per stage): warp 0 of each CTA TMA-loads its 128 rows of
+//     A8, its 112 rows of B8^T and the stage's scale chunks into a 5-stage
+//     ring; the leader's warp 1 copies the scale chunks into TMEM
+//     (tcgen05.cp.cta_group::2, each CTA's own chunk to its own TMEM) and
+//     issues four block-scaled MMAs per stage, one per K = 32 step, the step
+//     choosing the scale byte; four epilogue warps per CTA add acc and store
+//     fp32 D inside M x N.
+//
+// Scale placement in TMEM (per CTA, 32-bit columns, 4 scale bytes each): the
+// scale of row m (of this CTA's 128 rows of A) for step s sits in lane m,
+// column sfa + m / 32, byte s; that of column n of B (all 224 columns, in
+// both CTAs) in lanes n % 32 + 32 q of every quarter q, column sfb + n / 32,
+// byte s.  tcgen05.cp 32x128b.warpx4 writes row r of a [32][16-byte] chunk to
+// lane r of every quarter, so a chunk holds at byte 16 r + 4 j + s the scale
+// of row (or column) 32 j + r, step s.
+//
+// TMEM: two 224-column fp32 accumulators (the epilogue of one tile overlaps
+// the main loop of the next) and five 12-column scale slots, one per stage,
+// fill all 512 columns.  A slot is rewritten only after the stage's previous
+// MMAs completed: its new data arrives after the producer saw the stage's
+// empty barrier, which those MMAs' commit signals.
+#include <algorithm>
+#include <string>
+
+#include "sbt_internal.cuh"
+#include "tc_ptx.cuh"
+
+namespace {
+
+using namespace sbt_ptx;
+
+constexpr int MX_BN = 224;   // columns per tile
+constexpr int MX_BK = 128;   // K per stage (bytes of one 128-byte swizzle row)
+constexpr int kMxStages = 5;
+constexpr int kMxThreads = 192;  // warp 0: TMA, warp 1: MMA, warps 2..5: epilogue
+constexpr uint32_t kMxABytes = 128 * MX_BK;
+constexpr uint32_t kMxBBytes = (MX_BN / 2) * MX_BK;
+constexpr uint32_t kMxSfaOff = kMxABytes + kMxBBytes;  // 30720
+constexpr uint32_t kMxSfbOff = kMxSfaOff + 512;
+constexpr uint32_t kMxTxBytes = kMxSfbOff + 1024;      // bytes one CTA receives per stage
+constexpr uint32_t kMxStageBytes = 32768;              // keeps every stage's A tile 1024-aligned
+constexpr uint32_t kMxSfCol0 = 2 * MX_BN;              // scale slots after the two accumulators
+constexpr uint32_t kMxSfCols = 12;                      // 4 columns of A scales + 8 of B scales
+static_assert(kMxSfCol0 + kMxStages * kMxSfCols <= 512, "TMEM columns");
+static_assert(kMxTxBytes <= kMxStageBytes, "stage layout");
+constexpr int kMxEpiWarps = 4;
+constexpr int kMxEpiWords = 32 * 33;
+constexpr int kMxNumBars = 2 * kMxStages + 5;
+constexpr size_t kMxSmem =
+    1024 + (size_t)kMxStages * kMxStageBytes + (size_t)kMxEpiWarps * kMxEpiWords * 4 + kMxNumBars * 8 + 16;
+
+enum : unsigned int { kCodeProducer = 0x1100, kCodeMma = 0x1200, kCodeEpilogue = 0x1400, kCodeTeardown = 0x1800 };
+
+struct MxParams {
+    float* D;
+    int64_t ldd;
+    const float* acc;
+    int64_t ld_acc;
+    int M, N, K;
+    int m_tiles, n_tiles, k_blocks;  // 256-row tiles, 224-column tiles, 128-deep K blocks
+    uint32_t idesc;                  // formats, M = 256, N = 224; the scale byte is or-ed in per step
+    unsigned int* status;
+    uint64_t wait_ns;
+    int withhold_first_load;
+};
+
+constexpr int kGroupM = 8;
+__device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, int* mt, int* nt) {
+    const int per_group = kGroupM * n_tiles;
+    const int g = tile / per_group;
+    const int within = tile - g * per_group;
+    const int first_m = g * kGroupM;
+    const int gm = min(kGroupM, m_tiles - first_m);
+    *mt = first_m + within % gm;
+    *nt = within / gm;
+}
+
+// Drain this warp's 32 rows of one 128 x 224 accumulator, add acc and store
+// columns < N of rows < M through a padded shared transpose (one contiguous
+// 32-column segment per store instruction).
+__device__ __forceinline__ void mx_epilogue_tile(const MxParams& p, uint32_t tmem_acc, int q, int lane, float* buf,
+                                                 int row0, int n0) {
+    const int chunks = (min(MX_BN, p.N - n0) + 31) / 32;
+    for (int c = 0; c < chunks; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem_acc + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) buf[lane * 33 + j] = __uint_as_float(r[j]);
+        __syncwarp();
+        const int col = n0 + c * 32 + lane;
+        if (col < p.N) {
+            if (p.acc) {
+                for (int rr = 0; rr < 32 && row0 + rr < p.M; ++rr)
+                    p.D[(int64_t)(row0 + rr) * p.ldd + col] =
+                        buf[rr * 33 + lane] + __ldg(p.acc + (int64_t)(row0 + rr) * p.ld_acc + col);
+            } else {
+                for (int rr = 0; rr < 32 && row0 + rr < p.M; ++rr)
+                    p.D[(int64_t)(row0 + rr) * p.ldd + col] = buf[rr * 33 + lane];
+            }
+        }
+        __syncwarp();
+    }
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
+    k_gemm_mx_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
+                   const MxParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* epi = reinterpret_cast<float*>(smem + (size_t)kMxStages * kMxStageBytes);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(epi + kMxEpiWarps * kMxEpiWords);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kMxNumBars);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const uint32_t bar0 = smem_u32(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kMxStages + s); };
+    auto tfull_bar = [&](int a) { return bar0 + 8u * (2 * kMxStages + a); };
+    auto tempty_bar = [&](int a) { return bar0 + 8u * (2 * kMxStages + 2 + a); };
+    const uint32_t mma_done_bar = bar0 + 8u * (2 * kMxStages + 4);
+
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x / 32), 0);
+    const int lane = threadIdx.x % 32;
+    const uint32_t rank = cluster_ctarank();
+    const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kMxStages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(tfull_bar(a), 1);
+            mbar_init(tempty_bar(a), 2 * kMxEpiWarps * 32);
+        }
+        mbar_init(mma_done_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+        prefetch_tmap(&tmSA);
+        prefetch_tmap(&tmSB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), 512);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();  // both CTAs' barriers are initialised before any remote arrival
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    const int num_tiles = p.m_tiles * p.n_tiles;
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer (each CTA, own halves)
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            bool ok = true;
+            int64_t issued = 0;
+            for (int tile = cluster; ok && tile < num_tiles; tile += nclusters) {
+                int mt, nt;
+                tile_coords(tile, p.m_tiles, p.n_tiles, &mt, &nt);
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, p.wait_ns, abort_flag, p.status,
+                                           kCodeProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    const bool withhold = p.withhold_first_load && blockIdx.x == 0 && issued == 0;
+                    ++issued;
+                    if (!withhold) {
+                        const uint32_t sa = smem_u32(smem + (size_t)stage * kMxStageBytes);
+                        const uint32_t leader_full = mapa_shared(full_bar(stage), 0);
+                        if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * kMxTxBytes);
+                        tma_load_2d_pair(sa, &tmA, kb * MX_BK, mt * 256 + (int)rank * 128, leader_full);
+                        tma_load_2d_pair(sa + kMxABytes, &tmB, kb * MX_BK, nt * MX_BN + (int)rank * (MX_BN / 2),
+                                         leader_full);
+                        // scale chunks: [row group][K block] x 512 B as rows of 256 B; B: [tile][K block] x 1 KB
+                        tma_load_2d_pair(sa + kMxSfaOff, &tmSA, 0, ((mt * 2 + (int)rank) * p.k_blocks + kb) * 2,
+                                         leader_full);
+                        tma_load_2d_pair(sa + kMxSfbOff, &tmSB, 0, (nt * p.k_blocks + kb) * 4, leader_full);
+                    }
+                    if (++stage == kMxStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer (leader CTA only)
+        if (lane == 0 && rank == 0) {
+            uint32_t stage = 0, phase = 0;
+            int local = 0;
+            bool ok = true;
+            for (int tile = cluster; ok && tile < num_tiles; tile += nclusters, ++local) {
+                const int acc = local & 1;
+                const uint32_t use = (uint32_t)(local >> 1);
+                if (!mbar_wait_bounded(tempty_bar(acc), (use & 1u) ^ 1u, p.wait_ns, abort_flag, p.status,
+                                       kCodeMma)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * MX_BN);
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait_bounded(full_bar(stage), phase, p.wait_ns, abort_flag, p.status, kCodeMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + (size_t)stage * kMxStageBytes);
+                    const uint32_t sfa = tmem_base + kMxSfCol0 + kMxSfCols * (uint32_t)stage;
+                    const uint32_t sfb = sfa + 4;
+                    tc_cp_pair_32x128b_warpx4(sfa, smem_desc_rows16(sa + kMxSfaOff));
+                    tc_cp_pair_32x128b_warpx4(sfb, smem_desc_rows16(sa + kMxSfbOff));
+                    tc_cp_pair_32x128b_warpx4(sfb + 4, smem_desc_rows16(sa + kMxSfbOff + 512));
+                    const int k_rem = p.K - kb * MX_BK;
+                    const int k_steps = k_rem >= MX_BK ? MX_BK / 32 : (k_rem + 31) / 32;
+                    for (int ks = 0; ks < k_steps; ++ks)
+                        tc_mma_mx_pair(d_tmem, smem_desc_sw128(sa + 32u * ks),
+                                       smem_desc_sw128(sa + kMxABytes + 32u * ks),
+                                       p.idesc | ((uint32_t)ks << 4) | ((uint32_t)ks << 29), sfa, sfb,
+                                       (kb | ks) != 0 ? 1u : 0u);
+                    tc_commit_pair_multicast(empty_bar(stage), 0x3);
+                    if (++stage == kMxStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (ok) tc_commit_pair_multicast(tfull_bar(acc), 0x3);
+            }
+            tc_commit_pair_multicast(mma_done_bar, 0x1);
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(mma_done_bar, 0)) {
+                if (globaltimer() - t0 > p.wait_ns) {
+                    atomicOr(p.status, (unsigned int)kCodeTeardown);
+                    break;
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue (warps 2..5 of each CTA)
+        const int q = warp & 3;
+        float* buf = epi + (warp - 2) * kMxEpiWords;
+        const uint32_t leader_tempty0 = mapa_shared(tempty_bar(0), 0);
+        int local = 0;
+        for (int tile = cluster; tile < num_tiles; tile += nclusters, ++local) {
+            const int acc = local & 1;
+            const uint32_t use = (uint32_t)(local >> 1);
+            int mt, nt;
+            tile_coords(tile, p.m_tiles, p.n_tiles, &mt, &nt);
+            if (!mbar_wait_bounded(tfull_bar(acc), use & 1u, p.wait_ns, abort_flag, p.status, kCodeEpilogue)) break;
+            tc_fence_after();
+            mx_epilogue_tile(p, tmem_base + (uint32_t)(acc * MX_BN), q, lane, buf, mt * 256 + (int)rank * 128 + q * 32,
+                             nt * MX_BN);
+            tc_fence_before();
+            mbar_arrive_cluster(leader_tempty0 + 8u * acc);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // the leader's MMAs into the peer's TMEM are complete before either CTA frees it
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, 512);
+    }
+}
+
+// ---------------------------------------------------------------------------- staging
+
+// Eight bytes p..p+7, all inside the caller's array, through aligned 8-byte
+// loads (the words holding p and, when p is unaligned, p+7).
+__device__ __forceinline__ uint64_t load8_any(const uint8_t* p) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    const int sh = (int)(a & 7u) * 8;
+    const uint64_t* w = reinterpret_cast<const uint64_t*>(a & ~(uintptr_t)7);
+    const uint64_t lo = __ldg(w);
+    if (sh == 0) return lo;
+    return (lo >> sh) | (__ldg(w + 1) << (64 - sh));
+}
+
+// A8 [Mp][Kp] <- A [M][K] (row stride lda bytes), zero past M or K; 16 bytes per task.
+__global__ void __launch_bounds__(256) k_mx_stage_a(const uint8_t* __restrict__ A, int64_t lda, int M, int K,
+                                                    uint8_t* __restrict__ Ap, int Kp, int64_t tasks) {
+    const int kv = Kp / 16;
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < tasks; t += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t m = t / kv;
+        const int k0 = (int)(t - m * kv) * 16;
+        uint64_t lo = 0, hi = 0;
+        if (m < M && k0 < K) {
+            const uint8_t* row = A + m * lda;
+            if (k0 + 16 <= K) {
+                lo = load8_any(row + k0);
+                hi = load8_any(row + k0 + 8);
+            } else {
+                for (int e = 0; e < 16 && k0 + e < K; ++e) {
+                    const uint64_t b = __ldg(row + k0 + e);
+                    if (e < 8) lo |= b << (8 * e);
+                    else hi |= b << (8 * (e - 8));
+                }
+            }
+        }
+        sbt_st_v4(Ap + m * Kp + k0, make_uint4((uint32_t)lo, (uint32_t)(lo >> 32), (uint32_t)hi, (uint32_t)(hi >> 32)));
+    }
+}
+
+// B8^T [Np][Kp] <- transpose of B [K][N] (row stride ldb bytes), zero past K or N.
+// 64 (k) x 32 (n) tiles through shared memory, 128 threads.
+__global__ void __launch_bounds__(128) k_mx_stage_bt(const uint8_t* __restrict__ B, int64_t ldb, int K, int N,
+                                                     uint8_t* __restrict__ Bp, int Kp) {
+    __shared__ uint8_t t[64][36];
+    const int k0 = blockIdx.x * 64, n0 = blockIdx.y * 32;
+    {
+        const int kk = threadIdx.x >> 1, nh = (threadIdx.x & 1) * 16;
+        const int k = k0 + kk, n = n0 + nh;
+        uint64_t lo = 0, hi = 0;
+        if (k < K && n < N) {
+            const uint8_t* row = B + (int64_t)k * ldb;
+            if (n + 16 <= N) {
+                lo = load8_any(row + n);
+                hi = load8_any(row + n + 8);
+            } else {
+                for (int e = 0; e < 16 && n + e < N; ++e) {
+                    const uint64_t b = __ldg(row + n + e);
+                    if (e < 8) lo |= b << (8 * e);
+                    else hi |= b << (8 * (e - 8));
+                }
+            }
+        }
+#pragma unroll
+        for (int e = 0; e < 16; ++e) t[kk][nh + e] = (uint8_t)((e < 8 ? lo >> (8 * e) : hi >> (8 * (e - 8))) & 255u);
+    }
+    __syncthreads();
+    {
+        const int nn = threadIdx.x >> 2, kv = (threadIdx.x & 3) * 16;
+        uint32_t w[4] = {0, 0, 0, 0};
+#pragma unroll
+        for (int e = 0; e < 16; ++e) w[e >> 2] |= (uint32_t)t[kv + e][nn] << (8 * (e & 3));
+        sbt_st_v4(Bp + (int64_t)(n0 + nn) * Kp + k0 + kv, make_uint4(w[0], w[1], w[2], w[3]));
+    }
+}
+
+// Scale chunks.  SA8: chunk (g, kb) of 512 B for rows 128 g .. 128 g + 127 and
+// steps 4 kb .. 4 kb + 3; SB8: chunk (t, kb) of 1 KB = two 512-B halves for
+// columns 224 t + 128 h + (0..127).  Byte 16 r + 4 j + s of a 512-B part is
+// the scale of row / column 32 j + r of the part, step s; 127 (= 2^0) past
+// the extents (those operand codes are zero).  One 16-byte row r per task.
+__global__ void __launch_bounds__(256) k_mx_stage_scales(const uint8_t* __restrict__ SA, int64_t ld_sa,
+                                                         const uint8_t* __restrict__ SB, int64_t ld_sb, int M, int N,
+                                                         int Ks, int k_blocks, uint8_t* __restrict__ SAp,
+                                                         int64_t tasks_a, uint8_t* __restrict__ SBp, int64_t tasks_b) {
+    for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < tasks_a + tasks_b;
+         t += (int64_t)gridDim.x * blockDim.x) {
+        uint32_t w[4];
+        uint8_t* dst;
+        if (t < tasks_a) {
+            const int r = (int)(t & 31);
+            const int64_t chunk = t >> 5;
+            const int64_t g = chunk / k_blocks;
+            const int kb = (int)(chunk - g * k_blocks);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int64_t m = 128 * g + 32 * j + r;
+                uint32_t v = 0;
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const int ks = 4 * kb + s;
+                    const uint32_t c = (m < M && ks < Ks) ? (uint32_t)__ldg(SA + m * ld_sa + ks) : 127u;
+                    v |= c << (8 * s);
+                }
+                w[j] = v;
+            }
+            dst = SAp + t * 16;
+        } else {
+            const int64_t u = t - tasks_a;
+            const int r = (int)(u & 31);
+            const int h = (int)((u >> 5) & 1);
+            const int64_t chunk = u >> 6;
+            const int64_t tile = chunk / k_blocks;
+            const int kb = (int)(chunk - tile * k_blocks);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int within = 128 * h + 32 * j + r;
+                const int64_t n = tile * MX_BN + within;
+                uint32_t v = 0;
+#pragma unroll
+                for (int s = 0; s < 4; ++s) {
+                    const int ks = 4 * kb + s;
+                    const uint32_t c =
+                        (within < MX_BN && n < N && ks < Ks) ? (uint32_t)__ldg(SB + (int64_t)ks * ld_sb + n) : 127u;
+                    v |= c << (8 * s);
+                }
+                w[j] = v;
+            }
+            dst = SBp + u * 16;
+        }
+        sbt_st_v4(dst, make_uint4(w[0], w[1], w[2], w[3]));
+    }
+}
+
+struct MxLayout {
+    int64_t Mp, Np, Kp, k_blocks, m_tiles, n_tiles;
+    size_t a_off, b_off, sa_off, sb_off, total;
+};
+
+size_t round256(size_t x) { return (x + 255) / 256 * 256; }
+
+MxLayout mx_layout(int64_t M, int64_t N, int64_t K) {
+    MxLayout L;
+    L.k_blocks = sbt_cdiv(K, MX_BK);
+    L.Kp = L.k_blocks * MX_BK;
+    L.m_tiles = sbt_cdiv(M, 256);
+    L.Mp = L.m_tiles * 256;
+    L.n_tiles = sbt_cdiv(N, MX_BN);
+    L.Np = L.n_tiles * MX_BN;
+    L.a_off = 0;
+    L.b_off = round256((size_t)L.Mp * L.Kp);
+    L.sa_off = L.b_off + round256((size_t)L.Np * L.Kp);
+    L.sb_off = L.sa_off + round256((size_t)(L.Mp / 128) * L.k_blocks * 512);
+    L.total = L.sb_off + round256((size_t)L.n_tiles * L.k_blocks * 1024);
+    return L;
+}
+
+sbt_status encode_u8(sbt_context* ctx, CUtensorMap* map, void* base, int64_t inner, int64_t rows, int box_inner,
+                     int box_rows, bool swizzle) {
+    cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)inner};
+    cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = ctx->encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
+                                   CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                   swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS)
+        return sbt_fail(SBT_ERR_TENSOR_MAP, "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
+    return SBT_OK;
+}
+
+}  // namespace
+
+size_t sbt_gemm_mx_workspace_bytes(int64_t M, int64_t N, int64_t K) {
+    if (M <= 0 || N <= 0 || K <= 0) return 0;
+    return mx_layout(M, N, K).total;
+}
+
+sbt_status sbt_launch_gemm_mx(sbt_context* ctx, int a_fmt, const void* A, int64_t lda, int b_fmt, const void* B,
+                              int64_t ldb, const void* SA, int64_t ld_sa, const void* SB, int64_t ld_sb,
+                              const float* acc, int64_t ld_acc, float* D, int64_t ldd, int64_t M, int64_t N,
+                              int64_t K, void* workspace, cudaStream_t stream) {
+    const MxLayout L = mx_layout(M, N, K);
+    if (L.Np / 32 > 65535 || L.Kp / 64 > INT32_MAX)
+        return sbt_fail(SBT_ERR_INVALID_ARG, "gemm_block_scaled: N too large for the staging grid");
+    uint8_t* ws = (uint8_t*)workspace;
+    uint8_t *Ap = ws + L.a_off, *Bp = ws + L.b_off, *SAp = ws + L.sa_off, *SBp = ws + L.sb_off;
+    const int Ks = (int)(K / 32);
+
+    // 1. staging
+    {
+        const int64_t tasks = L.Mp * (L.Kp / 16);
+        const int grid = (int)std::min<int64_t>(sbt_cdiv(tasks, 256), (int64_t)ctx->sm_count * 8);
+        k_mx_stage_a<<<grid, 256, 0, stream>>>((const uint8_t*)A, lda, (int)M, (int)K, Ap, (int)L.Kp, tasks);
+        sbt_status st = sbt_after_launch(ctx, "gemm_block_scaled (stage A, 8-bit)");
+        if (st) return st;
+        dim3 g2((unsigned)(L.Kp / 64), (unsigned)(L.Np / 32));
+        k_mx_stage_bt<<<g2, 128, 0, stream>>>((const uint8_t*)B, ldb, (int)K, (int)N, Bp, (int)L.Kp);
+        if ((st = sbt_after_launch(ctx, "gemm_block_scaled (stage B, 8-bit)"))) return st;
+        const int64_t ta = (L.Mp / 128) * L.k_blocks * 32, tb = L.n_tiles * L.k_blocks * 64;
+        const int g3 = (int)std::min<int64_t>(sbt_cdiv(ta + tb, 256), (int64_t)ctx->sm_count * 8);
+        k_mx_stage_scales<<<g3, 256, 0, stream>>>((const uint8_t*)SA, ld_sa, (const uint8_t*)SB, ld_sb, (int)M,
+                                                  (int)N, Ks, (int)L.k_blocks, SAp, ta, SBp, tb);
+        if ((st = sbt_after_launch(ctx, "gemm_block_scaled (stage scales)"))) return st;
+    }
+
+    // 2. block-scaled tensor-core kernel
+    CUtensorMap tmA, tmB, tmSA, tmSB;
+    sbt_status st = encode_u8(ctx, &tmA, Ap, L.Kp, L.Mp, MX_BK, 128, true);
+    if (st) return st;
+    if ((st = encode_u8(ctx, &tmB, Bp, L.Kp, L.Np, MX_BK, MX_BN / 2, true))) return st;
+    if ((st = encode_u8(ctx, &tmSA, SAp, 256, (L.Mp / 128) * L.k_blocks * 2, 256, 2, false))) return st;
+    if ((st = encode_u8(ctx, &tmSB, SBp, 256, L.n_tiles * L.k_blocks * 4, 256, 4, false))) return st;
+    MxParams p;
+    p.D = D;
+    p.ldd = ldd;
+    p.acc = acc;
+    p.ld_acc = ld_acc;
+    p.M = (int)M;
+    p.N = (int)N;
+    p.K = (int)K;
+    p.m_tiles = (int)L.m_tiles;
+    p.n_tiles = (int)L.n_tiles;
+    p.k_blocks = (int)L.k_blocks;
+    p.idesc = idesc_mx_e8m0((uint32_t)a_fmt, (uint32_t)b_fmt, 256, MX_BN, 0);
+    p.status = ctx->status;
+    p.wait_ns = ctx->wait_limit_ns;
+    p.withhold_first_load = ctx->test_hook == SBT_TEST_WITHHOLD_LOAD;
+    static bool attr_set[64] = {false};
+    static int max_clusters[64] = {0};
+    const int dev = ctx->device & 63;
+    if (!attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(k_gemm_mx_pair, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kMxSmem);
+        if (e != cudaSuccess) return sbt_cuda_check(e, "cudaFuncSetAttribute(gemm mx smem)");
+        attr_set[dev] = true;
+    }
+    if (!max_clusters[dev]) {
+        cudaLaunchConfig_t cfg = {};
+        cudaLaunchAttribute attr;
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = 2;
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.gridDim = dim3(2 * (unsigned)(ctx->sm_count / 2), 1, 1);
+        cfg.blockDim = dim3(kMxThreads, 1, 1);
+        cfg.dynamicSmemBytes = kMxSmem;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, k_gemm_mx_pair, &cfg) != cudaSuccess || n < 1) {
+            (void)cudaGetLastError();
+            n = ctx->sm_count / 2;
+        }
+        max_clusters[dev] = n;
+    }
+    const int tiles = p.m_tiles * p.n_tiles;
+    const int clusters = std::min(tiles, max_clusters[dev]);
+    k_gemm_mx_pair<<<2 * clusters, kMxThreads, kMxSmem, stream>>>(tmA, tmB, tmSA, tmSB, p);
+    return sbt_after_launch(ctx, "gemm_block_scaled (tcgen05 block-scaled, CTA pairs)");
+}

@@ -7,6 +7,8 @@
 
 #include <string>
 
+#include <algorithm>
+
 #include "sbt_internal.cuh"
 
 // Per-device status flag set by kernels whose bounded waits ran out.
@@ -350,7 +352,7 @@ static bool is_operand_format(sbt_lowp_format f) {
 sbt_status sbt_gemm_block_scaled_workspace_size(sbt_context* ctx, int64_t M, int64_t N, int64_t K, size_t* bytes) {
     SBT_REQUIRE(ctx && bytes, "NULL argument");
     SBT_REQUIRE(M >= 0 && N >= 0 && K >= 0, "gemm_block_scaled: negative extent");
-    *bytes = sbt_gemm_workspace_bytes(M, N, K);
+    *bytes = std::max(sbt_gemm_workspace_bytes(M, N, K), sbt_gemm_mx_workspace_bytes(M, N, K));
     return SBT_OK;
 }
 
@@ -376,7 +378,7 @@ sbt_status sbt_gemm_block_scaled(sbt_context* ctx, sbt_lowp_format a_fmt, const 
     if (M == 0 || N == 0) return SBT_OK;
     SBT_REQUIRE(D, "gemm_block_scaled: D is NULL");
     SBT_REQUIRE(K == 0 || (A && B && a_scale && b_scale), "gemm_block_scaled: NULL operand or scale");
-    const size_t need = sbt_gemm_workspace_bytes(M, N, K);
+    const size_t need = std::max(sbt_gemm_workspace_bytes(M, N, K), sbt_gemm_mx_workspace_bytes(M, N, K));
     if (need > 0) {
         if (!workspace || workspace_bytes < need)
             return sbt_fail(SBT_ERR_ALIGNMENT,

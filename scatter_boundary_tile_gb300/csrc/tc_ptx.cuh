@@ -264,4 +264,45 @@ __device__ __forceinline__ void tc_commit_pair_multicast(uint32_t bar, uint16_t 
         : "memory");
 }
 
+// ---------------------------------------------------------------- block-scaled MMA (kind::mxf8f6f4)
+
+// Shared-memory descriptor of a dense [rows][16 B] array without swizzle
+// (8-row core matrices 128 B apart), the source form of tcgen05.cp 32x128b.
+__device__ __forceinline__ uint64_t smem_desc_rows16(uint32_t saddr) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)(128u >> 4) << 16) | ((uint64_t)(128u >> 4) << 32) |
+           ((uint64_t)1u << 46);
+}
+
+// Copy 32 rows x 16 B of each pair CTA's own shared memory into its TMEM at
+// column `taddr` .. +3, row r to lane r of every 32-lane quarter.
+__device__ __forceinline__ void tc_cp_pair_32x128b_warpx4(uint32_t taddr, uint64_t src_desc) {
+    asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(src_desc) : "memory");
+}
+
+// D[tmem of both CTAs] (+)= (A .* SFA) * (B .* SFB)^T over one K = 32 step,
+// 8-bit operands, E8M0 scales from TMEM (one per row of A, one per column of B).
+__device__ __forceinline__ void tc_mma_mx_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                               uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptor, kind::mxf8f6f4 with E8M0 scales: operand formats
+// (0 = E4M3, 1 = E5M2), K-major A and B, fp32 accumulator, M x N; `sf_id`
+// selects the byte of each 32-bit scale column used by this K = 32 step.
+__host__ __device__ __forceinline__ uint32_t idesc_mx_e8m0(uint32_t a_fmt, uint32_t b_fmt, uint32_t m, uint32_t n,
+                                                            uint32_t sf_id) {
+    return (sf_id << 4)          // B scale byte
+           | (a_fmt << 7)        // A format
+           | (b_fmt << 10)       // B format
+           | ((n >> 3) << 17)    // N / 8
+           | (1u << 23)          // scales are E8M0
+           | ((m >> 4) << 24)    // M / 16
+           | (sf_id << 29);      // A scale byte
+}
+
 }  // namespace sbt_ptx

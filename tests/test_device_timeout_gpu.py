@@ -55,6 +55,26 @@ def test_gemm_wait_runs_out_then_recovers(ctx, mnk):
     assert np.linalg.norm(got - ref_b) / np.linalg.norm(ref) <= 1e-3
 
 
+def test_block_scaled_mma_wait_runs_out_then_recovers(ctx):
+    # E4M3 operands with E8M0 scales per 32: the tcgen05 block-scaled CTA-pair kernel
+    M, N, K = 600, 700, 256
+    g = wl.gemm_block_scaled(M=M, N=N, K=K, block=32, tag=22)
+    A, B, SA, SB = (dev(g[k]) for k in ("A", "B", "SA", "SB"))
+    D = torch.empty(M * g["ldd"] * 4, dtype=torch.uint8, device="cuda")
+    ws_n = sbt.gemm_block_scaled_workspace_size(ctx, M, N, K)
+    ws = torch.empty(ws_n, dtype=torch.uint8, device="cuda")
+    run = lambda: sbt.gemm_block_scaled(ctx, A, g["lda"], B, g["ldb"], SA, g["ld_sa"], SB, g["ld_sb"], g["Ks"], D,
+                                        g["ldd"], M, N, K, workspace=ws, workspace_bytes=ws_n)
+    expect_timeout(ctx, run)
+    run()
+    sync()
+    ctx.check_status()
+    got = host(D, np.float32, (M, g["ldd"]))[:, :N].astype(np.float64)
+    ref = oracle.gemm_block_scaled_f64(g["A"], g["lda"], g["SA"], g["ld_sa"], g["B"], g["ldb"], g["SB"], g["ld_sb"],
+                                       M, N, K, 32)
+    assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 1e-5
+
+
 def test_bulk_scatter_wait_runs_out_then_recovers(ctx):
     d = wl.scatter_rows_f32(dst_rows=20000, n_idx=5000, cols=256)
     rows, n = d["dst_rows"], d["idx"].size

@@ -80,6 +80,25 @@ def test_shapes_and_formats_vs_oracle(ctx, fmts, shape):
     check(run(ctx, g), g)
 
 
+MX_FORMATS = [("e4m3", "e4m3"), ("e5m2", "e5m2"), ("e4m3", "e5m2"), ("e5m2", "e4m3")]
+MX_SHAPES = [(1, 1, 32), (7, 9, 96), (65, 97, 160), (256, 224, 128), (257, 225, 256), (300, 449, 544),
+             (513, 448, 32)]
+
+
+@pytest.mark.parametrize("path", ["auto", "scalar"], ids=["block_scale_mma", "bf16_staging"])
+@pytest.mark.parametrize("fmts", MX_FORMATS, ids=lambda f: "x".join(f))
+@pytest.mark.parametrize("shape", MX_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_e8m0_block32_both_paths_vs_oracle(ctx, path, fmts, shape):
+    # E4M3/E5M2 with E8M0 scales per 32 along K: "auto" takes the
+    # tcgen05 kind::mxf8f6f4 kernel (256 x 224 tiles, 128-deep K blocks, so
+    # these shapes cut tiles and K blocks at every kind of edge), "scalar"
+    # forces the bf16 staging path; both must meet the same bounds.
+    M, N, K = shape
+    ctx.set_path(path)
+    g = wl.gemm_block_scaled(M=M, N=N, K=K, block=32, afmt=fmts[0], bfmt=fmts[1], sfmt="e8m0", tag=8)
+    check(run(ctx, g), g)
+
+
 def test_several_tiles_ragged_tail(ctx):
     # 3 x 3 tiles of 128 x 256 (or 2 x 3 CTA-pair tiles) with one-row / one-column tails, 32 K blocks
     g = wl.gemm_block_scaled(M=257, N=513, K=1024, block=32, tag=4)
