@@ -300,9 +300,16 @@ SBT_API sbt_status sbt_gemm_bounded(sbt_context* ctx, const void* A, int64_t lda
  * 2^119 with E4M3 operands; any E4M3 scale).  NaN codes propagate to the row
  * (A, a_scale) or column (B, b_scale) of D they feed.
  *
+ * Paths: with E4M3/E5M2 operands, E8M0 scales and K / K_s = 32 the call runs
+ * on the tensor cores' block scaling (tcgen05.mma kind::mxf8f6f4, 8-bit
+ * staging) under SBT_PATH_AUTO or SBT_PATH_TMA; every other combination, and
+ * any combination under SBT_PATH_SCALAR or SBT_PATH_VECTOR, stages the scaled
+ * operands as bf16 for the bf16 tensor-core kernel.  The two paths meet the
+ * same accuracy statement; they may differ in the order of the fp32 sums.
+ *
  * workspace: device scratch of at least sbt_gemm_block_scaled_workspace_size()
- * bytes, 256-byte aligned, owned by the caller (bf16 copies of the scaled
- * operands).
+ * bytes (enough for either path), 256-byte aligned, owned by the caller
+ * (re-laid-out copies of the operands and scales).
  */
 typedef enum { SBT_FMT_E4M3 = 0, SBT_FMT_E5M2 = 1, SBT_FMT_E8M0 = 2, SBT_FMT_E2M1 = 3 } sbt_lowp_format;
 SBT_API sbt_status sbt_gemm_block_scaled_workspace_size(sbt_context* ctx, int64_t M, int64_t N, int64_t K,
