@@ -53,6 +53,9 @@ def parse():
     return ap.parse_args()
 
 
+FP8_NOMINAL_TFLOPS = 4500.0  # dense fp8 tensor rate, nominal (no measured fp8 peak is available)
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -415,7 +418,8 @@ def run_ops(ctx, pk):
     except Exception as e:  # the GEMM may be unavailable in this build
         ops["gemm_bounded"] = {"unavailable": str(e).splitlines()[0][:200]}
 
-    # block-scaled GEMM: E4M3 operands, E8M0 scales over blocks of 32 along K, fp32 out
+    # block-scaled GEMM: E4M3 operands, E8M0 scales over blocks of 32 along K, fp32 out;
+    # "auto" runs the tcgen05 block-scaled kernel, "scalar" the bf16-staging path
     for (M, N, K) in [(8191, 8193, 4096)]:
         g = wl.gemm_block_scaled(M=M, N=N, K=K, block=32)
         A, B, SA, SB = (dev_bytes(g[k]) for k in ("A", "B", "SA", "SB"))
@@ -424,16 +428,20 @@ def run_ops(ctx, pk):
         ws = torch.empty(max(ws_n, 256), dtype=torch.uint8, device="cuda")
         fn = lambda: sbt.gemm_block_scaled(ctx, A, g["lda"], B, g["ldb"], SA, g["ld_sa"], SB, g["ld_sb"], g["Ks"],
                                            D, g["ldd"], M, N, K, workspace=ws, workspace_bytes=ws_n)
-        med, _, _ = time_launches(fn, 10)
         flops = 2.0 * M * N * K
-        tf = flops / med / 1e9
-        entry = {"ms": med, "TFLOP/s": tf, "frac_bf16": tf / pk["bf16_tflops"],
-                 "workload": "E4M3 x E4M3, E8M0 scales per 32 along K, fp32 D, no acc",
-                 "note": "whole call: scaled staging to bf16 + bf16 tensor-core kernel; fraction of the bf16 peak"}
-        split = kernel_split(fn, 5)
-        if split:
-            entry["kernels_ms"] = split
-        ops[f"gemm_block_scaled_{M}x{N}x{K}"] = entry
+        for path, note in [("auto", "whole call: 8-bit staging + tcgen05 kind::mxf8f6f4 block-scaled kernel"),
+                           ("scalar", "whole call: scaled operands staged as bf16 + the bf16 tcgen05 kernel")]:
+            ctx.set_path(path)
+            med, _, _ = time_launches(fn, 10)
+            tf = flops / med / 1e9
+            entry = {"ms": med, "TFLOP/s": tf, "frac_bf16": tf / pk["bf16_tflops"],
+                     "frac_fp8_nominal": tf / FP8_NOMINAL_TFLOPS,
+                     "workload": "E4M3 x E4M3, E8M0 scales per 32 along K, fp32 D, no acc", "note": note}
+            split = kernel_split(fn, 5)
+            if split:
+                entry["kernels_ms"] = split
+            ops[f"gemm_block_scaled_{M}x{N}x{K}" + ("" if path == "auto" else "_bf16_staging")] = entry
+        ctx.set_path("auto")
         del A, B, SA, SB, D, ws
     return ops
 
