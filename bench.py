@@ -325,9 +325,11 @@ def run_ops(ctx, pk):
     fn = lambda: sbt.gather_cols(ctx, ad, 2048, 100_003, 100_003, cid, 4096, outc, 4096, 2048, dtype="bf16")
     med, _, _ = time_launches(fn, 20)
     nbytes = 2 * 2048 * 4096 * 2 + 4096 * 4
+    sector_bytes = 2048 * 4096 * 32 + 2048 * 4096 * 2 + 4096 * 4  # one 32-byte sector per element read
     ops["gather_cols"] = {"workload": "bf16 2,048 x 100,003, 4,096 random columns gathered from every row",
                           "ms": med, "GB/s": nbytes / med / 1e6, "frac_hbm": nbytes / med / 1e6 / hbm,
-                          "algorithmic_bytes": nbytes,
+                          "algorithmic_bytes": nbytes, "sector_bytes": sector_bytes,
+                          "frac_hbm_sectors": sector_bytes / med / 1e6 / hbm,
                           "note": "each 2-byte element read costs a 32-byte sector: random columns are sector-bound"}
     del a, ad, cid, outc
 
