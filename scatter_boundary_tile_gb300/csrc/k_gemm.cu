@@ -81,6 +81,8 @@ __device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, 
 // Drain one 128 x BN accumulator from TMEM (this warp's 32-lane quarter `q`),
 // round (or keep fp32) and store rows row0.. of C through a padded shared
 // transpose so that each store instruction covers 32 consecutive columns.
+// A bf16 C is rounded before the transpose, which then moves half the bytes
+// (shared memory is the resource the main loop competes for).
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tmem_acc, int q, int lane, float* buf,
                                               int row0, int n0) {
     const int n_valid = min(BN, p.N - n0);
@@ -89,25 +91,40 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tmem
         uint32_t r[32];
         tmem_ld_32x32b_x32(tmem_acc + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
         tmem_ld_wait();
+        if (!p.c_f32) {
+            // [32 rows][17 words]: row `lane` packs its 32 columns as bf16 pairs; odd padding keeps
+            // the row-wise writes and the column-wise reads free of bank conflicts.
+            uint32_t* wb = reinterpret_cast<uint32_t*>(buf);
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+                wb[lane * 17 + j] = *reinterpret_cast<const uint32_t*>(&v);
+            }
+            __syncwarp();
+            const int col = n0 + c * 32 + lane;
+            if (col < p.N) {
+                uint16_t* Cp = reinterpret_cast<uint16_t*>(p.C);
+                for (int rr = 0; rr < 32 && row0 + rr < p.M; ++rr) {
+                    const uint32_t w = wb[rr * 17 + (lane >> 1)];
+                    Cp[(int64_t)(row0 + rr) * p.ldc + col] = (uint16_t)((lane & 1) ? (w >> 16) : (w & 0xFFFFu));
+                }
+            }
+            __syncwarp();
+            continue;
+        }
 #pragma unroll
         for (int j = 0; j < 32; ++j) buf[lane * 33 + j] = __uint_as_float(r[j]);
         __syncwarp();
         const int col = n0 + c * 32 + lane;
-        if (col < p.N) {
-            if (p.c_f32) {
-                float* Cp = reinterpret_cast<float*>(p.C);
-                if (p.acc) {
-                    for (int rr = 0; rr < 32 && row0 + rr < p.M; ++rr)
-                        Cp[(int64_t)(row0 + rr) * p.ldc + col] =
-                            buf[rr * 33 + lane] + __ldg(p.acc + (int64_t)(row0 + rr) * p.ld_acc + col);
-                } else {
-                    for (int rr = 0; rr < 32 && row0 + rr < p.M; ++rr)
-                        Cp[(int64_t)(row0 + rr) * p.ldc + col] = buf[rr * 33 + lane];
-                }
-            } else {
-                __nv_bfloat16* Cp = reinterpret_cast<__nv_bfloat16*>(p.C);
+        if (col < p.N) {  // fp32 C
+            float* Cp = reinterpret_cast<float*>(p.C);
+            if (p.acc) {
                 for (int rr = 0; rr < 32 && row0 + rr < p.M; ++rr)
-                    Cp[(int64_t)(row0 + rr) * p.ldc + col] = __float2bfloat16_rn(buf[rr * 33 + lane]);
+                    Cp[(int64_t)(row0 + rr) * p.ldc + col] =
+                        buf[rr * 33 + lane] + __ldg(p.acc + (int64_t)(row0 + rr) * p.ld_acc + col);
+            } else {
+                for (int rr = 0; rr < 32 && row0 + rr < p.M; ++rr)
+                    Cp[(int64_t)(row0 + rr) * p.ldc + col] = buf[rr * 33 + lane];
             }
         }
         __syncwarp();
