@@ -36,6 +36,26 @@ def test_unique_rows_fp32(ctx, n_idx):
         assert np.array_equal(got.view(np.uint32), want.view(np.uint32)), path
 
 
+@pytest.mark.parametrize("tile_c,dtype", [(4096, "f32"), (3000, "f32"), (8192, "bf16")])
+def test_wide_rows_one_row_per_chunk(ctx, tile_c, dtype):
+    # Rows of up to 16 KiB plus a 4 KiB mask: the bulk ring holds one row per stage.
+    rows, n = 70, 23
+    idx = synth.permutation_prefix(311, rows, n).astype(np.int32)
+    if dtype == "f32":
+        src = synth.uniform_f32(312, (n, tile_c), -1.0, 1.0)
+        dst = np.full((rows, tile_c), wl.F32_CANARY_BITS, np.uint32).view(np.float32)
+    else:
+        src = synth.normal_bf16(312, (n, tile_c))
+        dst = np.full((rows, tile_c), 0xDEAD, np.uint16)
+    mask = synth.bernoulli_u8(313, (n, tile_c), 0.9)
+    want = oracle.scatter_rows_masked(dst.copy(), rows, tile_c, tile_c, idx, src, tile_c, tile_c, mask=mask,
+                                      ld_mask=tile_c)
+    for path in ("auto", "tma", "vector"):
+        got = gpu_scatter(ctx, dst, rows, tile_c, tile_c, idx, src, tile_c, tile_c, dtype, mask=mask, ld_mask=tile_c,
+                          path=path)
+        assert np.array_equal(got.view(np.uint8), want.view(np.uint8)), path
+
+
 CASES = [
     # rows, cols, ld_dst, tile_c, ld_src, col_offset, row_offset, ld_mask (0 = no mask)
     (300, 64, 64, 64, 64, 0, 0, 64),
