@@ -322,13 +322,21 @@ __global__ void __launch_bounds__(256) k_mx_stage_a(const uint8_t* __restrict__ 
 }
 
 // B8^T [Np][Kp] <- transpose of B [K][N] (row stride ldb bytes), zero past K or N.
-// 64 (k) x 32 (n) tiles through shared memory, 128 threads.
-__global__ void __launch_bounds__(128) k_mx_stage_bt(const uint8_t* __restrict__ B, int64_t ldb, int K, int N,
-                                                     uint8_t* __restrict__ Bp, int Kp) {
-    __shared__ uint8_t t[64][36];
-    const int k0 = blockIdx.x * 64, n0 = blockIdx.y * 32;
-    {
-        const int kk = threadIdx.x >> 1, nh = (threadIdx.x & 1) * 16;
+// 64 (k) x 224 (n) tiles (a whole N tile of the main kernel, so each B row
+// piece read is 224 bytes long), 224 threads.  Loads: four 16-byte row pieces
+// per thread into shared words; stores: each thread reads a 16 (k) x 4 (n)
+// block as sixteen words, transposes its four 4 x 4 byte blocks with byte
+// permutes and writes four 16-byte vectors (one per n row).
+constexpr int kBtK = 64, kBtN = MX_BN, kBtThreads = (kBtN / 4) * (kBtK / 16), kBtPitch = kBtN / 4 + 1;
+static_assert(kBtK * kBtN / 16 % kBtThreads == 0, "load split");
+__global__ void __launch_bounds__(kBtThreads) k_mx_stage_bt(const uint8_t* __restrict__ B, int64_t ldb, int K, int N,
+                                                            uint8_t* __restrict__ Bp, int Kp) {
+    __shared__ uint32_t t[kBtK][kBtPitch];
+    const int k0 = blockIdx.x * kBtK, n0 = blockIdx.y * kBtN;
+#pragma unroll
+    for (int i = 0; i < kBtK * kBtN / 16 / kBtThreads; ++i) {
+        const int v = i * kBtThreads + threadIdx.x;
+        const int kk = v / (kBtN / 16), nh = (v % (kBtN / 16)) * 16;
         const int k = k0 + kk, n = n0 + nh;
         uint64_t lo = 0, hi = 0;
         if (k < K && n < N) {
@@ -344,17 +352,30 @@ __global__ void __launch_bounds__(128) k_mx_stage_bt(const uint8_t* __restrict__
                 }
             }
         }
-#pragma unroll
-        for (int e = 0; e < 16; ++e) t[kk][nh + e] = (uint8_t)((e < 8 ? lo >> (8 * e) : hi >> (8 * (e - 8))) & 255u);
+        uint32_t* w = &t[kk][nh >> 2];
+        w[0] = (uint32_t)lo;
+        w[1] = (uint32_t)(lo >> 32);
+        w[2] = (uint32_t)hi;
+        w[3] = (uint32_t)(hi >> 32);
     }
     __syncthreads();
-    {
-        const int nn = threadIdx.x >> 2, kv = (threadIdx.x & 3) * 16;
-        uint32_t w[4] = {0, 0, 0, 0};
+    const int nw = threadIdx.x % (kBtN / 4), kv = (threadIdx.x / (kBtN / 4)) * 16;  // n = 4 nw .. + 3, k = kv .. + 15
+    if (k0 + kv >= Kp) return;
+    uint32_t out[4][4];  // out[j][g]: bytes k = kv + 4 g .. + 3 of row n = 4 nw + j
 #pragma unroll
-        for (int e = 0; e < 16; ++e) w[e >> 2] |= (uint32_t)t[kv + e][nn] << (8 * (e & 3));
-        sbt_st_v4(Bp + (int64_t)(n0 + nn) * Kp + k0 + kv, make_uint4(w[0], w[1], w[2], w[3]));
+    for (int g = 0; g < 4; ++g) {
+        const uint32_t w0 = t[kv + 4 * g][nw], w1 = t[kv + 4 * g + 1][nw];
+        const uint32_t w2 = t[kv + 4 * g + 2][nw], w3 = t[kv + 4 * g + 3][nw];
+        const uint32_t a0 = __byte_perm(w0, w1, 0x5140), a1 = __byte_perm(w0, w1, 0x7362);
+        const uint32_t a2 = __byte_perm(w2, w3, 0x5140), a3 = __byte_perm(w2, w3, 0x7362);
+        out[0][g] = __byte_perm(a0, a2, 0x5410);
+        out[1][g] = __byte_perm(a0, a2, 0x7632);
+        out[2][g] = __byte_perm(a1, a3, 0x5410);
+        out[3][g] = __byte_perm(a1, a3, 0x7632);
     }
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        sbt_st_v4(Bp + (int64_t)(n0 + 4 * nw + j) * Kp + k0 + kv, make_uint4(out[j][0], out[j][1], out[j][2], out[j][3]));
 }
 
 // Scale chunks.  SA8: chunk (g, kb) of 512 B for rows 128 g .. 128 g + 127 and
@@ -465,7 +486,7 @@ sbt_status sbt_launch_gemm_mx(sbt_context* ctx, int a_fmt, const void* A, int64_
                               const float* acc, int64_t ld_acc, float* D, int64_t ldd, int64_t M, int64_t N,
                               int64_t K, void* workspace, cudaStream_t stream) {
     const MxLayout L = mx_layout(M, N, K);
-    if (L.Np / 32 > 65535 || L.Kp / 64 > INT32_MAX)
+    if (L.Np / kBtN > 65535 || L.Kp / 64 > INT32_MAX)
         return sbt_fail(SBT_ERR_INVALID_ARG, "gemm_block_scaled: N too large for the staging grid");
     uint8_t* ws = (uint8_t*)workspace;
     uint8_t *Ap = ws + L.a_off, *Bp = ws + L.b_off, *SAp = ws + L.sa_off, *SBp = ws + L.sb_off;
@@ -478,8 +499,8 @@ sbt_status sbt_launch_gemm_mx(sbt_context* ctx, int a_fmt, const void* A, int64_
         k_mx_stage_a<<<grid, 256, 0, stream>>>((const uint8_t*)A, lda, (int)M, (int)K, Ap, (int)L.Kp, tasks);
         sbt_status st = sbt_after_launch(ctx, "gemm_block_scaled (stage A, 8-bit)");
         if (st) return st;
-        dim3 g2((unsigned)(L.Kp / 64), (unsigned)(L.Np / 32));
-        k_mx_stage_bt<<<g2, 128, 0, stream>>>((const uint8_t*)B, ldb, (int)K, (int)N, Bp, (int)L.Kp);
+        dim3 g2((unsigned)sbt_cdiv(L.Kp, kBtK), (unsigned)(L.Np / kBtN));
+        k_mx_stage_bt<<<g2, kBtThreads, 0, stream>>>((const uint8_t*)B, ldb, (int)K, (int)N, Bp, (int)L.Kp);
         if ((st = sbt_after_launch(ctx, "gemm_block_scaled (stage B, 8-bit)"))) return st;
         const int64_t ta = (L.Mp / 128) * L.k_blocks * 32, tb = L.n_tiles * L.k_blocks * 64;
         const int g3 = (int)std::min<int64_t>(sbt_cdiv(ta + tb, 256), (int64_t)ctx->sm_count * 8);
