@@ -8,8 +8,9 @@
 // Pipeline (all on the caller's stream):
 //  1. Staging (the bounded copy of Tylo.jl "Boundary tiles"): A -> A8 [Mp][Kp]
 //     and B -> B8^T [Np][Kp], 8-bit codes, K-major, zero past M, N, K; the
-//     scales are packed per (row tile, 128-deep K block) into 512-byte chunks
-//     in the order the tensor memory wants them (below), 2^0 past the extents.
+//     scales are packed per (row or column tile, 128-deep K block) into
+//     chunks in the order the tensor memory wants them (below), 2^0 past the
+//     extents.
 //  2. A persistent kernel on clusters of two CTAs (M = 256 per pair, N = 224
 //     per tile, 128 K per stage): warp 0 of each CTA TMA-loads its 128 rows of
 //     A8, its 112 rows of B8^T and the stage's scale chunks into a 5-stage
@@ -23,15 +24,20 @@
 // scale of row m (of this CTA's 128 rows of A) for step s sits in lane m,
 // column sfa + m / 32, byte s; that of column n of B (all 224 columns, in
 // both CTAs) in lanes n % 32 + 32 q of every quarter q, column sfb + n / 32,
-// byte s.  tcgen05.cp 32x128b.warpx4 writes row r of a [32][16-byte] chunk to
-// lane r of every quarter, so a chunk holds at byte 16 r + 4 j + s the scale
-// of row (or column) 32 j + r, step s.
+// byte s.  Scale addresses must be multiples of 4 columns.  A's scales come
+// with one tcgen05.cp 32x128b.warpx4 (row r of a [32][16-byte] chunk to lane
+// r of every quarter: byte 16 r + 4 j + s = scale of row 32 j + r, step s);
+// B's with one tcgen05.cp 128x256b from a 4 KB chunk that repeats the same
+// 32 rows for the four quarters.  Each copy costs about the same in the MMA
+// stream whatever its size (three 512-byte copies per stage cost ~57 us of
+// the 8191 x 8193 x 4096 call, two copies ~39 us), so B's eight columns take
+// one larger copy.
 //
 // TMEM: two 224-column fp32 accumulators (the epilogue of one tile overlaps
 // the main loop of the next) and five 12-column scale slots, one per stage,
-// fill all 512 columns.  A slot is rewritten only after the stage's previous
-// MMAs completed: its new data arrives after the producer saw the stage's
-// empty barrier, which those MMAs' commit signals.
+// fill 508 of the 512 columns.  A slot is rewritten only after the stage's
+// previous MMAs completed: its new data arrives after the producer saw the
+// stage's empty barrier, which those MMAs' commit signals.
 #include <algorithm>
 #include <string>
 
@@ -48,14 +54,14 @@ constexpr int kMxStages = 5;
 constexpr int kMxThreads = 192;  // warp 0: TMA, warp 1: MMA, warps 2..5: epilogue
 constexpr uint32_t kMxABytes = 128 * MX_BK;
 constexpr uint32_t kMxBBytes = (MX_BN / 2) * MX_BK;
-constexpr uint32_t kMxSfaOff = kMxABytes + kMxBBytes;  // 30720
-constexpr uint32_t kMxSfbOff = kMxSfaOff + 512;
-constexpr uint32_t kMxTxBytes = kMxSfbOff + 1024;      // bytes one CTA receives per stage
-constexpr uint32_t kMxStageBytes = 32768;              // keeps every stage's A tile 1024-aligned
+constexpr uint32_t kMxSfbOff = kMxABytes + kMxBBytes;  // 30720: B scales of the stage's K block (4 KB)
+constexpr uint32_t kMxSfaOff = kMxSfbOff + 4096;       // A scales of the stage's K block (512 B)
+constexpr uint32_t kMxTxBytes = kMxSfaOff + 512;       // bytes one CTA receives per stage
+constexpr uint32_t kMxStageBytes = 35840;              // keeps every stage's A tile 1024-aligned
 constexpr uint32_t kMxSfCol0 = 2 * MX_BN;              // scale slots after the two accumulators
 constexpr uint32_t kMxSfCols = 12;                      // 4 columns of A scales + 8 of B scales
 static_assert(kMxSfCol0 + kMxStages * kMxSfCols <= 512, "TMEM columns");
-static_assert(kMxTxBytes <= kMxStageBytes, "stage layout");
+static_assert(kMxTxBytes <= kMxStageBytes && kMxStageBytes % 1024 == 0, "stage layout");
 constexpr int kMxEpiWarps = 4;
 constexpr int kMxEpiWords = 32 * 33;
 constexpr int kMxNumBars = 2 * kMxStages + 5;
@@ -190,10 +196,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
                         tma_load_2d_pair(sa, &tmA, kb * MX_BK, mt * 256 + (int)rank * 128, leader_full);
                         tma_load_2d_pair(sa + kMxABytes, &tmB, kb * MX_BK, nt * MX_BN + (int)rank * (MX_BN / 2),
                                          leader_full);
-                        // scale chunks: [row group][K block] x 512 B as rows of 256 B; B: [tile][K block] x 1 KB
+                        // scale chunks viewed as rows of 256 B: B 4 KB per (tile, K block), A 512 B per
+                        // (128-row group, K block)
+                        tma_load_2d_pair(sa + kMxSfbOff, &tmSB, 0, (nt * p.k_blocks + kb) * 16, leader_full);
                         tma_load_2d_pair(sa + kMxSfaOff, &tmSA, 0, ((mt * 2 + (int)rank) * p.k_blocks + kb) * 2,
                                          leader_full);
-                        tma_load_2d_pair(sa + kMxSfbOff, &tmSB, 0, (nt * p.k_blocks + kb) * 4, leader_full);
                     }
                     if (++stage == kMxStages) {
                         stage = 0;
@@ -228,8 +235,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
                     const uint32_t sfa = tmem_base + kMxSfCol0 + kMxSfCols * (uint32_t)stage;
                     const uint32_t sfb = sfa + 4;
                     tc_cp_pair_32x128b_warpx4(sfa, smem_desc_rows16(sa + kMxSfaOff));
-                    tc_cp_pair_32x128b_warpx4(sfb, smem_desc_rows16(sa + kMxSfbOff));
-                    tc_cp_pair_32x128b_warpx4(sfb + 4, smem_desc_rows16(sa + kMxSfbOff + 512));
+                    tc_cp_pair_128x256b(sfb, smem_desc_rows32(sa + kMxSfbOff));
                     const int k_rem = p.K - kb * MX_BK;
                     const int k_steps = k_rem >= MX_BK ? MX_BK / 32 : (k_rem + 31) / 32;
                     for (int ks = 0; ks < k_steps; ++ks)
@@ -378,11 +384,17 @@ __global__ void __launch_bounds__(kBtThreads) k_mx_stage_bt(const uint8_t* __res
         sbt_st_v4(Bp + (int64_t)(n0 + 4 * nw + j) * Kp + k0 + kv, make_uint4(out[j][0], out[j][1], out[j][2], out[j][3]));
 }
 
-// Scale chunks.  SA8: chunk (g, kb) of 512 B for rows 128 g .. 128 g + 127 and
-// steps 4 kb .. 4 kb + 3; SB8: chunk (t, kb) of 1 KB = two 512-B halves for
-// columns 224 t + 128 h + (0..127).  Byte 16 r + 4 j + s of a 512-B part is
-// the scale of row / column 32 j + r of the part, step s; 127 (= 2^0) past
-// the extents (those operand codes are zero).  One 16-byte row r per task.
+// Scale chunks.
+//  SA8 chunk (g, kb), 512 B in the source form of tcgen05.cp 32x128b.warpx4
+//    (row r of [32][16 B] goes to lane r of every lane quarter): byte
+//    16 r + 4 j + s is the scale of A row 128 g + 32 j + r, step s (lane
+//    quarter q reads column sfa + q, so quarter q finds its rows in column j = q).
+//  SB8 chunk (t, kb), 4 KB in the source form of tcgen05.cp 128x256b (row r to
+//    lane r, 8 columns of 4 step bytes; byte b of row r at (r / 8) * 256 +
+//    (b / 16) * 128 + (r % 8) * 16 + b % 16): every lane quarter alike, row
+//    32 q + i column c holding the scales of B column 224 t + 32 c + i.
+// 127 (= 2^0) past the extents: those operand codes are zero.  One 16-byte
+// store per task.
 __global__ void __launch_bounds__(256) k_mx_stage_scales(const uint8_t* __restrict__ SA, int64_t ld_sa,
                                                          const uint8_t* __restrict__ SB, int64_t ld_sb, int M, int N,
                                                          int Ks, int k_blocks, uint8_t* __restrict__ SAp,
@@ -401,34 +413,34 @@ __global__ void __launch_bounds__(256) k_mx_stage_scales(const uint8_t* __restri
                 const int64_t m = 128 * g + 32 * j + r;
                 uint32_t v = 0;
 #pragma unroll
-                for (int s = 0; s < 4; ++s) {
-                    const int ks = 4 * kb + s;
-                    const uint32_t c = (m < M && ks < Ks) ? (uint32_t)__ldg(SA + m * ld_sa + ks) : 127u;
-                    v |= c << (8 * s);
+                for (int st = 0; st < 4; ++st) {
+                    const int ks = 4 * kb + st;
+                    v |= ((m < M && ks < Ks) ? (uint32_t)__ldg(SA + m * ld_sa + ks) : 127u) << (8 * st);
                 }
                 w[j] = v;
             }
             dst = SAp + t * 16;
         } else {
             const int64_t u = t - tasks_a;
-            const int r = (int)(u & 31);
-            const int h = (int)((u >> 5) & 1);
-            const int64_t chunk = u >> 6;
+            const int unit = (int)(u & 255);               // 16-byte unit within the 4 KB chunk
+            const int64_t chunk = u >> 8;
+            const int r = (unit >> 4) * 8 + (unit & 7);    // row (lane)
+            const int c0 = ((unit >> 3) & 1) * 4;          // first of the unit's 4 columns
+            const int i = r & 31;
             const int64_t tile = chunk / k_blocks;
             const int kb = (int)(chunk - tile * k_blocks);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int within = 128 * h + 32 * j + r;
+            for (int e = 0; e < 4; ++e) {
+                const int within = 32 * (c0 + e) + i;
                 const int64_t n = tile * MX_BN + within;
                 uint32_t v = 0;
 #pragma unroll
-                for (int s = 0; s < 4; ++s) {
-                    const int ks = 4 * kb + s;
-                    const uint32_t c =
-                        (within < MX_BN && n < N && ks < Ks) ? (uint32_t)__ldg(SB + (int64_t)ks * ld_sb + n) : 127u;
-                    v |= c << (8 * s);
+                for (int st = 0; st < 4; ++st) {
+                    const int ks = 4 * kb + st;
+                    const bool in = within < MX_BN && n < N && ks < Ks;
+                    v |= (in ? (uint32_t)__ldg(SB + (int64_t)ks * ld_sb + n) : 127u) << (8 * st);
                 }
-                w[j] = v;
+                w[e] = v;
             }
             dst = SBp + u * 16;
         }
@@ -455,7 +467,7 @@ MxLayout mx_layout(int64_t M, int64_t N, int64_t K) {
     L.b_off = round256((size_t)L.Mp * L.Kp);
     L.sa_off = L.b_off + round256((size_t)L.Np * L.Kp);
     L.sb_off = L.sa_off + round256((size_t)(L.Mp / 128) * L.k_blocks * 512);
-    L.total = L.sb_off + round256((size_t)L.n_tiles * L.k_blocks * 1024);
+    L.total = L.sb_off + round256((size_t)L.n_tiles * L.k_blocks * 4096);
     return L;
 }
 
@@ -502,7 +514,7 @@ sbt_status sbt_launch_gemm_mx(sbt_context* ctx, int a_fmt, const void* A, int64_
         dim3 g2((unsigned)sbt_cdiv(L.Kp, kBtK), (unsigned)(L.Np / kBtN));
         k_mx_stage_bt<<<g2, kBtThreads, 0, stream>>>((const uint8_t*)B, ldb, (int)K, (int)N, Bp, (int)L.Kp);
         if ((st = sbt_after_launch(ctx, "gemm_block_scaled (stage B, 8-bit)"))) return st;
-        const int64_t ta = (L.Mp / 128) * L.k_blocks * 32, tb = L.n_tiles * L.k_blocks * 64;
+        const int64_t ta = (L.Mp / 128) * L.k_blocks * 32, tb = L.n_tiles * L.k_blocks * 256;
         const int g3 = (int)std::min<int64_t>(sbt_cdiv(ta + tb, 256), (int64_t)ctx->sm_count * 8);
         k_mx_stage_scales<<<g3, 256, 0, stream>>>((const uint8_t*)SA, ld_sa, (const uint8_t*)SB, ld_sb, (int)M,
                                                   (int)N, Ks, (int)L.k_blocks, SAp, ta, SBp, tb);
@@ -515,7 +527,7 @@ sbt_status sbt_launch_gemm_mx(sbt_context* ctx, int a_fmt, const void* A, int64_
     if (st) return st;
     if ((st = encode_u8(ctx, &tmB, Bp, L.Kp, L.Np, MX_BK, MX_BN / 2, true))) return st;
     if ((st = encode_u8(ctx, &tmSA, SAp, 256, (L.Mp / 128) * L.k_blocks * 2, 256, 2, false))) return st;
-    if ((st = encode_u8(ctx, &tmSB, SBp, 256, L.n_tiles * L.k_blocks * 4, 256, 4, false))) return st;
+    if ((st = encode_u8(ctx, &tmSB, SBp, 256, L.n_tiles * L.k_blocks * 16, 256, 16, false))) return st;
     MxParams p;
     p.D = D;
     p.ldd = ldd;

@@ -279,6 +279,21 @@ __device__ __forceinline__ void tc_cp_pair_32x128b_warpx4(uint32_t taddr, uint64
     asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(src_desc) : "memory");
 }
 
+// Shared-memory descriptor of a [128 rows][32 B] source without swizzle, as
+// 8-row x 16-byte core matrices: byte b of row r at (r / 8) * 256 +
+// (b / 16) * 128 + (r % 8) * 16 + b % 16 (the two 16-byte halves of a row
+// 128 B apart, 8-row groups 256 B apart).
+__device__ __forceinline__ uint64_t smem_desc_rows32(uint32_t saddr) {
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)(128u >> 4) << 16) | ((uint64_t)(256u >> 4) << 32) |
+           ((uint64_t)1u << 46);
+}
+
+// Copy 128 rows x 32 B of each pair CTA's own shared memory into its TMEM:
+// row r to lane r, bytes 4c .. 4c + 3 to column taddr + c (c = 0..7).
+__device__ __forceinline__ void tc_cp_pair_128x256b(uint32_t taddr, uint64_t src_desc) {
+    asm volatile("tcgen05.cp.cta_group::2.128x256b [%0], %1;" ::"r"(taddr), "l"(src_desc) : "memory");
+}
+
 // D[tmem of both CTAs] (+)= (A .* SFA) * (B .* SFB)^T over one K = 32 step,
 // 8-bit operands, E8M0 scales from TMEM (one per row of A, one per column of B).
 __device__ __forceinline__ void tc_mma_mx_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
