@@ -173,6 +173,12 @@ __device__ __forceinline__ uint4 sbt_ld_nc_v4_l1(const void* p) {
     return v;
 }
 
+// Streaming (evict-first) 16-byte store, for outputs this kernel never reads back.
+__device__ __forceinline__ void sbt_st_v4_cs(void* p, uint4 v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
+                 : "memory");
+}
+
 __device__ __forceinline__ void sbt_st_v4(void* p, uint4 v) {
     asm volatile("st.global.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
                  : "memory");
