@@ -445,6 +445,21 @@ def run_ops(ctx, pk):
             ops[f"gemm_block_scaled_{M}x{N}x{K}" + ("" if path == "auto" else "_bf16_staging")] = entry
         ctx.set_path("auto")
         del A, B, SA, SB, D, ws
+        # MXFP4: E2M1 operands (two per byte), E8M0 scales per 32, on the tensor path
+        g = wl.gemm_block_scaled(M=M, N=N, K=K, block=32, afmt="e2m1", bfmt="e2m1")
+        A, B, SA, SB = (dev_bytes(g[k]) for k in ("A", "B", "SA", "SB"))
+        D = torch.empty(M * g["ldd"] * 4, dtype=torch.uint8, device="cuda")
+        ws = torch.empty(max(ws_n, 256), dtype=torch.uint8, device="cuda")
+        fn = lambda: sbt.gemm_block_scaled(ctx, A, g["lda"], B, g["ldb"], SA, g["ld_sa"], SB, g["ld_sb"], g["Ks"],
+                                           D, g["ldd"], M, N, K, workspace=ws, workspace_bytes=ws_n,
+                                           a_fmt="e2m1", b_fmt="e2m1")
+        med, _, _ = time_launches(fn, 10)
+        tf = flops / med / 1e9
+        ops[f"gemm_block_scaled_{M}x{N}x{K}_e2m1"] = {
+            "ms": med, "TFLOP/s": tf, "frac_bf16": tf / pk["bf16_tflops"], "frac_fp8_nominal": tf / FP8_NOMINAL_TFLOPS,
+            "workload": "E2M1 x E2M1 (packed), E8M0 scales per 32 along K, fp32 D, no acc",
+            "note": "whole call: staging to the 16-code + 8-byte-pad pieces kind::mxf8f6f4 reads, tcgen05 block-scaled kernel"}
+        del A, B, SA, SB, D, ws
     return ops
 
 

@@ -300,8 +300,8 @@ SBT_API sbt_status sbt_gemm_bounded(sbt_context* ctx, const void* A, int64_t lda
  * 2^119 with E4M3 operands; any E4M3 scale).  NaN codes propagate to the row
  * (A, a_scale) or column (B, b_scale) of D they feed.
  *
- * Paths: with E4M3/E5M2 operands, E8M0 scales and K / K_s = 32 the call runs
- * on the tensor cores' block scaling (tcgen05.mma kind::mxf8f6f4, 8-bit
+ * Paths: with E4M3/E5M2/E2M1 operands, E8M0 scales and K / K_s = 32 the call
+ * runs on the tensor cores' block scaling (tcgen05.mma kind::mxf8f6f4, 8-bit
  * staging) under SBT_PATH_AUTO or SBT_PATH_TMA; every other combination, and
  * any combination under SBT_PATH_SCALAR or SBT_PATH_VECTOR, stages the scaled
  * operands as bf16 for the bf16 tensor-core kernel.  The two paths meet the

@@ -1,7 +1,7 @@
 // Block-scaled GEMM on the tensor cores' own block scaling.
 //
-// cuTile.jl "Operations", muladd_scaled with E4M3 / E5M2 operands and E8M0
-// scales over blocks of 32 along K: exactly the microscaling form that
+// cuTile.jl "Operations", muladd_scaled with E4M3 / E5M2 / E2M1 operands and
+// E8M0 scales over blocks of 32 along K: exactly the microscaling form that
 // tcgen05.mma.kind::mxf8f6f4.block_scale computes, one scale per row of A and
 // per column of B for each K = 32 step, fp32 accumulation in TMEM.
 //
@@ -49,6 +49,10 @@ namespace {
 using namespace sbt_ptx;
 
 constexpr int MX_BN = 224;   // columns per tile
+constexpr int kMxFmtE4M3 = 0, kMxFmtE5M2 = 1, kMxFmtE2M1 = 3;  // sbt_lowp_format codes
+
+// Operand type field of the kind::mxf8f6f4 instruction descriptor.
+uint32_t mma_format(int fmt) { return fmt == kMxFmtE2M1 ? 5u : (uint32_t)fmt; }
 constexpr int MX_BK = 128;   // K per stage (bytes of one 128-byte swizzle row)
 constexpr int kMxStages = 5;
 constexpr int kMxThreads = 192;  // warp 0: TMA, warp 1: MMA, warps 2..5: epilogue
@@ -302,7 +306,58 @@ __device__ __forceinline__ uint64_t load8_any(const uint8_t* p) {
     return (lo >> sh) | (__ldg(w + 1) << (64 - sh));
 }
 
-// A8 [Mp][Kp] <- A [M][K] (row stride lda bytes), zero past M or K; 16 bytes per task.
+// E2M1 operands: kind::mxf8f6f4 reads a 4-bit type from each 16-byte piece of
+// a K-major row as 16 packed codes in the first 8 bytes (even element in the
+// low nibble, as in the caller's arrays) followed by 8 bytes of padding.
+// (Found by running one-K-block products with the codes one per byte: the
+// results matched this reading exactly and no other.)
+
+// Eight 4-bit codes (code i in bits 4i..4i+3) spread to one code per byte.
+__device__ __forceinline__ uint64_t spread_nibbles(uint32_t x) {
+    uint64_t v = x;
+    v = (v | (v << 16)) & 0x0000FFFF0000FFFFull;
+    v = (v | (v << 8)) & 0x00FF00FF00FF00FFull;
+    v = (v | (v << 4)) & 0x0F0F0F0F0F0F0F0Full;
+    return v;
+}
+
+// The inverse: eight bytes holding one code each (low nibble) packed into 32 bits.
+__device__ __forceinline__ uint32_t pack_nibbles(uint64_t v) {
+    v = (v | (v >> 4)) & 0x00FF00FF00FF00FFull;
+    v = (v | (v >> 8)) & 0x0000FFFF0000FFFFull;
+    v = (v | (v >> 16)) & 0x00000000FFFFFFFFull;
+    return (uint32_t)v;
+}
+
+// Sixteen codes of a row starting at element e0 (a multiple of 16), one per
+// byte: bytes of an 8-bit format, or the nibbles of packed E2M1 (two per
+// byte, even element low); `avail` codes are inside the row, the rest zero.
+template <bool P4>
+__device__ __forceinline__ void load16_codes(const uint8_t* row, int e0, int avail, uint64_t* lo, uint64_t* hi) {
+    *lo = 0;
+    *hi = 0;
+    if (avail >= 16) {
+        if (P4) {
+            const uint64_t c = load8_any(row + e0 / 2);
+            *lo = spread_nibbles((uint32_t)c);
+            *hi = spread_nibbles((uint32_t)(c >> 32));
+        } else {
+            *lo = load8_any(row + e0);
+            *hi = load8_any(row + e0 + 8);
+        }
+        return;
+    }
+    for (int e = 0; e < 16 && e < avail; ++e) {
+        uint64_t b;
+        if (P4) b = (uint64_t)((__ldg(row + (e0 + e) / 2) >> (4 * ((e0 + e) & 1))) & 15u);
+        else b = __ldg(row + e0 + e);
+        if (e < 8) *lo |= b << (8 * e);
+        else *hi |= b << (8 * (e - 8));
+    }
+}
+
+// A8 [Mp][Kp] <- A [M][K] (row stride lda elements), zero past M or K; 16 codes per task.
+template <bool P4>
 __global__ void __launch_bounds__(256) k_mx_stage_a(const uint8_t* __restrict__ A, int64_t lda, int M, int K,
                                                     uint8_t* __restrict__ Ap, int Kp, int64_t tasks) {
     const int kv = Kp / 16;
@@ -310,18 +365,10 @@ __global__ void __launch_bounds__(256) k_mx_stage_a(const uint8_t* __restrict__ 
         const int64_t m = t / kv;
         const int k0 = (int)(t - m * kv) * 16;
         uint64_t lo = 0, hi = 0;
-        if (m < M && k0 < K) {
-            const uint8_t* row = A + m * lda;
-            if (k0 + 16 <= K) {
-                lo = load8_any(row + k0);
-                hi = load8_any(row + k0 + 8);
-            } else {
-                for (int e = 0; e < 16 && k0 + e < K; ++e) {
-                    const uint64_t b = __ldg(row + k0 + e);
-                    if (e < 8) lo |= b << (8 * e);
-                    else hi |= b << (8 * (e - 8));
-                }
-            }
+        if (m < M && k0 < K) load16_codes<P4>(A + (P4 ? m * lda / 2 : m * lda), k0, K - k0, &lo, &hi);
+        if (P4) {  // 16 packed codes, then 8 bytes of padding
+            lo = (uint64_t)pack_nibbles(lo) | ((uint64_t)pack_nibbles(hi) << 32);
+            hi = 0;
         }
         sbt_st_v4(Ap + m * Kp + k0, make_uint4((uint32_t)lo, (uint32_t)(lo >> 32), (uint32_t)hi, (uint32_t)(hi >> 32)));
     }
@@ -335,6 +382,7 @@ __global__ void __launch_bounds__(256) k_mx_stage_a(const uint8_t* __restrict__ 
 // permutes and writes four 16-byte vectors (one per n row).
 constexpr int kBtK = 64, kBtN = MX_BN, kBtThreads = (kBtN / 4) * (kBtK / 16), kBtPitch = kBtN / 4 + 1;
 static_assert(kBtK * kBtN / 16 % kBtThreads == 0, "load split");
+template <bool P4>
 __global__ void __launch_bounds__(kBtThreads) k_mx_stage_bt(const uint8_t* __restrict__ B, int64_t ldb, int K, int N,
                                                             uint8_t* __restrict__ Bp, int Kp) {
     __shared__ uint32_t t[kBtK][kBtPitch];
@@ -345,19 +393,7 @@ __global__ void __launch_bounds__(kBtThreads) k_mx_stage_bt(const uint8_t* __res
         const int kk = v / (kBtN / 16), nh = (v % (kBtN / 16)) * 16;
         const int k = k0 + kk, n = n0 + nh;
         uint64_t lo = 0, hi = 0;
-        if (k < K && n < N) {
-            const uint8_t* row = B + (int64_t)k * ldb;
-            if (n + 16 <= N) {
-                lo = load8_any(row + n);
-                hi = load8_any(row + n + 8);
-            } else {
-                for (int e = 0; e < 16 && n + e < N; ++e) {
-                    const uint64_t b = __ldg(row + n + e);
-                    if (e < 8) lo |= b << (8 * e);
-                    else hi |= b << (8 * (e - 8));
-                }
-            }
-        }
+        if (k < K && n < N) load16_codes<P4>(B + (P4 ? (int64_t)k * ldb / 2 : (int64_t)k * ldb), n, N - n, &lo, &hi);
         uint32_t* w = &t[kk][nh >> 2];
         w[0] = (uint32_t)lo;
         w[1] = (uint32_t)(lo >> 32);
@@ -380,8 +416,13 @@ __global__ void __launch_bounds__(kBtThreads) k_mx_stage_bt(const uint8_t* __res
         out[3][g] = __byte_perm(a1, a3, 0x7632);
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j)
-        sbt_st_v4(Bp + (int64_t)(n0 + 4 * nw + j) * Kp + k0 + kv, make_uint4(out[j][0], out[j][1], out[j][2], out[j][3]));
+    for (int j = 0; j < 4; ++j) {
+        uint4 v = make_uint4(out[j][0], out[j][1], out[j][2], out[j][3]);
+        if (P4)  // 16 packed codes, then 8 bytes of padding
+            v = make_uint4(pack_nibbles((uint64_t)v.x | ((uint64_t)v.y << 32)),
+                           pack_nibbles((uint64_t)v.z | ((uint64_t)v.w << 32)), 0u, 0u);
+        sbt_st_v4(Bp + (int64_t)(n0 + 4 * nw + j) * Kp + k0 + kv, v);
+    }
 }
 
 // Scale chunks.
@@ -508,11 +549,17 @@ sbt_status sbt_launch_gemm_mx(sbt_context* ctx, int a_fmt, const void* A, int64_
     {
         const int64_t tasks = L.Mp * (L.Kp / 16);
         const int grid = (int)std::min<int64_t>(sbt_cdiv(tasks, 256), (int64_t)ctx->sm_count * 8);
-        k_mx_stage_a<<<grid, 256, 0, stream>>>((const uint8_t*)A, lda, (int)M, (int)K, Ap, (int)L.Kp, tasks);
+        if (a_fmt == kMxFmtE2M1)
+            k_mx_stage_a<true><<<grid, 256, 0, stream>>>((const uint8_t*)A, lda, (int)M, (int)K, Ap, (int)L.Kp, tasks);
+        else
+            k_mx_stage_a<false><<<grid, 256, 0, stream>>>((const uint8_t*)A, lda, (int)M, (int)K, Ap, (int)L.Kp, tasks);
         sbt_status st = sbt_after_launch(ctx, "gemm_block_scaled (stage A, 8-bit)");
         if (st) return st;
         dim3 g2((unsigned)sbt_cdiv(L.Kp, kBtK), (unsigned)(L.Np / kBtN));
-        k_mx_stage_bt<<<g2, kBtThreads, 0, stream>>>((const uint8_t*)B, ldb, (int)K, (int)N, Bp, (int)L.Kp);
+        if (b_fmt == kMxFmtE2M1)
+            k_mx_stage_bt<true><<<g2, kBtThreads, 0, stream>>>((const uint8_t*)B, ldb, (int)K, (int)N, Bp, (int)L.Kp);
+        else
+            k_mx_stage_bt<false><<<g2, kBtThreads, 0, stream>>>((const uint8_t*)B, ldb, (int)K, (int)N, Bp, (int)L.Kp);
         if ((st = sbt_after_launch(ctx, "gemm_block_scaled (stage B, 8-bit)"))) return st;
         const int64_t ta = (L.Mp / 128) * L.k_blocks * 32, tb = L.n_tiles * L.k_blocks * 256;
         const int g3 = (int)std::min<int64_t>(sbt_cdiv(ta + tb, 256), (int64_t)ctx->sm_count * 8);
@@ -539,7 +586,7 @@ sbt_status sbt_launch_gemm_mx(sbt_context* ctx, int a_fmt, const void* A, int64_
     p.m_tiles = (int)L.m_tiles;
     p.n_tiles = (int)L.n_tiles;
     p.k_blocks = (int)L.k_blocks;
-    p.idesc = idesc_mx_e8m0((uint32_t)a_fmt, (uint32_t)b_fmt, 256, MX_BN, 0);
+    p.idesc = idesc_mx_e8m0(mma_format(a_fmt), mma_format(b_fmt), 256, MX_BN, 0);
     p.status = ctx->status;
     p.wait_ns = ctx->wait_limit_ns;
     p.withhold_first_load = ctx->test_hook == SBT_TEST_WITHHOLD_LOAD;

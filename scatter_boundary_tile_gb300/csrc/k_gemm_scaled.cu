@@ -5,8 +5,8 @@
 // block of K / K_s elements along K (a_scale (M,K_s), b_scale (K_s,N), in
 // E8M0 or E4M3), fp32 accumulator and acc.
 //
-// E4M3 / E5M2 operands with E8M0 scales over blocks of 32 run on the tensor
-// cores' block scaling (k_gemm_mx.cu).  Every other combination takes this
+// E4M3 / E5M2 / E2M1 operands with E8M0 scales over blocks of 32 run on the
+// tensor cores' block scaling (k_gemm_mx.cu).  Every other combination takes this
 // path: the operand staging of the boundary-tile GEMM, with the scale folded
 // in.  Each element is decoded from its format and multiplied by its block's
 // scale in fp32, rounded to bf16 and written into the same padded K-major
@@ -214,8 +214,8 @@ sbt_status sbt_launch_gemm_block_scaled(sbt_context* ctx, int a_fmt, const void*
     if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2)
         return sbt_fail(SBT_ERR_INVALID_ARG, "gemm_block_scaled: extents must be below 2^30");
     if (K == 0) return sbt_launch_gemm_zero_k(ctx, D, ldd, true, acc, ld_acc, M, N, stream);
-    const bool byte_operands = (a_fmt == kFmtE4M3 || a_fmt == kFmtE5M2) && (b_fmt == kFmtE4M3 || b_fmt == kFmtE5M2);
-    if (byte_operands && s_fmt == kFmtE8M0 && K == 32 * Ks &&
+    // kind::mxf8f6f4 takes E4M3, E5M2 and (one code per byte) E2M1 operands
+    if (s_fmt == kFmtE8M0 && K == 32 * Ks &&
         (ctx->path == SBT_PATH_AUTO || ctx->path == SBT_PATH_TMA))
         return sbt_launch_gemm_mx(ctx, a_fmt, A, lda, b_fmt, B, ldb, SA, ld_sa, SB, ld_sb, acc, ld_acc, D, ldd, M, N,
                                   K, workspace, stream);

@@ -307,7 +307,7 @@ __device__ __forceinline__ void tc_mma_mx_pair(uint32_t d_tmem, uint64_t a_desc,
 }
 
 // Instruction descriptor, kind::mxf8f6f4 with E8M0 scales: operand formats
-// (0 = E4M3, 1 = E5M2), K-major A and B, fp32 accumulator, M x N; `sf_id`
+// (0 = E4M3, 1 = E5M2, 5 = E2M1), K-major A and B, fp32 accumulator, M x N; `sf_id`
 // selects the byte of each 32-bit scale column used by this K = 32 step.
 __host__ __device__ __forceinline__ uint32_t idesc_mx_e8m0(uint32_t a_fmt, uint32_t b_fmt, uint32_t m, uint32_t n,
                                                             uint32_t sf_id) {

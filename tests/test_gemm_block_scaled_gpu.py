@@ -80,7 +80,8 @@ def test_shapes_and_formats_vs_oracle(ctx, fmts, shape):
     check(run(ctx, g), g)
 
 
-MX_FORMATS = [("e4m3", "e4m3"), ("e5m2", "e5m2"), ("e4m3", "e5m2"), ("e5m2", "e4m3")]
+MX_FORMATS = [("e4m3", "e4m3"), ("e5m2", "e5m2"), ("e4m3", "e5m2"), ("e5m2", "e4m3"), ("e2m1", "e2m1"),
+              ("e2m1", "e4m3"), ("e5m2", "e2m1")]
 MX_SHAPES = [(1, 1, 32), (7, 9, 96), (65, 97, 160), (256, 224, 128), (257, 225, 256), (300, 449, 544),
              (513, 448, 32)]
 
@@ -89,7 +90,7 @@ MX_SHAPES = [(1, 1, 32), (7, 9, 96), (65, 97, 160), (256, 224, 128), (257, 225, 
 @pytest.mark.parametrize("fmts", MX_FORMATS, ids=lambda f: "x".join(f))
 @pytest.mark.parametrize("shape", MX_SHAPES, ids=lambda s: "x".join(map(str, s)))
 def test_e8m0_block32_both_paths_vs_oracle(ctx, path, fmts, shape):
-    # E4M3/E5M2 with E8M0 scales per 32 along K: "auto" takes the
+    # E4M3/E5M2/E2M1 with E8M0 scales per 32 along K: "auto" takes the
     # tcgen05 kind::mxf8f6f4 kernel (256 x 224 tiles, 128-deep K blocks, so
     # these shapes cut tiles and K blocks at every kind of edge), "scalar"
     # forces the bf16 staging path; both must meet the same bounds.
