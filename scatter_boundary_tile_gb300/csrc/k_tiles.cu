@@ -28,7 +28,8 @@ constexpr int kThreads = 256;
 //               that cover it (only when both chunks lie inside the array's
 //               byte span, so nothing outside the caller's buffer is read);
 //   kElem    -- element by element (column stride != 1, odd tile widths, or
-//               unaligned stores).
+//               unaligned stores; the store's element path is one warp per
+//               tile, k_tile_store_rows).
 enum TileMode { kAligned = 0, kRealign = 1, kElem = 2 };
 
 struct TileParams {
@@ -174,53 +175,89 @@ __global__ void __launch_bounds__(kThreads) k_tile_load(const TileParams p) {
     }
 }
 
-template <int ES, int MODE>
+// Vector path of the clipped store (every vector 16-byte aligned on both
+// sides); the element path is k_tile_store_rows below.
+template <int ES>
 __global__ void __launch_bounds__(kThreads) k_tile_store(const TileParams p) {
     constexpr int V = 16 / ES;
-    constexpr int U = MODE == kElem ? 8 : 4;
-    typedef typename sbt_elem<ES>::T T;
+    constexpr int U = 4;
     const uint32_t stride = gridDim.x * kThreads;
     for (uint32_t base = blockIdx.x * kThreads + threadIdx.x; base < p.ntasks; base += stride * U) {
-        if (MODE != kElem) {
-            uint4 val[U];
+        uint4 val[U];
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const uint32_t t = base + u * stride;
-                if (t < p.ntasks) val[u] = sbt_ld_nc_v4(p.tiles_r + ((int64_t)p.tile0 * p.per_tile + t) * 16);
-            }
+        for (int u = 0; u < U; ++u) {
+            const uint32_t t = base + u * stride;
+            if (t < p.ntasks) val[u] = sbt_ld_nc_v4(p.tiles_r + ((int64_t)p.tile0 * p.per_tile + t) * 16);
+        }
 #pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const uint32_t t = base + u * stride;
-                if (t >= p.ntasks) continue;
-                const TaskPos q = tile_task_pos(p, t, V);
-                if (q.r < 0 || q.r >= p.rows) continue;
-                if (q.c >= 0 && q.c + V <= p.cols) {
-                    sbt_st_v4(p.arr_w + (q.r * p.stride_r + q.c) * ES, val[u]);
-                } else if (q.c + V > 0 && q.c < p.cols) {
+        for (int u = 0; u < U; ++u) {
+            const uint32_t t = base + u * stride;
+            if (t >= p.ntasks) continue;
+            const TaskPos q = tile_task_pos(p, t, V);
+            if (q.r < 0 || q.r >= p.rows) continue;
+            if (q.c >= 0 && q.c + V <= p.cols) {
+                sbt_st_v4(p.arr_w + (q.r * p.stride_r + q.c) * ES, val[u]);
+            } else if (q.c + V > 0 && q.c < p.cols) {
 #pragma unroll
-                    for (int e = 0; e < V; ++e) {
-                        const int64_t c = q.c + e;
-                        if (c >= 0 && c < p.cols) st_elem<ES>(p.arr_w, q.r * p.stride_r + c, sbt_vec_get<ES>(val[u], e));
-                    }
+                for (int e = 0; e < V; ++e) {
+                    const int64_t c = q.c + e;
+                    if (c >= 0 && c < p.cols) st_elem<ES>(p.arr_w, q.r * p.stride_r + c, sbt_vec_get<ES>(val[u], e));
                 }
-            }
-        } else {
-            T val[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const uint32_t t = base + u * stride;
-                if (t < p.ntasks) val[u] = ld_elem<ES>(p.tiles_r, (int64_t)p.tile0 * p.per_tile + t);
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const uint32_t t = base + u * stride;
-                if (t >= p.ntasks) continue;
-                const TaskPos q = tile_task_pos(p, t, 1);
-                if (q.r >= 0 && q.r < p.rows && q.c >= 0 && q.c < p.cols)
-                    st_elem<ES>(p.arr_w, q.r * p.stride_r + q.c * p.stride_c, val[u]);
             }
         }
     }
+}
+
+// Element path of the clipped store, one warp per tile.  A tile's rows are
+// contiguous on the tile side, so lane j moves column j (then j + 32, ...) of
+// every row with one 2- or 4-byte load and store.  The tile's array origin,
+// its in-bounds row range and each lane's column test are worked out once
+// per tile, so a row costs a few address additions; rows outside the array
+// are not visited.  (One task per element, each decoding its own tile, row and
+// column, was instruction-bound at 0.62 ms on the unaligned fp32 workload.)
+template <int ES>
+__global__ void __launch_bounds__(kThreads) k_tile_store_rows(const TileParams p, uint32_t ntiles) {
+    typedef typename sbt_elem<ES>::T T;
+    constexpr int U = 32;  // rows in flight per lane (8: 0.51 ms, 16: 0.49, 32: 0.445, 64: 0.53 on the unaligned fp32 workload)
+    const int lane = threadIdx.x & 31;
+    const uint32_t nwarps = gridDim.x * (kThreads / 32);
+    const int64_t tile_elems = (int64_t)p.tile_r * p.tile_c;
+    for (uint32_t t = blockIdx.x * (kThreads / 32) + (threadIdx.x >> 5); t < ntiles; t += nwarps) {
+        const uint32_t tr = sbt_div(p.div_grid_c, t);
+        const uint32_t tc = t - tr * (uint32_t)p.grid_c;
+        const int64_t r0 = p.origin_r + (int64_t)tr * p.step_r;
+        const int64_t c0 = p.origin_c + (int64_t)tc * p.step_c;
+        // tile rows i with 0 <= r0 + i < rows
+        const int i_lo = r0 >= 0 ? 0 : (int)(-r0 < p.tile_r ? -r0 : p.tile_r);
+        const int i_hi = p.rows - r0 <= 0 ? 0 : (int)(p.rows - r0 < p.tile_r ? p.rows - r0 : p.tile_r);
+        const T* src = reinterpret_cast<const T*>(p.tiles_r) + (int64_t)t * tile_elems;
+        T* dst = reinterpret_cast<T*>(p.arr_w);
+        for (int j = lane; j < p.tile_c; j += 32) {
+            const int64_t c = c0 + j;
+            const bool col_ok = c >= 0 && c < p.cols;
+            const int64_t col_off = c * p.stride_c;
+            for (int i0 = i_lo; i0 < i_hi; i0 += U) {
+                T v[U];
+#pragma unroll
+                for (int u = 0; u < U; ++u)
+                    v[u] = i0 + u < i_hi ? src[(int64_t)(i0 + u) * p.tile_c + j] : T(0);
+                if (col_ok) {
+                    const int64_t row_off = (r0 + i0) * p.stride_r + col_off;
+#pragma unroll
+                    for (int u = 0; u < U; ++u)
+                        if (i0 + u < i_hi) dst[row_off + (int64_t)u * p.stride_r] = v[u];
+                }
+            }
+        }
+    }
+}
+
+template <int ES>
+sbt_status launch_tile_store_rows(sbt_context* ctx, const TileParams& p, int64_t ntiles, cudaStream_t s) {
+    auto kern = k_tile_store_rows<ES>;
+    const int grid = sbt_persistent_grid(ctx, (const void*)kern, kThreads, 0, sbt_cdiv(ntiles, kThreads / 32));
+    kern<<<grid, kThreads, 0, s>>>(p, (uint32_t)ntiles);
+    return sbt_after_launch(ctx, "tile_store_clipped (element rows)");
 }
 
 // ---------------------------------------------------------------------------- ragged
@@ -489,11 +526,11 @@ sbt_status sbt_launch_tile_store(sbt_context* ctx, int es, const void* src_tiles
     p.arr_w = (char*)dst;
     p.tiles_r = (const char*)src_tiles;
     const char* what = "tile_store_clipped";
-    if (es == 4)
-        return mode == kAligned ? launch_tiles(ctx, k_tile_store<4, kAligned>, p, ntiles, what, stream)
-                                : launch_tiles(ctx, k_tile_store<4, kElem>, p, ntiles, what, stream);
-    return mode == kAligned ? launch_tiles(ctx, k_tile_store<2, kAligned>, p, ntiles, what, stream)
-                            : launch_tiles(ctx, k_tile_store<2, kElem>, p, ntiles, what, stream);
+    if (mode == kElem)
+        return es == 4 ? launch_tile_store_rows<4>(ctx, p, ntiles, stream)
+                       : launch_tile_store_rows<2>(ctx, p, ntiles, stream);
+    return es == 4 ? launch_tiles(ctx, k_tile_store<4>, p, ntiles, what, stream)
+                   : launch_tiles(ctx, k_tile_store<2>, p, ntiles, what, stream);
 }
 
 sbt_status sbt_launch_ragged(sbt_context* ctx, int es, const void* x, int64_t total_rows, int32_t heads,
