@@ -491,11 +491,19 @@ __global__ void __launch_bounds__(256) k_stage_a(const uint16_t* __restrict__ A,
         uint32_t w[4] = {0, 0, 0, 0};
         if (m < M) {
             const uint16_t* row = A + m * lda;
+            if (k0 + 8 <= K) {  // whole vector inside the row: aligned 8-byte loads (lda may be odd)
+                const uint64_t lo = sbt_load8_any(row + k0), hi = sbt_load8_any(row + k0 + 4);
+                w[0] = (uint32_t)lo;
+                w[1] = (uint32_t)(lo >> 32);
+                w[2] = (uint32_t)hi;
+                w[3] = (uint32_t)(hi >> 32);
+            } else {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const int k = k0 + e;
-                const uint32_t x = k < K ? (uint32_t)__ldg(row + k) : 0u;
-                w[e >> 1] |= x << (16 * (e & 1));
+                for (int e = 0; e < 8; ++e) {
+                    const int k = k0 + e;
+                    const uint32_t x = k < K ? (uint32_t)__ldg(row + k) : 0u;
+                    w[e >> 1] |= x << (16 * (e & 1));
+                }
             }
         }
         sbt_st_v4(Ap + m * Kp + k0, make_uint4(w[0], w[1], w[2], w[3]));
@@ -503,29 +511,51 @@ __global__ void __launch_bounds__(256) k_stage_a(const uint16_t* __restrict__ A,
 }
 
 // B' [Np][Kp] <- transpose of B [K][N] (row stride ldb), zero past K or N.
-// 64 x 64 tiles through shared memory: coalesced reads along n, 16-byte writes along k.
+// 64 x 64 tiles: each thread loads two 16-byte row pieces (8 values along n,
+// through aligned 8-byte loads since ldb may be odd) into shared words, then
+// reads an 8 (k) x 2 (n) block as eight words, transposes its 2 x 2 blocks of
+// 16-bit values with byte permutes and writes two 16-byte vectors along k.
 __global__ void __launch_bounds__(256) k_stage_bt(const uint16_t* __restrict__ B, int64_t ldb, int K, int N,
                                                   uint16_t* __restrict__ Bp, int Kp) {
-    __shared__ uint16_t t[64][66];
+    __shared__ uint32_t t[64][33];  // [k][n pair]
     const int k0 = blockIdx.x * 64, n0 = blockIdx.y * 64;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const int idx = i * 256 + threadIdx.x;
-        const int kk = idx >> 6, nn = idx & 63;
-        const int k = k0 + kk, n = n0 + nn;
-        t[kk][nn] = (k < K && n < N) ? __ldg(B + (int64_t)k * ldb + n) : (uint16_t)0;
+    for (int i = 0; i < 2; ++i) {
+        const int v = i * 256 + threadIdx.x;  // 64 rows x 8 pieces
+        const int kk = v >> 3, nh = (v & 7) * 8;
+        const int k = k0 + kk, n = n0 + nh;
+        uint64_t lo = 0, hi = 0;
+        if (k < K && n < N) {
+            const uint16_t* row = B + (int64_t)k * ldb;
+            if (n + 8 <= N) {
+                lo = sbt_load8_any(row + n);
+                hi = sbt_load8_any(row + n + 4);
+            } else {
+                for (int e = 0; e < 8 && n + e < N; ++e) {
+                    const uint64_t x = __ldg(row + n + e);
+                    if (e < 4) lo |= x << (16 * e);
+                    else hi |= x << (16 * (e - 4));
+                }
+            }
+        }
+        uint32_t* w = &t[kk][nh >> 1];
+        w[0] = (uint32_t)lo;
+        w[1] = (uint32_t)(lo >> 32);
+        w[2] = (uint32_t)hi;
+        w[3] = (uint32_t)(hi >> 32);
     }
     __syncthreads();
+    // n = 2 np, 2 np + 1; k = kv .. kv + 7 (eight lanes cover one 128-byte run of a B' row)
+    const int np = threadIdx.x >> 3, kv = (threadIdx.x & 7) * 8;
+    uint32_t o0[4], o1[4];
 #pragma unroll
-    for (int i = 0; i < 2; ++i) {
-        const int task = i * 256 + threadIdx.x;  // 64 rows of B' x 8 vectors
-        const int nn = task >> 3, kv = task & 7;
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            w[e] = (uint32_t)t[kv * 8 + 2 * e][nn] | ((uint32_t)t[kv * 8 + 2 * e + 1][nn] << 16);
-        sbt_st_v4(Bp + (int64_t)(n0 + nn) * Kp + k0 + kv * 8, make_uint4(w[0], w[1], w[2], w[3]));
+    for (int e = 0; e < 4; ++e) {
+        const uint32_t w0 = t[kv + 2 * e][np], w1 = t[kv + 2 * e + 1][np];
+        o0[e] = __byte_perm(w0, w1, 0x5410);  // (k, k+1) of n = 2 np
+        o1[e] = __byte_perm(w0, w1, 0x7632);  // (k, k+1) of n = 2 np + 1
     }
+    sbt_st_v4(Bp + (int64_t)(n0 + 2 * np) * Kp + k0 + kv, make_uint4(o0[0], o0[1], o0[2], o0[3]));
+    sbt_st_v4(Bp + (int64_t)(n0 + 2 * np + 1) * Kp + k0 + kv, make_uint4(o1[0], o1[1], o1[2], o1[3]));
 }
 
 // C[m][n] = acc[m][n] (fp32 C), or 0 without acc, for m < M, n < N: the K = 0 result.

@@ -295,17 +295,6 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
 
 // ---------------------------------------------------------------------------- staging
 
-// Eight bytes p..p+7, all inside the caller's array, through aligned 8-byte
-// loads (the words holding p and, when p is unaligned, p+7).
-__device__ __forceinline__ uint64_t load8_any(const uint8_t* p) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    const int sh = (int)(a & 7u) * 8;
-    const uint64_t* w = reinterpret_cast<const uint64_t*>(a & ~(uintptr_t)7);
-    const uint64_t lo = __ldg(w);
-    if (sh == 0) return lo;
-    return (lo >> sh) | (__ldg(w + 1) << (64 - sh));
-}
-
 // E2M1 operands: kind::mxf8f6f4 reads a 4-bit type from each 16-byte piece of
 // a K-major row as 16 packed codes in the first 8 bytes (even element in the
 // low nibble, as in the caller's arrays) followed by 8 bytes of padding.
@@ -338,12 +327,12 @@ __device__ __forceinline__ void load16_codes(const uint8_t* row, int e0, int ava
     *hi = 0;
     if (avail >= 16) {
         if (P4) {
-            const uint64_t c = load8_any(row + e0 / 2);
+            const uint64_t c = sbt_load8_any(row + e0 / 2);
             *lo = spread_nibbles((uint32_t)c);
             *hi = spread_nibbles((uint32_t)(c >> 32));
         } else {
-            *lo = load8_any(row + e0);
-            *hi = load8_any(row + e0 + 8);
+            *lo = sbt_load8_any(row + e0);
+            *hi = sbt_load8_any(row + e0 + 8);
         }
         return;
     }

@@ -58,19 +58,8 @@ __device__ __forceinline__ uint32_t lowp_code(const uint8_t* __restrict__ p, int
     else return __ldg(p + i);
 }
 
-// Eight bytes from p..p+7 (all inside the array) through aligned 8-byte loads.
-// The aligned word holding p, and when p is unaligned the one holding p+7,
-// each contain a byte of the array, so neither reaches past its pages.
-__device__ __forceinline__ uint64_t load8_any(const uint8_t* p) {
-    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
-    const int sh = (int)(a & 7u) * 8;
-    const uint64_t* w = reinterpret_cast<const uint64_t*>(a & ~(uintptr_t)7);
-    const uint64_t lo = __ldg(w);
-    if (sh == 0) return lo;
-    return (lo >> sh) | (__ldg(w + 1) << (64 - sh));
-}
-
-// Four bytes from p..p+3 (all inside the array), the same way.
+// Four bytes p..p+3 (all inside the array) through aligned 4-byte loads, as
+// sbt_load8_any does with eight.
 __device__ __forceinline__ uint32_t load4_any(const uint8_t* p) {
     const uintptr_t a = reinterpret_cast<uintptr_t>(p);
     const int sh = (int)(a & 3u) * 8;
@@ -105,7 +94,7 @@ __global__ void __launch_bounds__(256) k_stage_scaled_a(const uint8_t* __restric
 #pragma unroll
                     for (int e = 0; e < 8; ++e) x[e] = lowp_value<FMT>((c >> (4 * e)) & 15u);
                 } else {
-                    const uint64_t c = load8_any(A + m * lda + k0);
+                    const uint64_t c = sbt_load8_any(A + m * lda + k0);
 #pragma unroll
                     for (int e = 0; e < 8; ++e) x[e] = lowp_value<FMT>((uint32_t)(c >> (8 * e)) & 255u);
                 }

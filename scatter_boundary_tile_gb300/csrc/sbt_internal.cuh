@@ -173,6 +173,18 @@ __device__ __forceinline__ uint4 sbt_ld_nc_v4_l1(const void* p) {
     return v;
 }
 
+// Eight bytes p..p+7, all inside the caller's array, through aligned 8-byte
+// loads: the word holding p and, when p is unaligned, the one holding p+7 each
+// contain a byte of the array, so neither reaches past its pages.
+__device__ __forceinline__ uint64_t sbt_load8_any(const void* ptr) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(ptr);
+    const int sh = (int)(a & 7u) * 8;
+    const uint64_t* w = reinterpret_cast<const uint64_t*>(a & ~(uintptr_t)7);
+    const uint64_t lo = __ldg(w);
+    if (sh == 0) return lo;
+    return (lo >> sh) | (__ldg(w + 1) << (64 - sh));
+}
+
 // Streaming (evict-first) 16-byte store, for outputs this kernel never reads back.
 __device__ __forceinline__ void sbt_st_v4_cs(void* p, uint4 v) {
     asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
