@@ -73,7 +73,8 @@ SBT_API sbt_status sbt_set_path(sbt_context* ctx, sbt_path path);
 /* Limit of every bounded device-side wait, in nanoseconds (default 2e9). */
 SBT_API sbt_status sbt_set_wait_limit_ns(sbt_context* ctx, uint64_t ns);
 /* Test hook for the bounded device waits.  SBT_TEST_WITHHOLD_LOAD makes the
- * next GEMM and bulk row launches on this context skip their first copy, so
+ * next GEMM (bf16 or block-scaled tensor path) and bulk row launches on this
+ * context skip their first copy, so
  * a consumer's bounded wait runs out (no fault, no hang): the kernel sets the
  * status flag, drains and returns, and sbt_check_status() reports
  * SBT_ERR_DEVICE_TIMEOUT.  Stays set until reset with SBT_TEST_NONE. */
