@@ -47,7 +47,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=8.0, help="CPU-baseline sample budget")
     ap.add_argument("--profile", default=None,
                     choices=["gather", "scatter", "scatter_add", "ragged", "ragged_store", "tile_load_tma", "tile_load", "tile_store", "tile_load_unaligned",
-                             "tile_store_unaligned", "gemm", "gemm_scaled"],
+                             "tile_store_unaligned", "gemm", "gemm_scaled", "gather_cols"],
                     help="only launch one operation's workload (warmup + steps launches) for ncu")
     ap.add_argument("--scale", type=float, default=1.0, help="--profile: fraction of the workload's rows")
     return ap.parse_args()
@@ -705,6 +705,13 @@ def run_profile(args):
         else:
             fn = lambda: sbt.tile_store_clipped(ctx, tiles, gr, gc, 64, 32, ad, r_, c_, ld, 1, 0, 0, 64, 32,
                                                 dtype="f32")
+    elif op == "gather_cols":  # bf16 2,048 x 100,003, 4,096 random columns (rows scaled)
+        rows_ = max(1, int(2048 * f))
+        a = synth.normal_bf16(0x5B7103, (rows_, 100_003))
+        ci = synth.int_below(0x5B7104, 4096, 100_003).astype(np.int32)
+        ad, cid = dev_bytes(a), dev_bytes(ci)
+        outc = torch.empty(rows_ * 4096 * 2, dtype=torch.uint8, device="cuda")
+        fn = lambda: sbt.gather_cols(ctx, ad, rows_, 100_003, 100_003, cid, 4096, outc, 4096, rows_, dtype="bf16")
     elif op == "gemm_scaled":  # (8191, 8193, 4096) E4M3 / E8M0 per 32, scaled along M
         M, N, K = max(1, int(8191 * f)), 8193, 4096
         g = wl.gemm_block_scaled(M=M, N=N, K=K, block=32)
