@@ -11,10 +11,10 @@
 //     scales are packed per (row or column tile, 128-deep K block) into
 //     chunks in the order the tensor memory wants them (below), 2^0 past the
 //     extents.
-//  2. A persistent kernel on clusters of two CTAs (M = 256 per pair, N = 224
-//     per tile, 128 K per stage): warp 0 of each CTA TMA-loads its 128 rows of
-//     A8, its 112 rows of B8^T and the stage's scale chunks into a 5-stage
-//     ring; the leader's warp 1 copies the scale chunks into TMEM
+//  2. A persistent kernel on clusters of two CTAs (M = 256 per pair, N = 208
+//     per tile, two 128-deep K blocks per stage): warp 0 of each CTA TMA-loads
+//     its 128 rows of A8, its 104 rows of B8^T and the scale chunks of the
+//     stage's K blocks into a 3-stage ring; the leader's warp 1 copies the scale chunks into TMEM
 //     (tcgen05.cp.cta_group::2, each CTA's own chunk to its own TMEM) and
 //     issues four block-scaled MMAs per stage, one per K = 32 step, the step
 //     choosing the scale byte; four epilogue warps per CTA add acc and store
@@ -22,7 +22,7 @@
 //
 // Scale placement in TMEM (per CTA, 32-bit columns, 4 scale bytes each): the
 // scale of row m (of this CTA's 128 rows of A) for step s sits in lane m,
-// column sfa + m / 32, byte s; that of column n of B (all 224 columns, in
+// column sfa + m / 32, byte s; that of column n of B (all 208 columns, in
 // both CTAs) in lanes n % 32 + 32 q of every quarter q, column sfb + n / 32,
 // byte s.  Scale addresses must be multiples of 4 columns.  A's scales come
 // with one tcgen05.cp 32x128b.warpx4 (row r of a [32][16-byte] chunk to lane
@@ -33,11 +33,15 @@
 // the 8191 x 8193 x 4096 call, two copies ~39 us), so B's eight columns take
 // one larger copy.
 //
-// TMEM: two 224-column fp32 accumulators (the epilogue of one tile overlaps
-// the main loop of the next) and five 12-column scale slots, one per stage,
-// fill 508 of the 512 columns.  A slot is rewritten only after the stage's
-// previous MMAs completed: its new data arrives after the producer saw the
-// stage's empty barrier, which those MMAs' commit signals.
+// TMEM: two 208-column fp32 accumulators (the epilogue of one tile overlaps
+// the main loop of the next) and six 12-column scale slots, one per K block
+// of each stage (488 of the 512 columns).  A slot is rewritten only after the
+// stage's previous MMAs completed: its new data arrives after the producer saw
+// the stage's empty barrier, which those MMAs' commit signals.  Two K blocks
+// per stage halve the barrier round trips (0.334 -> 0.327 ms for the
+// 8191 x 8193 x 4096 call); the scale slots of three such stages do not fit
+// beside two 224-column accumulators, hence N = 208 (224 with two stages:
+// 0.331 ms; 208 with five one-block stages: 0.352 ms).
 #include <algorithm>
 #include <string>
 
@@ -48,24 +52,28 @@ namespace {
 
 using namespace sbt_ptx;
 
-constexpr int MX_BN = 224;   // columns per tile
-constexpr int kMxFmtE4M3 = 0, kMxFmtE5M2 = 1, kMxFmtE2M1 = 3;  // sbt_lowp_format codes
+constexpr int MX_BN = 208;   // columns per tile
+constexpr int kMxFmtE2M1 = 3;  // sbt_lowp_format code of E2M1 (E4M3 = 0 and E5M2 = 1 are the MMA codes too)
 
 // Operand type field of the kind::mxf8f6f4 instruction descriptor.
 uint32_t mma_format(int fmt) { return fmt == kMxFmtE2M1 ? 5u : (uint32_t)fmt; }
 constexpr int MX_BK = 128;   // K per stage (bytes of one 128-byte swizzle row)
-constexpr int kMxStages = 5;
+constexpr int kMxStages = 3;
+constexpr int kMxKB = 2;     // 128-deep K blocks per stage
 constexpr int kMxThreads = 192;  // warp 0: TMA, warp 1: MMA, warps 2..5: epilogue
 constexpr uint32_t kMxABytes = 128 * MX_BK;
 constexpr uint32_t kMxBBytes = (MX_BN / 2) * MX_BK;
-constexpr uint32_t kMxSfbOff = kMxABytes + kMxBBytes;  // 30720: B scales of the stage's K block (4 KB)
-constexpr uint32_t kMxSfaOff = kMxSfbOff + 4096;       // A scales of the stage's K block (512 B)
-constexpr uint32_t kMxTxBytes = kMxSfaOff + 512;       // bytes one CTA receives per stage
-constexpr uint32_t kMxStageBytes = 35840;              // keeps every stage's A tile 1024-aligned
+// Stage layout per CTA: the K blocks' A atoms, then their B atoms, then their
+// B scale chunks (4 KB) and A scale chunks (512 B); every piece 1024-aligned.
+constexpr uint32_t kMxBOff = kMxKB * kMxABytes;
+constexpr uint32_t kMxSfbOff = kMxBOff + kMxKB * kMxBBytes;
+constexpr uint32_t kMxSfaOff = kMxSfbOff + kMxKB * 4096;
+constexpr uint32_t kMxTxBytes = kMxABytes + kMxBBytes + 4096 + 512;  // bytes one CTA receives per K block
+constexpr uint32_t kMxStageBytes = (kMxSfaOff + kMxKB * 512 + 1023u) & ~1023u;
 constexpr uint32_t kMxSfCol0 = 2 * MX_BN;              // scale slots after the two accumulators
-constexpr uint32_t kMxSfCols = 12;                      // 4 columns of A scales + 8 of B scales
-static_assert(kMxSfCol0 + kMxStages * kMxSfCols <= 512, "TMEM columns");
-static_assert(kMxTxBytes <= kMxStageBytes && kMxStageBytes % 1024 == 0, "stage layout");
+constexpr uint32_t kMxSfCols = 12;                      // per K block: 4 columns of A scales + 8 of B scales
+static_assert(kMxSfCol0 + kMxStages * kMxKB * kMxSfCols <= 512, "TMEM columns");
+static_assert(kMxBBytes % 1024 == 0 && kMxStageBytes % 1024 == 0 && kMxSfCol0 % 4 == 0, "layout");
 constexpr int kMxEpiWarps = 4;
 constexpr int kMxEpiWords = 32 * 33;
 constexpr int kMxNumBars = 2 * kMxStages + 5;
@@ -80,8 +88,8 @@ struct MxParams {
     const float* acc;
     int64_t ld_acc;
     int M, N, K;
-    int m_tiles, n_tiles, k_blocks;  // 256-row tiles, 224-column tiles, 128-deep K blocks
-    uint32_t idesc;                  // formats, M = 256, N = 224; the scale byte is or-ed in per step
+    int m_tiles, n_tiles, k_blocks;  // 256-row tiles, 208-column tiles, 128-deep K blocks
+    uint32_t idesc;                  // formats, M = 256, N = 208; the scale byte is or-ed in per step
     unsigned int* status;
     uint64_t wait_ns;
     int withhold_first_load;
@@ -98,12 +106,13 @@ __device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, 
     *nt = within / gm;
 }
 
-// Drain this warp's 32 rows of one 128 x 224 accumulator, add acc and store
+// Drain this warp's 32 rows of one 128 x 208 accumulator, add acc and store
 // columns < N of rows < M through a padded shared transpose (one contiguous
 // 32-column segment per store instruction).
 __device__ __forceinline__ void mx_epilogue_tile(const MxParams& p, uint32_t tmem_acc, int q, int lane, float* buf,
                                                  int row0, int n0) {
-    const int chunks = (min(MX_BN, p.N - n0) + 31) / 32;
+    const int n_valid = min(MX_BN, p.N - n0);  // columns of this tile inside N (MX_BN is not a multiple of 32)
+    const int chunks = (n_valid + 31) / 32;
     for (int c = 0; c < chunks; ++c) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(tmem_acc + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
@@ -112,7 +121,7 @@ __device__ __forceinline__ void mx_epilogue_tile(const MxParams& p, uint32_t tme
         for (int j = 0; j < 32; ++j) buf[lane * 33 + j] = __uint_as_float(r[j]);
         __syncwarp();
         const int col = n0 + c * 32 + lane;
-        if (col < p.N) {
+        if (c * 32 + lane < n_valid) {
             if (p.acc) {
                 for (int rr = 0; rr < 32 && row0 + rr < p.M; ++rr)
                     p.D[(int64_t)(row0 + rr) * p.ldd + col] =
@@ -185,7 +194,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
             for (int tile = cluster; ok && tile < num_tiles; tile += nclusters) {
                 int mt, nt;
                 tile_coords(tile, p.m_tiles, p.n_tiles, &mt, &nt);
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                for (int kb0 = 0; kb0 < p.k_blocks; kb0 += kMxKB) {
                     if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, p.wait_ns, abort_flag, p.status,
                                            kCodeProducer)) {
                         ok = false;
@@ -194,17 +203,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
                     const bool withhold = p.withhold_first_load && blockIdx.x == 0 && issued == 0;
                     ++issued;
                     if (!withhold) {
+                        const int nkb = p.k_blocks - kb0 < kMxKB ? p.k_blocks - kb0 : kMxKB;
                         const uint32_t sa = smem_u32(smem + (size_t)stage * kMxStageBytes);
                         const uint32_t leader_full = mapa_shared(full_bar(stage), 0);
-                        if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * kMxTxBytes);
-                        tma_load_2d_pair(sa, &tmA, kb * MX_BK, mt * 256 + (int)rank * 128, leader_full);
-                        tma_load_2d_pair(sa + kMxABytes, &tmB, kb * MX_BK, nt * MX_BN + (int)rank * (MX_BN / 2),
-                                         leader_full);
-                        // scale chunks viewed as rows of 256 B: B 4 KB per (tile, K block), A 512 B per
-                        // (128-row group, K block)
-                        tma_load_2d_pair(sa + kMxSfbOff, &tmSB, 0, (nt * p.k_blocks + kb) * 16, leader_full);
-                        tma_load_2d_pair(sa + kMxSfaOff, &tmSA, 0, ((mt * 2 + (int)rank) * p.k_blocks + kb) * 2,
-                                         leader_full);
+                        if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * (uint32_t)nkb * kMxTxBytes);
+                        for (int j = 0; j < nkb; ++j) {
+                            const int kb = kb0 + j;
+                            tma_load_2d_pair(sa + j * kMxABytes, &tmA, kb * MX_BK, mt * 256 + (int)rank * 128,
+                                             leader_full);
+                            tma_load_2d_pair(sa + kMxBOff + j * kMxBBytes, &tmB, kb * MX_BK,
+                                             nt * MX_BN + (int)rank * (MX_BN / 2), leader_full);
+                            // scale chunks viewed as rows of 256 B: B 4 KB per (tile, K block), A 512 B per
+                            // (128-row group, K block)
+                            tma_load_2d_pair(sa + kMxSfbOff + j * 4096, &tmSB, 0, (nt * p.k_blocks + kb) * 16,
+                                             leader_full);
+                            tma_load_2d_pair(sa + kMxSfaOff + j * 512, &tmSA, 0,
+                                             ((mt * 2 + (int)rank) * p.k_blocks + kb) * 2, leader_full);
+                        }
                     }
                     if (++stage == kMxStages) {
                         stage = 0;
@@ -229,24 +244,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + (uint32_t)(acc * MX_BN);
-                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                for (int kb0 = 0; kb0 < p.k_blocks; kb0 += kMxKB) {
                     if (!mbar_wait_bounded(full_bar(stage), phase, p.wait_ns, abort_flag, p.status, kCodeMma)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
+                    const int nkb = p.k_blocks - kb0 < kMxKB ? p.k_blocks - kb0 : kMxKB;
                     const uint32_t sa = smem_u32(smem + (size_t)stage * kMxStageBytes);
-                    const uint32_t sfa = tmem_base + kMxSfCol0 + kMxSfCols * (uint32_t)stage;
-                    const uint32_t sfb = sfa + 4;
-                    tc_cp_pair_32x128b_warpx4(sfa, smem_desc_rows16(sa + kMxSfaOff));
-                    tc_cp_pair_128x256b(sfb, smem_desc_rows32(sa + kMxSfbOff));
-                    const int k_rem = p.K - kb * MX_BK;
-                    const int k_steps = k_rem >= MX_BK ? MX_BK / 32 : (k_rem + 31) / 32;
-                    for (int ks = 0; ks < k_steps; ++ks)
-                        tc_mma_mx_pair(d_tmem, smem_desc_sw128(sa + 32u * ks),
-                                       smem_desc_sw128(sa + kMxABytes + 32u * ks),
-                                       p.idesc | ((uint32_t)ks << 4) | ((uint32_t)ks << 29), sfa, sfb,
-                                       (kb | ks) != 0 ? 1u : 0u);
+                    for (int j = 0; j < nkb; ++j) {
+                        const int kb = kb0 + j;
+                        const uint32_t sfa =
+                            tmem_base + kMxSfCol0 + kMxSfCols * (uint32_t)(stage * kMxKB + j);
+                        const uint32_t sfb = sfa + 4;
+                        tc_cp_pair_32x128b_warpx4(sfa, smem_desc_rows16(sa + kMxSfaOff + j * 512));
+                        tc_cp_pair_128x256b(sfb, smem_desc_rows32(sa + kMxSfbOff + j * 4096));
+                        const uint32_t a_s = sa + j * kMxABytes, b_s = sa + kMxBOff + j * kMxBBytes;
+                        const int k_rem = p.K - kb * MX_BK;
+                        const int k_steps = k_rem >= MX_BK ? MX_BK / 32 : (k_rem + 31) / 32;
+                        for (int ks = 0; ks < k_steps; ++ks)
+                            tc_mma_mx_pair(d_tmem, smem_desc_sw128(a_s + 32u * ks), smem_desc_sw128(b_s + 32u * ks),
+                                           p.idesc | ((uint32_t)ks << 4) | ((uint32_t)ks << 29), sfa, sfb,
+                                           (kb | ks) != 0 ? 1u : 0u);
+                    }
                     tc_commit_pair_multicast(empty_bar(stage), 0x3);
                     if (++stage == kMxStages) {
                         stage = 0;
@@ -364,8 +384,8 @@ __global__ void __launch_bounds__(256) k_mx_stage_a(const uint8_t* __restrict__ 
 }
 
 // B8^T [Np][Kp] <- transpose of B [K][N] (row stride ldb bytes), zero past K or N.
-// 64 (k) x 224 (n) tiles (a whole N tile of the main kernel, so each B row
-// piece read is 224 bytes long), 224 threads.  Loads: four 16-byte row pieces
+// 64 (k) x 208 (n) tiles (a whole N tile of the main kernel, so each B row
+// piece read is 208 bytes long), 208 threads.  Loads: four 16-byte row pieces
 // per thread into shared words; stores: each thread reads a 16 (k) x 4 (n)
 // block as sixteen words, transposes its four 4 x 4 byte blocks with byte
 // permutes and writes four 16-byte vectors (one per n row).
@@ -422,7 +442,7 @@ __global__ void __launch_bounds__(kBtThreads) k_mx_stage_bt(const uint8_t* __res
 //  SB8 chunk (t, kb), 4 KB in the source form of tcgen05.cp 128x256b (row r to
 //    lane r, 8 columns of 4 step bytes; byte b of row r at (r / 8) * 256 +
 //    (b / 16) * 128 + (r % 8) * 16 + b % 16): every lane quarter alike, row
-//    32 q + i column c holding the scales of B column 224 t + 32 c + i.
+//    32 q + i column c holding the scales of B column 208 t + 32 c + i.
 // 127 (= 2^0) past the extents: those operand codes are zero.  One 16-byte
 // store per task.
 __global__ void __launch_bounds__(256) k_mx_stage_scales(const uint8_t* __restrict__ SA, int64_t ld_sa,
