@@ -107,6 +107,19 @@ def test_many_tiles_per_block(ctx):
     assert rel_fro(got, ref_b) <= TOL
 
 
+@pytest.mark.parametrize("N", [2305, 2320, 2500])
+def test_pair_kernel_last_n_tile_widths(ctx, N):
+    """CTA-pair kernel (9 x 10 tiles of 256 x 256) whose last N tile holds 1, 16 or 196
+    valid columns: the ragged N tail of the pair layout (B split between the two CTAs)."""
+    M, K = 2304, 96
+    g = wl.gemm_bf16(M=M, N=N, K=K, tag=12)
+    got, _ = run_gemm(ctx, g, "bf16")
+    ref = oracle.gemm_f64(g["A"], g["lda"], g["B"], g["ldb"], M, N, K)
+    ref_b = synth.bf16_bits_to_f32(oracle.round_bf16(ref)).astype(np.float64)
+    assert rel_fro(got, ref_b) <= TOL
+    assert rel_fro(got[:, -(N % 256):], ref_b[:, -(N % 256):]) <= TOL  # the tail tile on its own
+
+
 def test_config_1000_full(ctx):
     g = wl.gemm_bf16(M=1000, N=1000, K=1000)
     got, _ = run_gemm(ctx, g, "bf16")
