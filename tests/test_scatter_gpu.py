@@ -63,6 +63,12 @@ CASES = [
     (300, 64, 64, 64, 64, -8, 3, 64),     # columns clipped on the left
     (300, 61, 64, 64, 64, 0, -2, 0),      # partial last vector, no mask
     (300, 50, 53, 37, 41, 5, 0, 37),      # unaligned everything
+    # masked rows through the bulk ring: destination units not 4-byte aligned (bf16), odd clips
+    (300, 64, 72, 64, 64, 3, 0, 64),      # odd column offset, right clip
+    (300, 64, 65, 64, 64, 0, 0, 64),      # odd destination stride
+    (300, 61, 64, 64, 64, -2, 0, 64),     # left clip by a whole unit, right clip inside one
+    (300, 60, 64, 64, 64, -3, 5, 64),     # odd left clip
+    (300, 16, 16, 16, 16, 0, 0, 16),      # narrow rows: a block step spans many rows
 ]
 
 
