@@ -185,8 +185,14 @@ def dev_bytes(a: np.ndarray):
     return torch.from_numpy(flat).to("cuda")
 
 
+GATE_CYCLES = 400_000  # ~0.2 ms of device-side spin at 2 GHz
+
+
 def time_launches(fn, reps: int, warmup: int = 3, flush=None):
-    """Median and mean device time (ms) of fn() over reps, CUDA events on the current stream."""
+    """Median, mean and best device time (ms) of one fn() call over reps, CUDA events on
+    the current stream.  Each timed call is queued behind a short device-side spin
+    (torch.cuda._sleep), so the host's own work for the call (binding, argument checks,
+    launches) overlaps the spin and the events see the call's device work alone."""
     import torch
     for _ in range(warmup):
         fn()
@@ -195,6 +201,7 @@ def time_launches(fn, reps: int, warmup: int = 3, flush=None):
     for _ in range(reps):
         if flush is not None:
             flush()
+        torch.cuda._sleep(GATE_CYCLES)
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record()
