@@ -79,23 +79,24 @@ __device__ __forceinline__ void st_elem(char* base, int64_t off, typename sbt_el
     reinterpret_cast<typename sbt_elem<ES>::T*>(base)[off] = v;
 }
 
-__device__ __forceinline__ uint32_t pick8(const uint32_t (&w)[8], uint32_t i) {
-    uint32_t r = w[0];
-#pragma unroll
-    for (uint32_t k = 1; k < 8; ++k) r = (i == k) ? w[k] : r;
-    return r;
+__device__ __forceinline__ uint32_t sel4(uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint32_t q) {
+    return q == 0 ? a : q == 1 ? b : q == 2 ? c : d;
 }
 
-// Bytes [s, s + 16) of the 32 bytes (lo, hi), 0 < s < 16.
-__device__ __forceinline__ uint4 realign16(const uint4& lo, const uint4& hi, uint32_t s) {
-    const uint32_t w[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
-    const uint32_t q = s >> 2, b = (s & 3u) * 8u;
-    uint4 r;
-    r.x = __funnelshift_r(pick8(w, q), pick8(w, q + 1), b);
-    r.y = __funnelshift_r(pick8(w, q + 1), pick8(w, q + 2), b);
-    r.z = __funnelshift_r(pick8(w, q + 2), pick8(w, q + 3), b);
-    r.w = __funnelshift_r(pick8(w, q + 3), pick8(w, q + 4), b);
-    return r;
+// Bytes [d, d + 16) of the 32 bytes (lo, hi) for an even d, 0 < d < 16: word
+// selects, then (2-byte elements only) one 16-bit funnel shift per word.
+template <int ES>
+__device__ __forceinline__ uint4 realign16_even(const uint4& lo, const uint4& hi, uint32_t d) {
+    const uint32_t q = d >> 2;
+    const uint32_t s0 = sel4(lo.x, lo.y, lo.z, lo.w, q);
+    const uint32_t s1 = sel4(lo.y, lo.z, lo.w, hi.x, q);
+    const uint32_t s2 = sel4(lo.z, lo.w, hi.x, hi.y, q);
+    const uint32_t s3 = sel4(lo.w, hi.x, hi.y, hi.z, q);
+    if (ES == 4) return make_uint4(s0, s1, s2, s3);
+    const uint32_t s4 = sel4(hi.x, hi.y, hi.z, hi.w, q);
+    const uint32_t b = (d & 2u) * 8u;  // 0 or 16 bits
+    return make_uint4(__funnelshift_r(s0, s1, b), __funnelshift_r(s1, s2, b), __funnelshift_r(s2, s3, b),
+                      __funnelshift_r(s3, s4, b));
 }
 
 // One 16-byte vector of array row r starting at column c (the whole vector in bounds).
@@ -110,7 +111,7 @@ __device__ __forceinline__ uint4 load_row_vector(const TileParams& p, int64_t r,
     if (base >= p.arr_lo && base + 32 <= p.arr_hi) {
         const uint4 lo = sbt_ld_nc_v4_l1(reinterpret_cast<const void*>(base));
         const uint4 hi = sbt_ld_nc_v4_l1(reinterpret_cast<const void*>(base + 16));
-        return realign16(lo, hi, s);
+        return realign16_even<ES>(lo, hi, s);
     }
     uint4 v = make_uint4(0, 0, 0, 0);
 #pragma unroll
@@ -121,7 +122,11 @@ __device__ __forceinline__ uint4 load_row_vector(const TileParams& p, int64_t r,
 template <int ES, int MODE>
 __global__ void __launch_bounds__(kThreads) k_tile_load(const TileParams p) {
     constexpr int V = 16 / ES;
-    constexpr int U = MODE == kElem ? 8 : 4;
+    // Vectors per thread and loop trip: one.  With more, the realign path's
+    // chunk pairs overflow L1 before neighbouring lanes reuse them (unaligned fp32
+    // 16,381 x 16,411: 0.373 ms at 1, 0.400 at 2, 0.427 at 4, 0.486 at 8), and the
+    // aligned path gains nothing either (0.349 / 0.351 / 0.357 ms at 1 / 2 / 4).
+    constexpr int U = MODE == kElem ? 8 : 1;
     typedef typename sbt_elem<ES>::T T;
     const uint32_t stride = gridDim.x * kThreads;
     for (uint32_t base = blockIdx.x * kThreads + threadIdx.x; base < p.ntasks; base += stride * U) {
@@ -180,7 +185,7 @@ __global__ void __launch_bounds__(kThreads) k_tile_load(const TileParams p) {
 template <int ES>
 __global__ void __launch_bounds__(kThreads) k_tile_store(const TileParams p) {
     constexpr int V = 16 / ES;
-    constexpr int U = 4;
+    constexpr int U = 1;  // vectors per thread and trip (aligned fp32 store: 0.337 ms at 1, 0.351 at 2, 0.354 at 4, 0.365 at 8)
     const uint32_t stride = gridDim.x * kThreads;
     for (uint32_t base = blockIdx.x * kThreads + threadIdx.x; base < p.ntasks; base += stride * U) {
         uint4 val[U];
@@ -214,7 +219,11 @@ __global__ void __launch_bounds__(kThreads) k_tile_store(const TileParams p) {
 // its in-bounds row range and each lane's column test are worked out once
 // per tile, so a row costs a few address additions; rows outside the array
 // are not visited.  (One task per element, each decoding its own tile, row and
-// column, was instruction-bound at 0.62 ms on the unaligned fp32 workload.)
+// column, was instruction-bound at 0.62 ms on the unaligned fp32 workload.
+// A vector kernel that passed each tile vector one lane up and wrote aligned
+// 16-byte destination chunks, the row ends element by element, took 0.70 ms
+// there: its many partial-sector writes cost more than this kernel's 4-byte
+// ones.)
 template <int ES>
 __global__ void __launch_bounds__(kThreads) k_tile_store_rows(const TileParams p, uint32_t ntiles) {
     typedef typename sbt_elem<ES>::T T;

@@ -110,6 +110,12 @@ STORE_CASES = [
     (30, 20, 24, 1, (-100, -100), (64, 64), (2, 2), (8, 8)),  # wholly outside: writes nothing
     (70, 72, 80, 1, (0, 0), (64, 32), (2, 3), (64, 32)),        # TMA store, partial edge tiles
     (70, 72, 80, 1, (3, 40), (34, 24), (3, 2), (32, 16)),       # TMA store, gaps, rows and columns past the end
+    # unaligned destination rows (every row offset mod 16), tile rows of 1 to 32 vectors
+    (65, 73, 73, 1, (0, 0), (64, 32), (2, 3), (64, 32)),        # every row offset mod 16, partial edge tiles
+    (50, 70, 71, 1, (-3, -5), (16, 16), (4, 5), (16, 16)),      # negative origin, odd column steps
+    (40, 300, 301, 1, (1, 3), (8, 128), (5, 3), (8, 128)),      # 32 (fp32) / 16 (bf16) vectors per tile row
+    (33, 37, 37, 1, (0, 1), (3, 8), (11, 5), (3, 8)),           # 2 (fp32) / 1 (bf16) vectors per tile row
+    (40, 100, 101, 1, (0, 0), (8, 48), (5, 3), (8, 48)),        # 12 / 6 vectors per row: element rows
 ]
 
 
