@@ -20,6 +20,9 @@ namespace {
 constexpr int kThreads = 256;
 constexpr int kChunkRows = 32;
 constexpr int kUnroll = 8;
+// Vector gather: one 16-byte vector per thread and trip.  Measured on the 1 KiB
+// bf16 rows of the headline gather: 0.322 ms at 1, 0.341 at 2, 0.333 at 8.
+constexpr int kGatherVecUnroll = 1;
 
 enum MaskMode { kNoMask = 0, kMaskVec = 1, kMaskBytes = 2 };
 
@@ -151,10 +154,10 @@ __global__ void __launch_bounds__(kThreads) k_gather_rows(const RowParams p) {
         if (VEC) {
             const int nvec = p.nvec;
             const int ntask = nrows * nvec;
-            for (int base = threadIdx.x; base < ntask; base += kThreads * kUnroll) {
-                uint4 val[kUnroll];
+            for (int base = threadIdx.x; base < ntask; base += kThreads * kGatherVecUnroll) {
+                uint4 val[kGatherVecUnroll];
 #pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
+                for (int u = 0; u < kGatherVecUnroll; ++u) {
                     const int t = base + u * kThreads;
                     if (t < ntask) {
                         const int row = t / nvec;
@@ -163,7 +166,7 @@ __global__ void __launch_bounds__(kThreads) k_gather_rows(const RowParams p) {
                     }
                 }
 #pragma unroll
-                for (int u = 0; u < kUnroll; ++u) {
+                for (int u = 0; u < kGatherVecUnroll; ++u) {
                     const int t = base + u * kThreads;
                     if (t < ntask) {
                         const int row = t / nvec;
