@@ -407,12 +407,14 @@ __global__ void __launch_bounds__(kThreads) k_scatter_add_rows(const RowParams p
         const uint32_t valid = s_valid[buf];
         const int64_t* rows_of = s_row[buf];
         const int per_row = VEC ? p.nvec : p.tile_c;
+        // vectors: one per thread and trip (bf16 1 KiB rows: 0.466 ms at 1, 0.484 at 2, 0.486 at 8)
+        constexpr int UA = VEC ? 1 : kUnroll;
         const int ntask = nrows * per_row;
-        for (int base = threadIdx.x; base < ntask; base += kThreads * kUnroll) {
-            uint4 val[kUnroll];
-            T sv[kUnroll];
+        for (int base = threadIdx.x; base < ntask; base += kThreads * UA) {
+            uint4 val[UA];
+            T sv[UA];
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
+            for (int u = 0; u < UA; ++u) {
                 const int t = base + u * kThreads;
                 if (t < ntask) {
                     const int row = t / per_row;
@@ -426,7 +428,7 @@ __global__ void __launch_bounds__(kThreads) k_scatter_add_rows(const RowParams p
                 }
             }
 #pragma unroll
-            for (int u = 0; u < kUnroll; ++u) {
+            for (int u = 0; u < UA; ++u) {
                 const int t = base + u * kThreads;
                 if (t >= ntask) continue;
                 const int row = t / per_row;
