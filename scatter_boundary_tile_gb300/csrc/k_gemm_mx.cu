@@ -388,8 +388,12 @@ __global__ void __launch_bounds__(256) k_mx_stage_a(const uint8_t* __restrict__ 
 // piece read is 208 bytes long), 208 threads.  Loads: four 16-byte row pieces
 // per thread into shared words; stores: each thread reads a 16 (k) x 4 (n)
 // block as sixteen words, transposes its four 4 x 4 byte blocks with byte
-// permutes and writes four 16-byte vectors (one per n row).
-constexpr int kBtK = 64, kBtN = MX_BN, kBtThreads = (kBtN / 4) * (kBtK / 16), kBtPitch = kBtN / 4 + 1;
+// permutes and writes four 16-byte vectors (one per n row).  The four threads
+// of an n group are adjacent lanes, so each row's 64 bytes leave in one warp
+// store as two whole sectors; rows k >= 32 of the shared tile sit 8 words to
+// the right, which with the odd pitch puts the four k quarters a warp reads in
+// four different bank octets.
+constexpr int kBtK = 64, kBtN = MX_BN, kBtThreads = (kBtN / 4) * (kBtK / 16), kBtPitch = kBtN / 4 + 9;
 static_assert(kBtK * kBtN / 16 % kBtThreads == 0, "load split");
 template <bool P4>
 __global__ void __launch_bounds__(kBtThreads) k_mx_stage_bt(const uint8_t* __restrict__ B, int64_t ldb, int K, int N,
@@ -403,20 +407,21 @@ __global__ void __launch_bounds__(kBtThreads) k_mx_stage_bt(const uint8_t* __res
         const int k = k0 + kk, n = n0 + nh;
         uint64_t lo = 0, hi = 0;
         if (k < K && n < N) load16_codes<P4>(B + (P4 ? (int64_t)k * ldb / 2 : (int64_t)k * ldb), n, N - n, &lo, &hi);
-        uint32_t* w = &t[kk][nh >> 2];
+        uint32_t* w = &t[kk][(nh >> 2) + ((kk >> 5) << 3)];
         w[0] = (uint32_t)lo;
         w[1] = (uint32_t)(lo >> 32);
         w[2] = (uint32_t)hi;
         w[3] = (uint32_t)(hi >> 32);
     }
     __syncthreads();
-    const int nw = threadIdx.x % (kBtN / 4), kv = (threadIdx.x / (kBtN / 4)) * 16;  // n = 4 nw .. + 3, k = kv .. + 15
+    const int nw = threadIdx.x >> 2, kv = (threadIdx.x & 3) * 16;  // n = 4 nw .. + 3, k = kv .. + 15
+    const int col = nw + ((kv >> 5) << 3);
     if (k0 + kv >= Kp) return;
     uint32_t out[4][4];  // out[j][g]: bytes k = kv + 4 g .. + 3 of row n = 4 nw + j
 #pragma unroll
     for (int g = 0; g < 4; ++g) {
-        const uint32_t w0 = t[kv + 4 * g][nw], w1 = t[kv + 4 * g + 1][nw];
-        const uint32_t w2 = t[kv + 4 * g + 2][nw], w3 = t[kv + 4 * g + 3][nw];
+        const uint32_t w0 = t[kv + 4 * g][col], w1 = t[kv + 4 * g + 1][col];
+        const uint32_t w2 = t[kv + 4 * g + 2][col], w3 = t[kv + 4 * g + 3][col];
         const uint32_t a0 = __byte_perm(w0, w1, 0x5140), a1 = __byte_perm(w0, w1, 0x7362);
         const uint32_t a2 = __byte_perm(w2, w3, 0x5140), a3 = __byte_perm(w2, w3, 0x7362);
         out[0][g] = __byte_perm(a0, a2, 0x5410);
