@@ -39,14 +39,19 @@ constexpr int BM = 128, BN = 256, BK = 64;
 constexpr int kStages = 4;
 constexpr int kGemmThreads = 192;  // warp 0: TMA, warp 1: MMA, warps 2..5: epilogue
 constexpr uint32_t kABytes = BM * BK * 2;
-constexpr uint32_t kBBytes = BN * BK * 2;
-constexpr uint32_t kStageBytes = kABytes + kBBytes;
 constexpr int kEpiWarps = 4;
 constexpr int kEpiWords = 32 * 33;  // per-warp 32x32 transpose buffer, padded rows
-constexpr uint32_t kTmemCols = 2 * BN;
 constexpr int kNumBars = 2 * kStages + 5;
-constexpr size_t kGemmSmem = 1024 + (size_t)kStages * kStageBytes + (size_t)kEpiWarps * kEpiWords * 4 +
-                             kNumBars * 8 + 16;
+// Single-CTA kernel with BM x BN_ tiles (BN_ = 256, 128 or 64: narrower tiles
+// spread a small problem over more SMs).
+template <int BN_>
+struct TcShape {
+    static constexpr uint32_t kBBytes = BN_ * BK * 2;
+    static constexpr uint32_t kStageBytes = kABytes + kBBytes;  // a multiple of 1024: swizzle atoms stay aligned
+    static constexpr uint32_t kTmemCols = 2 * BN_;              // two accumulators; a power of two >= 32
+    static constexpr size_t kSmem =
+        1024 + (size_t)kStages * kStageBytes + (size_t)kEpiWarps * kEpiWords * 4 + kNumBars * 8 + 16;
+};
 
 enum : unsigned int { kCodeProducer = 0x100, kCodeMma = 0x200, kCodeEpilogue = 0x400, kCodeTeardown = 0x800 };
 
@@ -78,14 +83,15 @@ __device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, 
     *nt = within / gm;
 }
 
-// Drain one 128 x BN accumulator from TMEM (this warp's 32-lane quarter `q`),
+// Drain one 128 x BN_ accumulator from TMEM (this warp's 32-lane quarter `q`),
 // round (or keep fp32) and store rows row0.. of C through a padded shared
 // transpose so that each store instruction covers 32 consecutive columns.
 // A bf16 C is rounded before the transpose, which then moves half the bytes
 // (shared memory is the resource the main loop competes for).
+template <int BN_>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tmem_acc, int q, int lane, float* buf,
                                               int row0, int n0) {
-    const int n_valid = min(BN, p.N - n0);
+    const int n_valid = min(BN_, p.N - n0);
     const int chunks = (n_valid + 31) / 32;
     for (int c = 0; c < chunks; ++c) {
         uint32_t r[32];
@@ -131,9 +137,13 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tmem
     }
 }
 
+template <int BN_>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     k_gemm_bf16_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p) {
+    typedef TcShape<BN_> S;
+    constexpr uint32_t kStageBytes = S::kStageBytes;
+    constexpr uint32_t kTmemCols = S::kTmemCols;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float* epi = reinterpret_cast<float*>(smem + (size_t)kStages * kStageBytes);
@@ -204,7 +214,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
                     tma_load_2d(sa, &tmA, kb * BK, mt * BM, full_bar(stage));
-                    tma_load_2d(sa + kABytes, &tmB, kb * BK, nt * BN, full_bar(stage));
+                    tma_load_2d(sa + kABytes, &tmB, kb * BK, nt * BN_, full_bar(stage));
                     ++issued;
                     if (++stage == kStages) {
                         stage = 0;
@@ -239,7 +249,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 const uint32_t use = (uint32_t)(local >> 1);
                 int mt_unused, nt;
                 tile_coords(tile, p.m_tiles, p.n_tiles, &mt_unused, &nt);
-                const int n_valid = min(BN, p.N - nt * BN);
+                const int n_valid = min(BN_, p.N - nt * BN_);
                 const uint32_t idesc = idesc_bf16_f32(BM, (uint32_t)((n_valid + 15) & ~15));
                 if (!mbar_wait_bounded(tempty_bar(acc), (use & 1u) ^ 1u, p.wait_ns, abort_flag, p.status,
                                        kCodeMma)) {
@@ -247,7 +257,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     break;
                 }
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN);
+                const uint32_t d_tmem = tmem_base + (uint32_t)(acc * BN_);
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!mbar_wait_bounded(full_bar(stage), phase, p.wait_ns, abort_flag, p.status, kCodeMma)) {
                         ok = false;
@@ -292,7 +302,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 tile_coords(tile, p.m_tiles, p.n_tiles, &mt, &nt);
             if (!mbar_wait_bounded(tfull_bar(acc), use & 1u, p.wait_ns, abort_flag, p.status, kCodeEpilogue)) break;
             tc_fence_after();
-            epilogue_tile(p, tmem_base + (uint32_t)(acc * BN), q, lane, buf, mt * BM + q * 32, nt * BN);
+            epilogue_tile<BN_>(p, tmem_base + (uint32_t)(acc * BN_), q, lane, buf, mt * BM + q * 32, nt * BN_);
             tc_fence_before();
             mbar_arrive(tempty_bar(acc));
         }
@@ -323,6 +333,7 @@ constexpr int kStages2 = 3;
 constexpr uint32_t kHalfBytes = 128 * BK * 2;          // A rows or B rows of one CTA, one K step
 constexpr int kKB2 = 2;                                // K steps per stage
 constexpr uint32_t kStageBytes2 = 2 * kKB2 * kHalfBytes;  // per CTA: A atoms, then B atoms
+constexpr uint32_t kTmemCols2 = 2 * BN;                    // two 128 x 256 accumulators per CTA
 constexpr int kNumBars2 = 2 * kStages2 + 5;
 constexpr size_t kGemmSmem2 = 1024 + (size_t)kStages2 * kStageBytes2 + (size_t)kEpiWarps * kEpiWords * 4 +
                               kNumBars2 * 8 + 16;
@@ -365,7 +376,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
         prefetch_tmap(&tmB);
     }
     if (warp == 1) {
-        tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols);
+        tmem_alloc_pair(smem_u32(tmem_slot), kTmemCols2);
         tmem_relinquish_pair();
     }
     tc_fence_before();
@@ -474,7 +485,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                 tile_coords(tile, p.m_tiles, p.n_tiles, &mt, &nt);
             if (!mbar_wait_bounded(tfull_bar(acc), use & 1u, p.wait_ns, abort_flag, p.status, kCodeEpilogue)) break;
             tc_fence_after();
-            epilogue_tile(p, tmem_base + (uint32_t)(acc * BN), q, lane, buf, mt * 256 + (int)rank * 128 + q * 32,
+            epilogue_tile<BN>(p, tmem_base + (uint32_t)(acc * BN), q, lane, buf, mt * 256 + (int)rank * 128 + q * 32,
                           nt * BN);
             tc_fence_before();
             mbar_arrive_cluster(leader_tempty0 + 8u * acc);
@@ -486,7 +497,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     cluster_sync();  // the leader's MMAs into the peer's TMEM are complete before either CTA frees it
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc_pair(tmem_base, kTmemCols);
+        tmem_dealloc_pair(tmem_base, kTmemCols2);
     }
 }
 
@@ -655,12 +666,20 @@ sbt_status sbt_launch_gemm_main(sbt_context* ctx, const uint16_t* Ap, const uint
                                 int64_t N, int64_t K, cudaStream_t stream) {
     // 2. tensor-core main kernel
     // CTA pairs when there are at least as many 256 x 256 tiles as SM pairs;
-    // single CTAs (128 x 256 tiles) for smaller problems.
+    // single CTAs for smaller problems, with 128 x 256 tiles when those give
+    // three quarters of the SMs work, else 128 x 128 or 128 x 64 tiles.
     const bool pair = ctx->sm_count >= 2 && (d.Mp / 256) * (d.Np / 256) >= ctx->sm_count / 2;
+    const int64_t m_tiles1 = sbt_cdiv(M, BM);
+    int bn1 = 64;
+    for (int w : {256, 128})
+        if (m_tiles1 * sbt_cdiv(N, w) * 4 >= (int64_t)ctx->sm_count * 3) {
+            bn1 = w;
+            break;
+        }
     CUtensorMap tmA, tmB;
     sbt_status st = encode_kmajor(ctx, &tmA, (void*)Ap, d.Mp, d.Kp, BM);
     if (st) return st;
-    if ((st = encode_kmajor(ctx, &tmB, (void*)Bp, d.Np, d.Kp, pair ? 128 : BN))) return st;
+    if ((st = encode_kmajor(ctx, &tmB, (void*)Bp, d.Np, d.Kp, pair ? 128 : bn1))) return st;
     GemmParams p;
     p.C = (char*)C;
     p.ldc = ldc;
@@ -678,7 +697,14 @@ sbt_status sbt_launch_gemm_main(sbt_context* ctx, const uint16_t* Ap, const uint
     p.withhold_first_load = ctx->test_hook == SBT_TEST_WITHHOLD_LOAD;
     static bool attr_set[64] = {false};
     if (!attr_set[ctx->device & 63]) {
-        cudaError_t e = cudaFuncSetAttribute(k_gemm_bf16_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem);
+        cudaError_t e = cudaFuncSetAttribute(k_gemm_bf16_tc<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)TcShape<256>::kSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_gemm_bf16_tc<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)TcShape<128>::kSmem);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_gemm_bf16_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)TcShape<64>::kSmem);
         if (e != cudaSuccess) return sbt_cuda_check(e, "cudaFuncSetAttribute(gemm smem)");
         e = cudaFuncSetAttribute(k_gemm_bf16_tc_pair, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem2);
         if (e != cudaSuccess) return sbt_cuda_check(e, "cudaFuncSetAttribute(gemm pair smem)");
@@ -712,8 +738,16 @@ sbt_status sbt_launch_gemm_main(sbt_context* ctx, const uint16_t* Ap, const uint
         k_gemm_bf16_tc_pair<<<2 * clusters, kGemmThreads, kGemmSmem2, stream>>>(tmA, tmB, p);
         return sbt_after_launch(ctx, "gemm_bounded (tcgen05, CTA pairs)");
     }
+    // single CTAs: only the tiles that hold rows < M and columns < N
+    p.m_tiles = (int)m_tiles1;
+    p.n_tiles = (int)sbt_cdiv(N, bn1);
     const int tiles = p.m_tiles * p.n_tiles;
     const int grid = std::min(tiles, ctx->sm_count);
-    k_gemm_bf16_tc<<<grid, kGemmThreads, kGemmSmem, stream>>>(tmA, tmB, p);
+    if (bn1 == 256)
+        k_gemm_bf16_tc<256><<<grid, kGemmThreads, TcShape<256>::kSmem, stream>>>(tmA, tmB, p);
+    else if (bn1 == 128)
+        k_gemm_bf16_tc<128><<<grid, kGemmThreads, TcShape<128>::kSmem, stream>>>(tmA, tmB, p);
+    else
+        k_gemm_bf16_tc<64><<<grid, kGemmThreads, TcShape<64>::kSmem, stream>>>(tmA, tmB, p);
     return sbt_after_launch(ctx, "gemm_bounded (tcgen05)");
 }

@@ -120,6 +120,24 @@ def test_pair_kernel_last_n_tile_widths(ctx, N):
     assert rel_fro(got[:, -(N % 256):], ref_b[:, -(N % 256):]) <= TOL  # the tail tile on its own
 
 
+@pytest.mark.parametrize("mnk", [(2048, 1800, 96), (1000, 2000, 96), (1000, 1000, 96), (300, 250, 70),
+                                 (129, 1000, 130)])
+def test_single_cta_tile_widths(ctx, mnk):
+    """Single-CTA kernel at the tile widths it picks for problems too small for CTA pairs:
+    128 x 256 tiles (2048 x 1800), 128 x 128 (1000 x 2000) and 128 x 64 (the rest, on a
+    148- or 152-SM part), with ragged last M and N tiles; the last N tile is also checked
+    on its own."""
+    M, N, K = mnk
+    g = wl.gemm_bf16(M=M, N=N, K=K, tag=13)
+    got, _ = run_gemm(ctx, g, "bf16")
+    ref = oracle.gemm_f64(g["A"], g["lda"], g["B"], g["ldb"], M, N, K)
+    ref_b = synth.bf16_bits_to_f32(oracle.round_bf16(ref)).astype(np.float64)
+    assert rel_fro(got, ref_b) <= TOL
+    tail = N % 64 or 64
+    assert rel_fro(got[:, -tail:], ref_b[:, -tail:]) <= TOL
+    assert rel_fro(got[-(M % 128 or 128):], ref_b[-(M % 128 or 128):]) <= TOL
+
+
 def test_config_1000_full(ctx):
     g = wl.gemm_bf16(M=1000, N=1000, K=1000)
     got, _ = run_gemm(ctx, g, "bf16")
