@@ -156,8 +156,15 @@ __global__ void __launch_bounds__(kThreads) k_tile_load(const TileParams p) {
                 }
             }
 #pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (lin[u] >= 0) sbt_st_v4(p.tiles_w + lin[u] * 16, val[u]);
+            for (int u = 0; u < U; ++u) {
+                if (lin[u] < 0) continue;
+                // aligned path: streaming stores (tiles not read again here; 0.349 -> 0.337 ms on the
+                // 16,384 x 16,416 fp32 grid); the realign path measured 2% slower with them
+                if (MODE == kAligned)
+                    sbt_st_v4_cs(p.tiles_w + lin[u] * 16, val[u]);
+                else
+                    sbt_st_v4(p.tiles_w + lin[u] * 16, val[u]);
+            }
         } else {
             T val[U];
             int64_t lin[U];
