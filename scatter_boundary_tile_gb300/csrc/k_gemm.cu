@@ -184,6 +184,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Set-up above overlaps the end of the staging kernel ahead in the stream (launched as a
+    // programmatic dependent); from here on the staged operands are read and C is written.
+    griddep_wait();
     const int num_tiles = p.m_tiles * p.n_tiles;
 
     if (warp == 0) {
@@ -383,6 +386,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     cluster_sync();  // both CTAs' barriers are initialised before any remote arrival
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Set-up above overlaps the end of the staging kernel ahead in the stream (launched as a
+    // programmatic dependent); from here on the staged operands are read and C is written.
+    griddep_wait();
     const int num_tiles = p.m_tiles * p.n_tiles;  // 256 x 256 tiles
 
     if (warp == 0) {
@@ -735,7 +741,9 @@ sbt_status sbt_launch_gemm_main(sbt_context* ctx, const uint16_t* Ap, const uint
             max_clusters[ctx->device & 63] = n;
         }
         const int clusters = std::min(tiles, max_clusters[ctx->device & 63]);
-        k_gemm_bf16_tc_pair<<<2 * clusters, kGemmThreads, kGemmSmem2, stream>>>(tmA, tmB, p);
+        const cudaError_t e = sbt_launch_dependent(k_gemm_bf16_tc_pair, dim3(2 * clusters), dim3(kGemmThreads),
+                                                   kGemmSmem2, stream, tmA, tmB, p);
+        if (e != cudaSuccess) return sbt_cuda_check(e, "gemm_bounded (tcgen05, CTA pairs)");
         return sbt_after_launch(ctx, "gemm_bounded (tcgen05, CTA pairs)");
     }
     // single CTAs: only the tiles that hold rows < M and columns < N
@@ -743,11 +751,16 @@ sbt_status sbt_launch_gemm_main(sbt_context* ctx, const uint16_t* Ap, const uint
     p.n_tiles = (int)sbt_cdiv(N, bn1);
     const int tiles = p.m_tiles * p.n_tiles;
     const int grid = std::min(tiles, ctx->sm_count);
+    cudaError_t e;
     if (bn1 == 256)
-        k_gemm_bf16_tc<256><<<grid, kGemmThreads, TcShape<256>::kSmem, stream>>>(tmA, tmB, p);
+        e = sbt_launch_dependent(k_gemm_bf16_tc<256>, dim3(grid), dim3(kGemmThreads), TcShape<256>::kSmem, stream,
+                                 tmA, tmB, p);
     else if (bn1 == 128)
-        k_gemm_bf16_tc<128><<<grid, kGemmThreads, TcShape<128>::kSmem, stream>>>(tmA, tmB, p);
+        e = sbt_launch_dependent(k_gemm_bf16_tc<128>, dim3(grid), dim3(kGemmThreads), TcShape<128>::kSmem, stream,
+                                 tmA, tmB, p);
     else
-        k_gemm_bf16_tc<64><<<grid, kGemmThreads, TcShape<64>::kSmem, stream>>>(tmA, tmB, p);
+        e = sbt_launch_dependent(k_gemm_bf16_tc<64>, dim3(grid), dim3(kGemmThreads), TcShape<64>::kSmem, stream,
+                                 tmA, tmB, p);
+    if (e != cudaSuccess) return sbt_cuda_check(e, "gemm_bounded (tcgen05)");
     return sbt_after_launch(ctx, "gemm_bounded (tcgen05)");
 }

@@ -183,6 +183,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
     cluster_sync();  // both CTAs' barriers are initialised before any remote arrival
     tc_fence_after();
     const uint32_t tmem_base = *tmem_slot;
+    // Set-up above overlaps the end of the staging kernel ahead in the stream (launched as a
+    // programmatic dependent); from here on the staged operands are read and C is written.
+    griddep_wait();
     const int num_tiles = p.m_tiles * p.n_tiles;
 
     if (warp == 0) {
@@ -633,6 +636,8 @@ sbt_status sbt_launch_gemm_mx(sbt_context* ctx, int a_fmt, const void* A, int64_
     }
     const int tiles = p.m_tiles * p.n_tiles;
     const int clusters = std::min(tiles, max_clusters[dev]);
-    k_gemm_mx_pair<<<2 * clusters, kMxThreads, kMxSmem, stream>>>(tmA, tmB, tmSA, tmSB, p);
+    const cudaError_t e = sbt_launch_dependent(k_gemm_mx_pair, dim3(2 * clusters), dim3(kMxThreads), kMxSmem, stream,
+                                               tmA, tmB, tmSA, tmSB, p);
+    if (e != cudaSuccess) return sbt_cuda_check(e, "gemm_block_scaled (tcgen05 block-scaled, CTA pairs)");
     return sbt_after_launch(ctx, "gemm_block_scaled (tcgen05 block-scaled, CTA pairs)");
 }

@@ -147,6 +147,26 @@ sbt_status sbt_launch_scatter_bulk(sbt_context* ctx, int es, void* dst, int64_t 
 // Checks the launch that was just enqueued and counts it.
 sbt_status sbt_after_launch(sbt_context* ctx, const char* what);
 
+// Enqueues `kern` as a programmatic dependent of the kernel ahead of it in the
+// stream: its blocks may start (and run their set-up) while that kernel drains;
+// the kernel itself must call griddep_wait() before it touches memory the
+// earlier kernel writes.  Cluster shapes come from the kernel's __cluster_dims__.
+template <typename... KArgs, typename... Args>
+cudaError_t sbt_launch_dependent(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                                 Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<Args&&>(args)...);
+}
+
 // ----------------------------------------------------------------------------
 // Device side: raw element types and 16-byte vector accesses
 // ----------------------------------------------------------------------------
