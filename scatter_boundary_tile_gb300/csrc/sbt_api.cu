@@ -195,6 +195,10 @@ sbt_status sbt_tile_store_clipped(sbt_context* ctx, sbt_dtype dtype, const void*
     SBT_REQUIRE(src_tiles && dst, "tile_store_clipped: NULL pointer");
     SBT_REQUIRE(stride_r != 0 && stride_c != 0, "tile_store_clipped: strides must be nonzero");
     if ((st = sbt_use_device(ctx))) return st;
+    if (sbt_tile_store_runs_ok(ctx, es, src_tiles, grid_r, grid_c, tile_r, tile_c, dst, stride_r, stride_c, origin_c,
+                               step_c))
+        return sbt_launch_tile_store_runs(ctx, es, src_tiles, grid_r, grid_c, tile_r, tile_c, dst, rows, cols,
+                                          stride_r, origin_r, origin_c, step_r, (cudaStream_t)stream);
     return sbt_launch_tile_store(ctx, es, src_tiles, grid_r, grid_c, tile_r, tile_c, dst, rows, cols, stride_r,
                                  stride_c, origin_r, origin_c, step_r, step_c, (cudaStream_t)stream);
 }

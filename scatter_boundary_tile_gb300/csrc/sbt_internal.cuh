@@ -65,6 +65,15 @@ sbt_status sbt_launch_tile_store(sbt_context* ctx, int es, const void* src_tiles
                                  int32_t tile_r, int32_t tile_c, void* dst, int64_t rows, int64_t cols,
                                  int64_t stride_r, int64_t stride_c, int64_t origin_r, int64_t origin_c,
                                  int64_t step_r, int64_t step_c, cudaStream_t stream);
+// Clipped store along whole destination runs when the destination rows are not
+// 16-byte aligned and the tiles sit side by side along the row (k_tiles_runs.cu).
+bool sbt_tile_store_runs_ok(sbt_context* ctx, int es, const void* src_tiles, int32_t grid_r, int32_t grid_c,
+                            int32_t tile_r, int32_t tile_c, const void* dst, int64_t stride_r, int64_t stride_c,
+                            int64_t origin_c, int64_t step_c);
+sbt_status sbt_launch_tile_store_runs(sbt_context* ctx, int es, const void* src_tiles, int32_t grid_r,
+                                      int32_t grid_c, int32_t tile_r, int32_t tile_c, void* dst, int64_t rows,
+                                      int64_t cols, int64_t stride_r, int64_t origin_r, int64_t origin_c,
+                                      int64_t step_r, cudaStream_t stream);
 sbt_status sbt_launch_gather(sbt_context* ctx, int es, const void* src, int64_t rows, int64_t cols, int64_t ld_src,
                              const int32_t* idx, int64_t n_idx, int64_t row_offset, int64_t col_offset,
                              int32_t tile_c, const uint8_t* mask, int64_t ld_mask, void* out, int64_t ld_out,

@@ -163,7 +163,7 @@ def test_validation(ctx):
                                         ((16381, 16411, 16416), "auto")])
 def test_large_fp32_grid(ctx, shape, path):
     """fp32 arrays over a ceil-div grid of 64 x 32 tiles: 16,381 x 16,411 with ld 16,411
-    (unaligned rows: realigned loads, element stores), 16,384 x 16,416 with ld 16,416 (16-byte
+    (unaligned rows: realigned loads, stores along whole destination rows), 16,384 x 16,416 with ld 16,416 (16-byte
     rows: vector or TMA tiles), and 16,381 x 16,411 with ld 16,416 (aligned rows, ragged edge)."""
     rows, cols, ld = shape
     a = synth.uniform_f32(205, (rows, ld), -1.0, 1.0)
