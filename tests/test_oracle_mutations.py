@@ -1,0 +1,136 @@
+"""Planted mistakes in the oracle fail its pins.
+
+Each case copies the oracle, the input generators and the pin tests into a
+scratch directory, plants one plausible mistake in the oracle's C source (a
+dropped bound, swapped strides, a truncated offset, pad replaced by data, an
+ignored mask, an off-by-one length, a transposed operand, a skipped term, the
+wrong rounding, a wrong format field), rebuilds that copy and runs
+tests/test_oracle_pins.py against it: every mutant must fail at least one pin.
+This is what makes the pins evidence: they are not the oracle's formulas
+typed twice.  Everything runs on the CPU; the repository's own oracle is not
+touched.
+"""
+import concurrent.futures
+import os
+import shutil
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+MUTATIONS = {
+    # gather (warp.tile_load_indexed, description)
+    "gather_row_bound_dropped": (
+        "if (m && r >= 0 && r < rows && c >= 0 && c < cols)\n                put(out, k * ld_out + j, es, at(src, r * ld_src + c, es));",
+        "if (m && r >= 0 && c >= 0 && c < cols)\n                put(out, k * ld_out + j, es, at(src, r * ld_src + c, es));"),
+    "gather_offset_in_32_bits": (
+        "int64_t ld_out, const void* pad) {\n    for (int64_t k = 0; k < n_idx; ++k) {\n        int64_t r = (int64_t)idx[k] + row_offset;",
+        "int64_t ld_out, const void* pad) {\n    for (int64_t k = 0; k < n_idx; ++k) {\n        int64_t r = (int32_t)((uint32_t)idx[k] + (uint32_t)row_offset);"),
+    "gather_pad_replaced_by_data": (
+        "                put(out, k * ld_out + j, es, pad);",
+        "                put(out, k * ld_out + j, es, at(src, 0, es));"),
+    "gather_mask_ignored": (
+        "            int m = mask ? (mask[k * ld_mask + j] != 0) : 1;\n            if (m && r >= 0 && r < rows && c >= 0 && c < cols)\n                put(out",
+        "            int m = 1;\n            if (m && r >= 0 && r < rows && c >= 0 && c < cols)\n                put(out"),
+    "gather_cols_row_and_column_swapped": (
+        "put(out, i * ld_out + k, es, at(src, r * ld_src + c, es));",
+        "put(out, i * ld_out + k, es, at(src, c * ld_src + r, es));"),
+    # padded load / clipped store (Tylo "Boundary tiles", cuTile "Memory")
+    "tile_load_strides_swapped": (
+        "put(dst, o, es, at(src, r * stride_r + c * stride_c, es));",
+        "put(dst, o, es, at(src, r * stride_c + c * stride_r, es));"),
+    "tile_load_column_bound_dropped": (
+        "if (r >= 0 && r < rows && c >= 0 && c < cols)\n                        put(dst, o, es, at(src",
+        "if (r >= 0 && r < rows && c >= 0)\n                        put(dst, o, es, at(src"),
+    "tile_store_writes_one_column_past": (
+        "if (r >= 0 && r < rows && c >= 0 && c < cols)\n                        put(dst, r * stride_r",
+        "if (r >= 0 && r < rows && c >= 0 && c <= cols)\n                        put(dst, r * stride_r"),
+    # masked scatter
+    "scatter_mask_ignored": (
+        "            int m = mask ? (mask[k * ld_mask + j] != 0) : 1;\n            if (m && r >= 0 && r < rows && c >= 0 && c < cols)\n                put(dst",
+        "            int m = 1;\n            if (m && r >= 0 && r < rows && c >= 0 && c < cols)\n                put(dst"),
+    # ragged load / store (Mojo "RaggedTMA3DTile")
+    "ragged_load_length_off_by_one": (
+        "if (r < len && row >= 0 && row < total_rows)\n                        put(out, o",
+        "if (r <= len && row >= 0 && row < total_rows)\n                        put(out, o"),
+    "ragged_load_head_and_row_strides_swapped": (
+        "put(out, o, es, at(x, row * ld_row + (int64_t)h * ld_head + d, es));",
+        "put(out, o, es, at(x, row * ld_head + (int64_t)h * ld_row + d, es));"),
+    "ragged_store_length_off_by_one": (
+        "if (r < len && row >= 0 && row < total_rows)\n                        put(x,",
+        "if (r <= len && row >= 0 && row < total_rows)\n                        put(x,"),
+    # gather backward
+    "scatter_add_overwrites": (
+        "float v = (float)((double)f32_of(d) + (double)f32_of(s));",
+        "float v = f32_of(s);"),
+    # GEMM and bf16 rounding
+    "gemm_a_transposed": (
+        "s += bf16_to_f64(A[m * lda + k]) * bf16_to_f64(B[k * ldb + n]);",
+        "s += bf16_to_f64(A[k * lda + m]) * bf16_to_f64(B[k * ldb + n]);"),
+    "gemm_skips_k0": (
+        "for (int64_t k = 0; k < K; ++k) s += bf16_to_f64(A[m * lda + k])",
+        "for (int64_t k = 1; k < K; ++k) s += bf16_to_f64(A[m * lda + k])"),
+    "bf16_ties_away_from_zero": (
+        "double q = rint(ldexp(x, -q_exp));",
+        "double q = round(ldexp(x, -q_exp));"),
+    "bf16_subnormal_clamp_dropped": (
+        "int q_exp = e - 8 > -133 ? e - 8 : -133;",
+        "int q_exp = e - 8;"),
+    # block-scaled GEMM (cuTile "Operations", muladd_scaled) and the 8-bit / 4-bit formats
+    "scale_indexed_by_k_mod_block": ("SA[m * ldsa + k / block]", "SA[m * ldsa + k % block]"),
+    "b_scale_transposed": ("SB[(k / block) * ldsb + n]", "SB[n * ldsb + k / block]"),
+    "e4m3_subnormal_exponent": (
+        "v = e == 0 ? ldexp((double)m, -9) : ldexp((double)(8 + m), e - 10);",
+        "v = e == 0 ? ldexp((double)m, -10) : ldexp((double)(8 + m), e - 10);"),
+    "e4m3_bias": (
+        "v = e == 0 ? ldexp((double)m, -9) : ldexp((double)(8 + m), e - 10);",
+        "v = e == 0 ? ldexp((double)m, -9) : ldexp((double)(8 + m), e - 11);"),
+    "e5m2_infinity_and_nan_swapped": (
+        "if (e == 31) return m ? NAN : (sign ? -INFINITY : INFINITY);",
+        "if (e == 31) return m ? (sign ? -INFINITY : INFINITY) : NAN;"),
+    "e2m1_nibble_order": (
+        "return oracle_fp8_decode(3, (uint8_t)(p[i >> 1] >> (4 * (i & 1))));",
+        "return oracle_fp8_decode(3, (uint8_t)(p[i >> 1] >> (4 * (1 - (i & 1)))));"),
+    "e8m0_bias": (
+        "if (fmt == 2) return b == 0xFF ? NAN : ldexp(1.0, (int)b - 127);",
+        "if (fmt == 2) return b == 0xFF ? NAN : ldexp(1.0, (int)b - 126);"),
+    "block_scaled_acc_dropped": (
+        "D[m * ldd + n] = s + (acc ? (double)acc[m * ld_acc + n] : 0.0);",
+        "D[m * ldd + n] = s;"),
+    "e4m3_nan_read_as_a_number": ("        if (e == 15 && m == 7) return NAN;\n", ""),
+    "e2m1_sign_ignored": ("        sign = (b >> 3) & 1;", "        sign = 0;"),
+}
+
+IGNORE = shutil.ignore_patterns("__pycache__", "*.tmp*")
+
+
+def run_mutant(base, name, old, new):
+    d = os.path.join(base, name)
+    shutil.copytree(os.path.join(ROOT, "oracle"), os.path.join(d, "oracle"),
+                    ignore=shutil.ignore_patterns("__pycache__", "*.so", "*.tmp*"))
+    shutil.copytree(os.path.join(ROOT, "synth"), os.path.join(d, "synth"), ignore=IGNORE)
+    os.makedirs(os.path.join(d, "tests"))
+    for f in ("conftest.py", "test_oracle_pins.py"):
+        shutil.copy(os.path.join(ROOT, "tests", f), os.path.join(d, "tests", f))
+    shutil.copytree(os.path.join(ROOT, "tests", "golden"), os.path.join(d, "tests", "golden"))
+    src = os.path.join(d, "oracle", "sbt_oracle.c")
+    s = open(src).read()
+    if s.count(old) != 1:
+        return "mutation site not found once"
+    open(src, "w").write(s.replace(old, new))
+    env = dict(os.environ, PYTHONPATH=d, CUDA_VISIBLE_DEVICES="")
+    r = subprocess.run([sys.executable, "-c", "import synth, oracle; synth.build(); oracle.build(force=True)"],
+                       cwd=d, env=env, capture_output=True, text=True, timeout=300)
+    if r.returncode:
+        return "does not compile: " + r.stderr[-300:]
+    r = subprocess.run([sys.executable, "-m", "pytest", "tests/test_oracle_pins.py", "-q", "-x", "-p",
+                        "no:cacheprovider"], cwd=d, env=env, capture_output=True, text=True, timeout=600)
+    return "caught" if r.returncode != 0 else "NOT CAUGHT"
+
+
+def test_every_planted_mistake_fails_a_pin(tmp_path):
+    with concurrent.futures.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 1)) as ex:
+        futs = {name: ex.submit(run_mutant, str(tmp_path), name, old, new) for name, (old, new) in MUTATIONS.items()}
+        results = {name: f.result() for name, f in futs.items()}
+    bad = {name: r for name, r in results.items() if r != "caught"}
+    assert not bad, bad

@@ -415,6 +415,19 @@ def test_ragged_store_clips_long_sequences_and_bad_metadata():
     assert np.all(x[10:12] == 0x1234)        # sequence 2's rows 4.. are past t_pad
 
 
+def test_ragged_store_leaves_rows_outside_every_sequence():
+    # Mojo "RaggedTMA3DTile", async_copy_from_col: only the first dynamic_dim rows of a tile are written.
+    # The packed buffer has 4 spare rows after the last sequence, and every tile row (also those past a
+    # sequence's length) holds data: only rows [cu[b], cu[b] + len_b) may change.
+    cu = np.array([0, 3, 3, 8], np.int32)  # lengths 3, 0, 5, all below t_pad = 6
+    tiles = synth.normal_bf16(45, (3, 2, 6, 4))
+    x = np.full((12, 2, 4), 0x1234, np.uint16)
+    oracle.ragged_tile_store(tiles, x, 12, 8, 4, cu)
+    np.testing.assert_array_equal(x[0:3], tiles[0, :, :3].transpose(1, 0, 2))
+    np.testing.assert_array_equal(x[3:8], tiles[2, :, :5].transpose(1, 0, 2))
+    assert np.all(x[8:12] == 0x1234)
+
+
 # ----------------------------------------------------------------------------- GEMM and bf16 rounding
 
 def _bits_of(vals):
