@@ -113,6 +113,19 @@ def test_store_fp32_strided_heads_and_bad_metadata(ctx):
     assert np.array_equal(got.view(np.uint32), want.view(np.uint32))
 
 
+def test_store_leaves_spare_rows_after_the_last_sequence(ctx):
+    # every tile row (also those past a length) holds data; the packed buffer has 6 spare rows
+    cu = np.array([0, 3, 3, 40, 45], np.int32)  # lengths 3, 0, 37, 5, all below t_pad = 48
+    total, H, D = 51, 2, 16
+    tiles = synth.normal_bf16(407, (4, H, 48, D))
+    x0 = np.full((total, H, D), 0xDEAD, np.uint16)
+    want = oracle.ragged_tile_store(tiles, x0.copy(), total, H * D, D, cu)
+    assert np.all(want[45:] == 0xDEAD)
+    for path in ("auto", "scalar"):
+        got = gpu_ragged_store(ctx, tiles, x0, total, H * D, D, cu, "bf16", path=path)
+        assert np.array_equal(got, want), path
+
+
 def test_store_round_trip(ctx):
     d = wl.ragged_bf16(batch=9, max_len=700, heads=8, depth=128)
     x, cu, total = d["x"], d["cu_seqlens"], d["total_rows"]
