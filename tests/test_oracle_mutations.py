@@ -99,7 +99,53 @@ MUTATIONS = {
         "D[m * ldd + n] = s;"),
     "e4m3_nan_read_as_a_number": ("        if (e == 15 && m == 7) return NAN;\n", ""),
     "e2m1_sign_ignored": ("        sign = (b >> 3) & 1;", "        sign = 0;"),
+    "e2m1_subnormal_value": (
+        "v = e == 0 ? 0.5 * m : ldexp((double)(2 + m), e - 2);",
+        "v = e == 0 ? 1.0 * m : ldexp((double)(2 + m), e - 2);"),
+    "e5m2_subnormal_exponent": (
+        "v = e == 0 ? ldexp((double)m, -16) : ldexp((double)(4 + m), e - 17);",
+        "v = e == 0 ? ldexp((double)m, -17) : ldexp((double)(4 + m), e - 17);"),
+    "a_scale_decoded_in_the_operand_format": (
+        "oracle_fp8_decode(sfmt, SA[m * ldsa + k / block])",
+        "oracle_fp8_decode(afmt, SA[m * ldsa + k / block])"),
+    # more movement mistakes
+    "gather_cols_column_bound_dropped": (
+        "if (r >= 0 && r < rows && c >= 0 && c < cols)\n                put(out, i * ld_out + k",
+        "if (r >= 0 && r < rows && c >= 0)\n                put(out, i * ld_out + k"),
+    "gather_cols_offset_ignored": (
+        "int64_t c = (int64_t)idx[k] + col_offset;",
+        "int64_t c = (int64_t)idx[k];"),
+    "scatter_row_bound_dropped": (
+        "if (m && r >= 0 && r < rows && c >= 0 && c < cols)\n                put(dst",
+        "if (m && r >= 0 && c >= 0 && c < cols)\n                put(dst"),
+    "scatter_source_transposed": (
+        "put(dst, r * ld_dst + c, es, at(src, k * ld_src + j, es));",
+        "put(dst, r * ld_dst + c, es, at(src, j * ld_src + k, es));"),
+    "tile_store_strides_swapped": (
+        "put(dst, r * stride_r + c * stride_c, es, at(src_tiles, o, es));",
+        "put(dst, r * stride_c + c * stride_r, es, at(src_tiles, o, es));"),
+    "ragged_load_packed_bound_dropped": (
+        "if (r < len && row >= 0 && row < total_rows)\n                        put(out, o",
+        "if (r < len && row >= 0)\n                        put(out, o"),
+    "scatter_add_column_bound_dropped": ("if (c < 0 || c >= cols) continue;", "if (c < 0) continue;"),
+    "scatter_add_f16_rounded_as_bf16": (
+        "out = f16_rne(f16_bits_f64(a) + f16_bits_f64(b));",
+        "out = oracle_bf16_rne(f16_bits_f64(a) + f16_bits_f64(b));"),
+    "f16_decode_subnormal_exponent": (
+        "double v = e == 0 ? ldexp((double)m, -24) : (e == 31",
+        "double v = e == 0 ? ldexp((double)m, -25) : (e == 31"),
+    "gemm_spot_check_indices_swapped": (
+        "bf16_to_f64(A[ms[t] * lda + k]) * bf16_to_f64(B[k * ldb + ns[t]])",
+        "bf16_to_f64(A[ns[t] * lda + k]) * bf16_to_f64(B[k * ldb + ms[t]])"),
+    "bf16_nan_becomes_infinity": (
+        "if (isnan(x)) return (uint16_t)0x7FC0;",
+        "if (isnan(x)) return (uint16_t)0x7F80;"),
 }
+
+# Not in the list because no input can tell them from the oracle (equivalent mutants): rounding a
+# scatter-add sum through binary32 before bf16 (binary32 carries more than 2p + 2 bits for p = 8, so
+# the double rounding is innocuous), and dropping the subnormal clamp of the fp16 rounding (a sum of
+# two binary16 values that lands below 2^-14 is a multiple of 2^-24 and needs no rounding).
 
 IGNORE = shutil.ignore_patterns("__pycache__", "*.tmp*")
 

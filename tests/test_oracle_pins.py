@@ -274,6 +274,18 @@ def test_scatter_out_of_bounds_rows_and_columns_clipped():
     np.testing.assert_array_equal(dst, want)
 
 
+def test_scatter_rows_past_the_end_leave_the_memory_after_the_array():
+    # cuTile.jl "Memory": a bounds-checked store never writes outside the array.  The array is the first
+    # 10 rows of a 12-row buffer; indices 10 and 11 name the two rows after it, which must stay zero.
+    buf = np.zeros((12, 6), np.float32)
+    idx = np.array([10, 11, 3], np.int32)
+    src = np.arange(3 * 6, dtype=np.float32).reshape(3, 6) + 1
+    oracle.scatter_rows_masked(buf[:10], 10, 6, 6, idx, src, 6, 6)
+    want = np.zeros((12, 6), np.float32)
+    want[3] = src[2]
+    np.testing.assert_array_equal(buf, want)
+
+
 def test_scatter_duplicates_take_a_candidate():
     rows, cols = 8, 4
     dst = np.full((rows, cols), -1.0, np.float32)
@@ -325,6 +337,20 @@ def test_scatter_add_half_types_equal_torch(kind, tdt):
     want[torch.from_numpy(idx.astype(np.int64))] = (base[torch.from_numpy(idx.astype(np.int64))].float()
                                                    + add.float()).to(tdt)
     np.testing.assert_array_equal(dst, want.view(torch.int16).numpy().view(np.uint16))
+
+
+def test_scatter_add_fp16_subnormals_equal_torch():
+    # binary16 subnormals (exponent field 0: m * 2^-24) on both sides of the addition, and sums that
+    # cross into and out of the subnormal range; torch adds in fp32 and rounds once to fp16, which is
+    # exact rounding for two fp16 operands
+    a_bits = np.array([0x0001, 0x03FF, 0x8200, 0x0400, 0x8001, 0x0155, 0x3C00, 0x83FF], np.uint16)
+    b_bits = np.array([0x0001, 0x0001, 0x0300, 0x8001, 0x8001, 0x02AB, 0x0001, 0x0400], np.uint16)
+    dst = a_bits.reshape(1, 8).copy()
+    oracle.scatter_add_rows(dst, 1, 8, 8, np.array([0], np.int32), b_bits.reshape(1, 8), 8, 8, kind="f16")
+    ta = torch.from_numpy(a_bits.view(np.int16)).view(torch.float16)
+    tb = torch.from_numpy(b_bits.view(np.int16)).view(torch.float16)
+    want = (ta.float() + tb.float()).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    np.testing.assert_array_equal(dst.reshape(8), want)
 
 
 def test_scatter_add_clips_rows_and_columns():
