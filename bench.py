@@ -177,6 +177,79 @@ class ClockSampler:
                 "reasons": reasons, "samples": len(use), "samples_in_timed_region": len(inside)}
 
 
+class NvmlClockSampler:
+    """SM clock and clock-event reasons read through NVML (ctypes, no Python package) every
+    `period_s` from a host thread, so that a timed region of a few milliseconds still gets
+    samples; `summary()` is None when NVML cannot be opened."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, device_index: int, period_s: float = 0.0005):
+        import ctypes
+        self.period = period_s
+        self.rows = []
+        self.t0 = self.t1 = None
+        self._stop = threading.Event()
+        self.ok = False
+        try:
+            self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+            if self.lib.nvmlInit_v2() != 0:
+                return
+            self.h = ctypes.c_void_p()
+            bus = None
+            try:
+                import torch
+                pr = torch.cuda.get_device_properties(device_index)
+                bus = "%08X:%02X:%02X.0" % (pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+            except Exception:
+                bus = None
+            if not (bus and self.lib.nvmlDeviceGetHandleByPciBusId_v2(bus.encode(), ctypes.byref(self.h)) == 0):
+                if self.lib.nvmlDeviceGetHandleByIndex_v2(device_index, ctypes.byref(self.h)) != 0:
+                    return
+            self._mhz = ctypes.c_uint()
+            self._reasons = ctypes.c_ulonglong()
+            self._reason_fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                self.lib.nvmlDeviceGetCurrentClocksThrottleReasons
+            mx = ctypes.c_uint()
+            self.max_mhz = float(mx.value) if self.lib.nvmlDeviceGetMaxClockInfo(self.h, 1, ctypes.byref(mx)) == 0 \
+                else None
+            self.ok = True
+        except Exception:
+            self.ok = False
+
+    def _run(self):
+        import ctypes
+        while not self._stop.is_set():
+            if self.lib.nvmlDeviceGetClockInfo(self.h, 1, ctypes.byref(self._mhz)) == 0 and \
+                    self._reason_fn(self.h, ctypes.byref(self._reasons)) == 0:
+                self.rows.append((time.perf_counter(), float(self._mhz.value), int(self._reasons.value)))
+            time.sleep(self.period)
+
+    def start(self):
+        if self.ok:
+            self._thread = threading.Thread(target=self._run, daemon=True)
+            self._thread.start()
+
+    def mark(self, which: str):
+        setattr(self, which, time.perf_counter())
+
+    def stop(self):
+        if self.ok:
+            self._stop.set()
+            self._thread.join(timeout=2)
+
+    def summary(self):
+        if not self.ok or not self.rows:
+            return None
+        inside = [r for r in self.rows if self.t0 is not None and self.t1 is not None and self.t0 <= r[0] <= self.t1]
+        if not inside:
+            return None
+        reasons = sorted({name for r in inside for bit, name in self.REASONS.items() if r[2] & bit})
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                "samples_in_timed_region": len(inside), "source": f"NVML every {self.period * 1e3:.1f} ms"}
+
+
 # ----------------------------------------------------------------------------- helpers
 
 def dev_bytes(a: np.ndarray):
@@ -261,25 +334,85 @@ def read_profile_traffic(name: str, source: str):
 
 # ----------------------------------------------------------------------------- oracle (CPU) baseline
 
-def cpu_gather_sample(d, budget_s: float):
-    """Time the oracle's gather on a prefix of the index tile; returns (GB/s, rows, seconds)."""
+def host_info():
+    """The host's usable cores (affinity mask) and CPU model."""
+    import platform
+    model = None
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        model = None
+    if not model:
+        try:
+            for line in open("/proc/cpuinfo"):
+                if line.lower().startswith("model name"):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        except Exception:
+            model = None
+    return {"host_cores_available": len(os.sched_getaffinity(0)), "cpu_model": model or "unknown",
+            "arch": platform.machine()}
+
+
+def oracle_gather(d, idx):
     import oracle
-    t, idx = d["table"], d["idx"]
-    n = 16384
-    while True:
+    return oracle.gather_rows(d["table"], d["n_rows"], d["cols"], d["cols"], idx, d["cols"])
+
+
+def oracle_gather_all_cores(d, idx, threads: int):
+    """The unchanged single-threaded oracle on `threads` disjoint slices of the index tile at
+    once (its C call releases the GIL under ctypes, so the slices run on separate cores);
+    returns the joined output."""
+    import concurrent.futures as cf
+    bounds = np.linspace(0, idx.size, threads + 1).astype(np.int64)
+    with cf.ThreadPoolExecutor(max_workers=threads) as ex:
+        parts = list(ex.map(lambda i: oracle_gather(d, idx[bounds[i]:bounds[i + 1]]), range(threads)))
+    return np.concatenate(parts, axis=0)
+
+
+def cpu_gather_sample(d, budget_s: float):
+    """Time the oracle's gather on a prefix of the index tile, single-threaded and on every
+    host core; the all-core output is checked bit for bit against the single-core one.
+    Returns the cpu_baseline record."""
+    idx = d["idx"]
+    info = host_info()
+    cores = info["host_cores_available"]
+
+    def sample(run, n0):
+        n = n0
+        while True:
+            t0 = time.perf_counter()
+            run(idx[:n])
+            dt = time.perf_counter() - t0
+            if dt > budget_s / 8 or n >= idx.size:
+                break
+            n = min(idx.size, int(n * max(2.0, (budget_s / 8) / max(dt, 1e-3))))
+        run(idx[:n])  # warm: the sizing runs above were partly first touches
         t0 = time.perf_counter()
-        oracle.gather_rows(t, d["n_rows"], d["cols"], d["cols"], idx[:n], d["cols"])
+        run(idx[:n])
         dt = time.perf_counter() - t0
-        if dt > budget_s / 4 or n >= idx.size:
-            break
-        n = min(idx.size, int(n * max(2.0, (budget_s / 4) / max(dt, 1e-3))))
-    reps = max(1, int(budget_s / max(dt, 1e-3)))
-    reps = min(reps, 20)
-    t0 = time.perf_counter()
-    for _ in range(reps):
-        oracle.gather_rows(t, d["n_rows"], d["cols"], d["cols"], idx[:n], d["cols"])
-    dt = (time.perf_counter() - t0) / reps
-    return gather_bytes(idx[:n], d["n_rows"], d["cols"], 2) / dt / 1e9, n, dt * reps
+        reps = min(20, max(1, int(budget_s / 2 / max(dt, 1e-3))))
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            run(idx[:n])
+        dt = (time.perf_counter() - t0) / reps
+        return gather_bytes(idx[:n], d["n_rows"], d["cols"], 2) / dt / 1e9, n, dt * reps
+
+    gbs1, n1, s1 = sample(lambda ix: oracle_gather(d, ix), 16384)
+    gbsp, npar, sp = sample(lambda ix: oracle_gather_all_cores(d, ix, cores), 16384 * cores)
+    check_n = min(npar, idx.size)
+    same = bool(np.array_equal(oracle_gather_all_cores(d, idx[:check_n], cores), oracle_gather(d, idx[:check_n])))
+    return {"value": gbsp, "unit": "GB/s", "cores": cores, "kind": "oracle",
+            "sample": f"oracle gather of the first {npar} of {idx.size} indices, split into {cores} disjoint slices "
+                      f"run at once (one thread each), {sp:.1f} s",
+            "all_core_output_equals_single_core": same,
+            "single_core": {"value": gbs1, "unit": "GB/s", "cores": 1,
+                            "sample": f"oracle gather of the first {n1} indices, {s1:.1f} s"},
+            **info}
 
 
 # ----------------------------------------------------------------------------- extra operations
@@ -475,6 +608,24 @@ def run_ops(ctx, pk):
     return ops
 
 
+def clocks_record(smi: ClockSampler, nvml: NvmlClockSampler):
+    """nvidia-smi samples (100 ms) of the timed region, refined by NVML samples taken every
+    0.5 ms when the region is too short for nvidia-smi: the SM clock median and the
+    reasons come from whichever source saw more samples inside the region; both are kept."""
+    a = smi.summary()
+    b = nvml.summary()
+    if b and b["samples_in_timed_region"] > a.get("samples_in_timed_region", 0):
+        out = dict(b)
+        out["sm_max_mhz"] = b["sm_max_mhz"] or a.get("sm_max_mhz")
+        out["reasons"] = sorted(set(b["reasons"]) | set(r for r in a.get("reasons", []) if r != "no nvidia-smi samples"))
+        out["nvidia_smi"] = a
+        return out
+    if b:
+        a = dict(a)
+        a["nvml"] = b
+    return a
+
+
 # ----------------------------------------------------------------------------- arms
 
 def run_e2e(ctx, table, idx, n_rows, cols, t_dev, i_dev, out, steps, dist):
@@ -536,30 +687,31 @@ def run_e2e(ctx, table, idx, n_rows, cols, t_dev, i_dev, out, steps, dist):
 def run_reference(args, dist):
     if dist.rank != 0:
         return 0
-    import multiprocessing
     import synth.workloads as wl
     d = wl.gather_rows_bf16()
-    n = 65536  # each step: the oracle on a 65,536-index prefix of the workload
-    import oracle
+    info = host_info()
+    cores = info["host_cores_available"]
+    n = 65536 * cores  # each step: the oracle on a prefix of the workload, one slice per host core
+    idx = d["idx"][:n]
     for _ in range(min(args.warmup, 3)):
-        oracle.gather_rows(d["table"], d["n_rows"], d["cols"], d["cols"], d["idx"][:n], d["cols"])
+        oracle_gather_all_cores(d, idx, cores)
     times = []
     for _ in range(args.steps):
         t0 = time.perf_counter()
-        oracle.gather_rows(d["table"], d["n_rows"], d["cols"], d["cols"], d["idx"][:n], d["cols"])
+        oracle_gather_all_cores(d, idx, cores)
         times.append(time.perf_counter() - t0)
         if sum(times) > 120:
             break
     dt = statistics.fmean(times)
-    gbs = gather_bytes(d["idx"][:n], d["n_rows"], d["cols"], 2) / dt / 1e9
-    sample = f"oracle gather of the first {n} of 1,048,576 indices per step ({len(times)} steps)"
+    gbs = gather_bytes(idx, d["n_rows"], d["cols"], 2) / dt / 1e9
+    sample = (f"oracle gather of the first {idx.size} of 1,048,576 indices per step, {cores} disjoint slices "
+              f"run at once (one thread each; the oracle itself is single-threaded C) ({len(times)} steps)")
     line = {"impl": "reference", "metric": METRIC, "value": gbs, "unit": "GB/s", "n_gpus": args.gpus,
             "steps": len(times), "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
             "config": {"workload": GATHER_WORKLOAD, "l2": "CPU run"},
-            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample,
-                             "host_cores_available": len(os.sched_getaffinity(0)),
-                             "cpu": multiprocessing.cpu_count()},
+            "cpu_baseline": {"value": gbs, "unit": "GB/s", "cores": cores, "kind": "oracle", "sample": sample,
+                             **info},
             "e2e": {"value": gbs, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
@@ -592,22 +744,27 @@ def run_sbt(args, dist):
 
     sampler = ClockSampler(torch.cuda.current_device())
     sampler.start()
+    fine = NvmlClockSampler(torch.cuda.current_device())
+    fine.start()
     time.sleep(0.3)
     dist.barrier()
     torch.cuda.synchronize()
     launches0 = ctx.launch_count
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     sampler.mark("t0")
+    fine.mark("t0")
     ev0.record(stream)
     for _ in range(args.steps):
         step()
     ev1.record(stream)
     ev1.synchronize()
+    fine.mark("t1")
     sampler.mark("t1")
     torch.cuda.synchronize()
     dist.barrier()
     launches = ctx.launch_count - launches0
     sampler.stop()
+    fine.stop()
     ms_total = ev0.elapsed_time(ev1)
     value, ms_max = aggregate(dist, bytes_step, ms_total, args.steps)
     ms_step = ms_max / args.steps
@@ -637,16 +794,14 @@ def run_sbt(args, dist):
                 "d2h_bytes_per_step": d2h_bytes, "ms_per_step": e2e_ms,
                 "note": "inputs copied host->device and the output device->host every step; steps pipelined "
                         "over two buffer sets (upload of step i+1 overlaps download of step i)"},
-        "clocks": sampler.summary(),
+        "clocks": clocks_record(sampler, fine),
     }
     if not args.no_ops:
         del out, t_dev
         torch.cuda.empty_cache()
         line["ops"] = run_ops(ctx, pk)
     if dist.rank == 0:
-        gbs, nrows, secs = cpu_gather_sample(d, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": gbs, "unit": "GB/s", "cores": 1, "kind": "oracle",
-                                "sample": f"oracle gather of the first {nrows} of {n} indices, {secs:.1f} s"}
+        line["cpu_baseline"] = cpu_gather_sample(d, args.cpu_seconds)
         print(json.dumps(line), flush=True)
     ctx.close()
     return 0

@@ -325,24 +325,28 @@ SBT_API sbt_status sbt_gemm_block_scaled(sbt_context* ctx, sbt_lowp_format a_fmt
 /*
  * Boundary-tile GEMM without any device allocation.
  * The pages have no counterpart to this call; it exists for callers that
- * cannot allocate device memory when they multiply: code running while a
- * stream is captured into a CUDA graph (cudaMalloc is not allowed there),
- * plugins confined to another framework's memory pool, and latency-critical
- * paths that cannot take cudaMalloc's implicit device synchronisation.
+ * cannot allocate device memory when they multiply: plugins confined to
+ * another framework's memory pool (they may not call the CUDA allocator
+ * themselves), code running under a device-memory budget committed up front,
+ * and latency-critical paths that cannot take the implicit device
+ * synchronisation of cudaMalloc and cudaFree.
  *
  * Same arguments and result as sbt_gemm_bounded, minus the workspace: the
  * operand-staging scratch is a fixed array of SBT_GEMM_NOALLOC_SCRATCH_BYTES
  * inside the library (one per device, held from module load until process
  * exit).  Shapes whose sbt_gemm_bounded_workspace_size() exceeds that size
  * are rejected with SBT_ERR_INVALID_ARG before anything is launched.  The
- * call itself allocates nothing (no cudaMalloc, no cudaFree).
+ * call itself allocates nothing (no cudaMalloc, no cudaFree, no allocating
+ * library routine).
  *
- * The first call on a device looks up the array's device address with
- * cudaGetSymbolAddress (with that device current) and caches it; make that
- * first call before any stream capture.  All calls share the one array and
- * it keeps the previous call's contents (the call rewrites every byte it
- * reads, so nothing needs clearing); calls that can overlap on the GPU --
- * different streams, or unsynchronised host threads -- race on it.
+ * Set-up: the first call on a device (whatever its shape) looks up the
+ * array's device address with cudaGetSymbolAddress, with that device current,
+ * and caches it; make that first call before any stream capture.  Like every
+ * call of this library it leaves ctx's device current on the calling thread.
+ * All calls share the one array and it keeps the previous call's contents
+ * (the call rewrites every byte it reads, so nothing needs clearing); calls
+ * that can overlap on the GPU -- different streams, or unsynchronised host
+ * threads -- race on it.
  */
 #define SBT_GEMM_NOALLOC_SCRATCH_BYTES (16u << 20)
 SBT_API sbt_status sbt_gemm_bounded_noalloc(sbt_context* ctx, const void* A, int64_t lda, const void* B, int64_t ldb,

@@ -282,11 +282,12 @@ def gemm_block_scaled(ctx, A, lda, B, ldb, a_scale, ld_sa, b_scale, ld_sb, K_s, 
 def gemm_bounded_noalloc(ctx, A, lda, B, ldb, C, ldc, M, N, K, c_dtype="bf16", stream=None):
     """sbt_gemm_bounded_noalloc: the bounded GEMM with the library's fixed staging scratch.
 
-    For callers that cannot allocate device memory at the call (inside a CUDA
-    graph capture, inside another framework's memory pool, or on paths that
-    cannot take cudaMalloc's implicit synchronisation).  Shapes needing more
-    than GEMM_NOALLOC_SCRATCH_BYTES of staging are rejected; calls that may
-    overlap on the GPU race on the shared scratch.
+    For callers that cannot allocate device memory at the call: plugins
+    confined to another framework's memory pool, code under a device-memory
+    budget committed up front, or paths that cannot take cudaMalloc's implicit
+    synchronisation.  Shapes needing more than GEMM_NOALLOC_SCRATCH_BYTES of
+    staging are rejected; calls that may overlap on the GPU race on the shared
+    scratch.
     """
     code = {"bf16": SBT_BF16, "f32": SBT_F32}[c_dtype] if isinstance(c_dtype, str) else int(c_dtype)
     _check(load_library().sbt_gemm_bounded_noalloc(ctx.handle, _ptr(A), lda, _ptr(B), ldb, _ptr(C), ldc, code, M, N,

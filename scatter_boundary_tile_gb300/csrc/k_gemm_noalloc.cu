@@ -2,17 +2,21 @@
 // in a fixed, library-owned device array instead of a caller workspace.
 //
 // Who needs this: callers that cannot allocate device memory at the point of
-// the call -- code that runs while a stream is being captured into a CUDA
-// graph (cudaMalloc is not allowed inside a capture), plugins that live
-// inside another framework's memory pool and are forbidden from calling the
-// CUDA allocator, and latency-critical paths that cannot afford the implicit
-// device synchronisation of cudaMalloc/cudaFree.  They still pass A, B and C.
+// the call -- plugins that live inside another framework's memory pool and
+// are not allowed to call the CUDA allocator themselves, code running under a
+// fixed device-memory budget that was committed up front, and latency-critical
+// paths that cannot afford the implicit device synchronisation of
+// cudaMalloc/cudaFree.  They still pass A, B and C.
 //
 // The scratch is one file-scope __device__ array per device, created when the
 // library's module is loaded on that device and held until process exit.
 // Host code may not use the array's name as a device address (on the host it
-// is only a stand-in), so the device address is looked up once per device
-// with cudaGetSymbolAddress while that device is current, and cached.
+// is only a stand-in), so the device address is looked up with
+// cudaGetSymbolAddress while that device is current, once per device, and
+// cached.  The lookup runs on every call's first visit to a device, whatever
+// the shape (also when nothing has to be staged), so the first call on a
+// device is the only one that does it.  It leaves that device current on the
+// calling thread, as every other call of the library does.
 //
 // Every call shares the array and it keeps the previous call's contents.  The
 // GEMM's staging kernels write every byte of the scratch that the main kernel
@@ -65,7 +69,7 @@ extern "C" SBT_API sbt_status sbt_gemm_bounded_noalloc(sbt_context* ctx, const v
                             std::to_string((size_t)SBT_GEMM_NOALLOC_SCRATCH_BYTES) +
                             " bytes; use sbt_gemm_bounded with a caller workspace");
     void* scratch = nullptr;
-    if (need > 0 && (st = scratch_for_device(ctx->device, &scratch))) return st;
+    if ((st = scratch_for_device(ctx->device, &scratch))) return st;
     return sbt_gemm_bounded(ctx, A, lda, B, ldb, C, ldc, c_dtype, M, N, K, scratch, need > 0 ? SBT_GEMM_NOALLOC_SCRATCH_BYTES : 0,
                             stream);
 }

@@ -59,3 +59,11 @@ def test_create_without_a_gpu_reports_cuda_error(lib):
     st = lib.sbt_create(0, ctypes.byref(h))
     assert st in (sbt.SBT_ERR_CUDA, sbt.SBT_ERR_INVALID_ARG) and not h.value
     assert lib.sbt_last_error_message()
+
+
+def test_noalloc_scratch_size_matches_header():
+    """The binding's size check and the library's fixed GEMM scratch are the same number."""
+    text = open(os.path.join(ROOT, "include", "sbt.h")).read()
+    m = re.search(r"#define\s+SBT_GEMM_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", text)
+    assert m, "SBT_GEMM_NOALLOC_SCRATCH_BYTES not found in include/sbt.h"
+    assert int(m.group(1)) << int(m.group(2)) == sbt.GEMM_NOALLOC_SCRATCH_BYTES
