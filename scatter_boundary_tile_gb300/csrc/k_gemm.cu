@@ -42,6 +42,9 @@ constexpr uint32_t kABytes = BM * BK * 2;
 constexpr int kEpiWarps = 4;
 constexpr int kEpiWords = 32 * 33;  // per-warp 32x32 transpose buffer, padded rows
 constexpr int kNumBars = 2 * kStages + 5;
+// MN-major B in shared memory: one TMA box of 64 columns x BK rows (128-byte rows) per 64 columns.
+constexpr uint32_t kMnAtomBytes = 64 * BK * 2;  // 8 KB: next 64 columns
+constexpr uint32_t kMnKStepBytes = 16 * 128;     // one K = 16 step: 16 rows of 128 B
 // Single-CTA kernel with BM x BN_ tiles (BN_ = 256, 128 or 64: narrower tiles
 // spread a small problem over more SMs).
 template <int BN_>
@@ -66,6 +69,7 @@ struct GemmParams {
     unsigned int* status;
     uint64_t wait_ns;
     int withhold_first_load;  // test hook: block 0 never issues its first stage
+    int b_mn;                 // B read by TMA where it lies (MN-major boxes of 64 columns), not from B'^T
 };
 
 // Tile order: groups of kGroupM M-tiles are walked N column by N column, so the
@@ -217,7 +221,14 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     }
                     mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
                     tma_load_2d(sa, &tmA, kb * BK, mt * BM, full_bar(stage));
-                    tma_load_2d(sa + kABytes, &tmB, kb * BK, nt * BN_, full_bar(stage));
+                    if (p.b_mn) {
+#pragma unroll
+                        for (int a = 0; a < BN_ / 64; ++a)
+                            tma_load_2d(sa + kABytes + a * kMnAtomBytes, &tmB, nt * BN_ + 64 * a, kb * BK,
+                                        full_bar(stage));
+                    } else {
+                        tma_load_2d(sa + kABytes, &tmB, kb * BK, nt * BN_, full_bar(stage));
+                    }
                     ++issued;
                     if (++stage == kStages) {
                         stage = 0;
@@ -253,7 +264,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                 int mt_unused, nt;
                 tile_coords(tile, p.m_tiles, p.n_tiles, &mt_unused, &nt);
                 const int n_valid = min(BN_, p.N - nt * BN_);
-                const uint32_t idesc = idesc_bf16_f32(BM, (uint32_t)((n_valid + 15) & ~15));
+                const uint32_t idesc =
+                    idesc_bf16_f32(BM, (uint32_t)((n_valid + 15) & ~15)) | (p.b_mn ? kIdescBMnMajor : 0u);
                 if (!mbar_wait_bounded(tempty_bar(acc), (use & 1u) ^ 1u, p.wait_ns, abort_flag, p.status,
                                        kCodeMma)) {
                     ok = false;
@@ -272,7 +284,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
                     const uint32_t sa = smem_u32(smem + (size_t)stage * kStageBytes);
                     const uint32_t sb = sa + kABytes;
                     for (int ks = 0; ks < k_steps; ++ks) {
-                        tc_mma_f16(d_tmem, smem_desc_sw128(sa + 32u * ks), smem_desc_sw128(sb + 32u * ks), idesc,
+                        const uint64_t bd = p.b_mn ? smem_desc_mn_sw128(sb + kMnKStepBytes * ks, kMnAtomBytes)
+                                                   : smem_desc_sw128(sb + 32u * ks);
+                        tc_mma_f16(d_tmem, smem_desc_sw128(sa + 32u * ks), bd, idesc,
                                    (kb | ks) != 0 ? 1u : 0u);
                     }
                     tc_commit(empty_bar(stage));
@@ -415,7 +429,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                         if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * nkb * 2 * kHalfBytes);
                         for (int j = 0; j < nkb; ++j) {
                             tma_load_2d_pair(sa + j * kHalfBytes, &tmA, (kb0 + j) * BK, mt * 256 + (int)rank * 128, leader_full);
-                            tma_load_2d_pair(sa + (kKB2 + j) * kHalfBytes, &tmB, (kb0 + j) * BK, nt * 256 + (int)rank * 128, leader_full);
+                            if (p.b_mn) {
+                                for (int a = 0; a < 2; ++a)
+                                    tma_load_2d_pair(sa + (kKB2 + j) * kHalfBytes + a * kMnAtomBytes, &tmB,
+                                                     nt * 256 + (int)rank * 128 + 64 * a, (kb0 + j) * BK, leader_full);
+                            } else {
+                                tma_load_2d_pair(sa + (kKB2 + j) * kHalfBytes, &tmB, (kb0 + j) * BK,
+                                                 nt * 256 + (int)rank * 128, leader_full);
+                            }
                         }
                     }
                     if (++stage == kStages2) {
@@ -431,7 +452,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
             uint32_t stage = 0, phase = 0;
             int local = 0;
             bool ok = true;
-            const uint32_t idesc = idesc_bf16_f32(256, 256);
+            const uint32_t idesc = idesc_bf16_f32(256, 256) | (p.b_mn ? kIdescBMnMajor : 0u);
             for (int tile = cluster; ok && tile < num_tiles; tile += nclusters, ++local) {
                 const int acc = local & 1;
                 const uint32_t use = (uint32_t)(local >> 1);
@@ -457,7 +478,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
                     const uint32_t sa = sa0 + j * kHalfBytes;
                     const uint32_t sb = sa0 + (kKB2 + j) * kHalfBytes;
                     for (int ks = 0; ks < k_steps; ++ks) {
-                        tc_mma_f16_pair(d_tmem, smem_desc_sw128(sa + 32u * ks), smem_desc_sw128(sb + 32u * ks),
+                        const uint64_t bd = p.b_mn ? smem_desc_mn_sw128(sb + kMnKStepBytes * ks, kMnAtomBytes)
+                                                   : smem_desc_sw128(sb + 32u * ks);
+                        tc_mma_f16_pair(d_tmem, smem_desc_sw128(sa + 32u * ks), bd,
                                         idesc, (kb | ks) != 0 ? 1u : 0u);
                     }
                     }
@@ -623,6 +646,40 @@ sbt_status encode_kmajor(sbt_context* ctx, CUtensorMap* map, void* base, int64_t
     return SBT_OK;
 }
 
+// Tensor map over the caller's A itself, for rows that are 16-byte aligned:
+// elements past K or M lie outside the tensor and TMA fills them with zeros,
+// so the boundary tiles come out zero-filled without a staged copy.
+sbt_status encode_direct_a(sbt_context* ctx, CUtensorMap* map, const void* A, int64_t lda, int64_t M, int64_t K) {
+    cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)M};
+    cuuint64_t strides[1] = {(cuuint64_t)lda * 2};
+    cuuint32_t box[2] = {(cuuint32_t)BK, (cuuint32_t)BM};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = ctx->encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(A), dims, strides,
+                                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return sbt_fail(SBT_ERR_TENSOR_MAP, "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
+    return SBT_OK;
+}
+
+// Tensor map over the caller's B itself (rows 16-byte aligned), read MN-major:
+// boxes of 64 columns x BK rows; columns past N and rows past K are zero-filled.
+sbt_status encode_direct_b(sbt_context* ctx, CUtensorMap* map, const void* B, int64_t ldb, int64_t K, int64_t N) {
+    cuuint64_t dims[2] = {(cuuint64_t)N, (cuuint64_t)K};
+    cuuint64_t strides[1] = {(cuuint64_t)ldb * 2};
+    cuuint32_t box[2] = {64u, (cuuint32_t)BK};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = ctx->encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(B), dims, strides,
+                                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return sbt_fail(SBT_ERR_TENSOR_MAP, "cuTensorMapEncodeTiled failed (" + std::to_string((int)r) + ")");
+    return SBT_OK;
+}
+
+sbt_status launch_main(sbt_context* ctx, const CUtensorMap* tmA_direct, const CUtensorMap* tmB_direct,
+                       const uint16_t* Ap, const uint16_t* Bp, const sbt_gemm_layout& d, void* C, int64_t ldc,
+                       bool c_f32, const float* acc, int64_t ld_acc, int64_t M, int64_t N, int64_t K,
+                       cudaStream_t stream);
+
 }  // namespace
 
 size_t sbt_gemm_workspace_bytes(int64_t M, int64_t N, int64_t K) {
@@ -653,23 +710,47 @@ sbt_status sbt_launch_gemm(sbt_context* ctx, const void* A, int64_t lda, const v
     uint16_t* Ap = (uint16_t*)workspace;
     uint16_t* Bp = (uint16_t*)((char*)workspace + d.a_bytes);
 
-    // 1. operand staging
-    {
+    // 1. operand staging.  An operand whose rows are 16-byte aligned is read by TMA where it
+    //    lies (unless the caller forces the staged path with SBT_PATH_SCALAR or SBT_PATH_VECTOR).
+    const bool tma_ok = ctx->path == SBT_PATH_AUTO || ctx->path == SBT_PATH_TMA;
+    const bool direct_a = tma_ok && lda % 8 == 0 && (reinterpret_cast<uintptr_t>(A) & 15u) == 0;
+    const bool direct_b = tma_ok && ldb % 8 == 0 && (reinterpret_cast<uintptr_t>(B) & 15u) == 0;
+    CUtensorMap tmA;
+    if (direct_a) {
+        sbt_status st = encode_direct_a(ctx, &tmA, A, lda, M, K);
+        if (st) return st;
+    } else {
         const int64_t vecs = d.Mp * (d.Kp / 8);
         const int grid = (int)std::min<int64_t>(sbt_cdiv(vecs, 256), (int64_t)ctx->sm_count * 8);
         k_stage_a<<<grid, 256, 0, stream>>>((const uint16_t*)A, lda, (int)M, (int)K, Ap, (int)d.Kp, vecs);
         sbt_status st = sbt_after_launch(ctx, "gemm_bounded (stage A)");
         if (st) return st;
+    }
+    CUtensorMap tmB;
+    if (direct_b) {
+        sbt_status st = encode_direct_b(ctx, &tmB, B, ldb, K, N);
+        if (st) return st;
+    } else {
         dim3 g2((unsigned)(d.Kp / 64), (unsigned)(d.Np / 64));
         k_stage_bt<<<g2, 256, 0, stream>>>((const uint16_t*)B, ldb, (int)K, (int)N, Bp, (int)d.Kp);
-        if ((st = sbt_after_launch(ctx, "gemm_bounded (stage B)"))) return st;
+        sbt_status st = sbt_after_launch(ctx, "gemm_bounded (stage B)");
+        if (st) return st;
     }
-    return sbt_launch_gemm_main(ctx, Ap, Bp, d, C, ldc, c_dtype == SBT_F32, nullptr, 0, M, N, K, stream);
+    return launch_main(ctx, direct_a ? &tmA : nullptr, direct_b ? &tmB : nullptr, Ap, Bp, d, C, ldc,
+                       c_dtype == SBT_F32, nullptr, 0, M, N, K, stream);
 }
 
 sbt_status sbt_launch_gemm_main(sbt_context* ctx, const uint16_t* Ap, const uint16_t* Bp, const sbt_gemm_layout& d,
                                 void* C, int64_t ldc, bool c_f32, const float* acc, int64_t ld_acc, int64_t M,
                                 int64_t N, int64_t K, cudaStream_t stream) {
+    return launch_main(ctx, nullptr, nullptr, Ap, Bp, d, C, ldc, c_f32, acc, ld_acc, M, N, K, stream);
+}
+
+namespace {
+sbt_status launch_main(sbt_context* ctx, const CUtensorMap* tmA_direct, const CUtensorMap* tmB_direct,
+                       const uint16_t* Ap, const uint16_t* Bp, const sbt_gemm_layout& d, void* C, int64_t ldc,
+                       bool c_f32, const float* acc, int64_t ld_acc, int64_t M, int64_t N, int64_t K,
+                       cudaStream_t stream) {
     // 2. tensor-core main kernel
     // CTA pairs when there are at least as many 256 x 256 tiles as SM pairs;
     // single CTAs for smaller problems, with 128 x 256 tiles when those give
@@ -683,9 +764,15 @@ sbt_status sbt_launch_gemm_main(sbt_context* ctx, const uint16_t* Ap, const uint
             break;
         }
     CUtensorMap tmA, tmB;
-    sbt_status st = encode_kmajor(ctx, &tmA, (void*)Ap, d.Mp, d.Kp, BM);
-    if (st) return st;
-    if ((st = encode_kmajor(ctx, &tmB, (void*)Bp, d.Np, d.Kp, pair ? 128 : bn1))) return st;
+    sbt_status st = SBT_OK;
+    if (tmA_direct)
+        tmA = *tmA_direct;
+    else if ((st = encode_kmajor(ctx, &tmA, (void*)Ap, d.Mp, d.Kp, BM)))
+        return st;
+    if (tmB_direct)
+        tmB = *tmB_direct;
+    else if ((st = encode_kmajor(ctx, &tmB, (void*)Bp, d.Np, d.Kp, pair ? 128 : bn1)))
+        return st;
     GemmParams p;
     p.C = (char*)C;
     p.ldc = ldc;
@@ -701,6 +788,7 @@ sbt_status sbt_launch_gemm_main(sbt_context* ctx, const uint16_t* Ap, const uint
     p.status = ctx->status;
     p.wait_ns = ctx->wait_limit_ns;
     p.withhold_first_load = ctx->test_hook == SBT_TEST_WITHHOLD_LOAD;
+    p.b_mn = tmB_direct != nullptr;
     static bool attr_set[64] = {false};
     if (!attr_set[ctx->device & 63]) {
         cudaError_t e = cudaFuncSetAttribute(k_gemm_bf16_tc<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -764,3 +852,4 @@ sbt_status sbt_launch_gemm_main(sbt_context* ctx, const uint16_t* Ap, const uint
     if (e != cudaSuccess) return sbt_cuda_check(e, "gemm_bounded (tcgen05)");
     return sbt_after_launch(ctx, "gemm_bounded (tcgen05)");
 }
+}  // namespace

@@ -195,6 +195,21 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
     return d;
 }
 
+// Shared-memory descriptor for an MN-major operand tile with the 128-byte
+// swizzle, as TMA writes boxes of 64 (MN) x rows (K) 16-bit elements: each
+// 128-byte row holds 64 consecutive MN elements of one k, 8-row swizzle atoms
+// are 1024 B apart along K (stride-dimension offset), and the next 64 MN
+// elements start `mn_stride` bytes further (leading-dimension offset).
+__device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t saddr, uint32_t mn_stride) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);          // start address
+    d |= (uint64_t)((mn_stride >> 4) & 0x3FFFu) << 16; // leading-dimension byte offset: next 64 MN elements
+    d |= (uint64_t)(1024u >> 4) << 32;                 // stride-dimension byte offset: next 8 rows of K
+    d |= (uint64_t)1u << 46;                           // descriptor version for tcgen05
+    d |= (uint64_t)2u << 61;                           // 128-byte swizzle
+    return d;
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B (K-major), fp32 accumulator, M x N.
 __host__ __device__ __forceinline__ uint32_t idesc_bf16_f32(uint32_t m, uint32_t n) {
     return (1u << 4)            // D format: f32
@@ -203,6 +218,9 @@ __host__ __device__ __forceinline__ uint32_t idesc_bf16_f32(uint32_t m, uint32_t
            | ((n >> 3) << 17)   // N / 8
            | ((m >> 4) << 24);  // M / 16
 }
+
+// Bit of the kind::f16 instruction descriptor that makes B MN-major (transposed).
+constexpr uint32_t kIdescBMnMajor = 1u << 16;
 
 // ---------------------------------------------------------------- clusters and CTA pairs
 

@@ -84,6 +84,90 @@ def test_integer_inputs_exact(ctx, mnk):
     np.testing.assert_array_equal(got32, want.astype(np.float64))
 
 
+def gemm_aligned(M, N, K, tag, align_a, align_b, extra=0):
+    """Like the workload generator, but A's and/or B's leading dimension is a multiple of 8
+    elements (16-byte rows: TMA reads that operand where it lies); NaN in every padding
+    column, so a read past K or N would show."""
+    g = dict(wl.gemm_bf16(M=M, N=N, K=K, tag=tag))
+    if align_a:
+        lda = -(-K // 8) * 8 + extra
+        A = np.full((M, lda), wl.BF16_NAN_BITS, np.uint16)
+        A[:, :K] = g["A"][:, :K]
+        g["A"], g["lda"] = A, lda
+    if align_b:
+        ldb = -(-N // 8) * 8 + extra
+        B = np.full((K, ldb), wl.BF16_NAN_BITS, np.uint16)
+        B[:, :N] = g["B"][:, :N]
+        g["B"], g["ldb"] = B, ldb
+    return g
+
+
+ALIGNED_SHAPES = [(65, 97, 73), (1000, 1000, 1000), (300, 257, 129), (129, 600, 64), (2048, 1800, 96),
+                  (2304, 2500, 200), (4096, 2560, 128), (1, 8, 8), (200, 16, 1000)]
+
+
+@pytest.mark.parametrize("path", ["auto", "scalar"])
+@pytest.mark.parametrize("align", [(1, 0), (0, 1), (1, 1)])
+@pytest.mark.parametrize("mnk", ALIGNED_SHAPES)
+def test_aligned_rows_vs_oracle(ctx, mnk, align, path):
+    """16-byte-aligned rows: under "auto" TMA reads that operand where it lies (A K-major,
+    B MN-major in 64-column boxes; the K, M and N tails come from TMA's zero fill, the NaN
+    padding columns stay unread), under "scalar" both operands are staged.  Both meet the
+    gate, on the single-CTA and the CTA-pair kernel."""
+    M, N, K = mnk
+    ctx.set_path(path)
+    g = gemm_aligned(M, N, K, tag=21, align_a=align[0], align_b=align[1], extra=8 if M == 300 else 0)
+    got, _ = run_gemm(ctx, g, "bf16")
+    ref = oracle.gemm_f64(g["A"], g["lda"], g["B"], g["ldb"], M, N, K)
+    ref_b = synth.bf16_bits_to_f32(oracle.round_bf16(ref)).astype(np.float64)
+    assert rel_fro(got, ref_b) <= TOL
+    assert not np.isnan(got).any()
+
+
+@pytest.mark.parametrize("mnk", [(16, 16, 64), (65, 97, 64), (130, 300, 48), (2304, 2320, 80)])
+def test_aligned_rows_integer_inputs_exact(ctx, mnk):
+    """Both operands read by TMA where they lie (no staging launch), integer inputs: every
+    partial sum is exact, so C must equal the integer product bit for bit."""
+    M, N, K = mnk
+    lda, ldb = -(-K // 8) * 8 + 8, -(-N // 8) * 8
+    a = synth.int_below(511, M * K, 5, lo=-2).reshape(M, K).astype(np.float32)
+    b = synth.int_below(512, K * N, 5, lo=-2).reshape(K, N).astype(np.float32)
+    A = np.full((M, lda), wl.BF16_NAN_BITS, np.uint16)
+    B = np.full((K, ldb), wl.BF16_NAN_BITS, np.uint16)
+    A[:, :K] = (a.view(np.uint32) >> 16).astype(np.uint16)
+    B[:, :N] = (b.view(np.uint32) >> 16).astype(np.uint16)
+    g = {"A": A, "B": B, "M": M, "N": N, "K": K, "lda": lda, "ldb": ldb, "ldc": N + 1}
+    want = (a.astype(np.int64) @ b.astype(np.int64)).astype(np.float64)
+    before = ctx.launch_count
+    got, _ = run_gemm(ctx, g, "bf16")
+    assert ctx.launch_count - before == 1  # the tensor-core kernel alone
+    np.testing.assert_array_equal(got, want)
+    got32, _ = run_gemm(ctx, g, "f32")
+    np.testing.assert_array_equal(got32, want)
+
+
+def test_aligned_stride_misaligned_pointers(ctx):
+    """Row strides that are multiples of 8 elements but A and B pointers 2 bytes off a 16-byte
+    boundary: the rows are not 16-byte aligned, so both operands are staged (result unchanged)."""
+    M, N, K = 200, 300, 136
+    g = gemm_aligned(M, N, K, tag=22, align_a=1, align_b=1)
+    A = dev(np.concatenate([np.zeros(1, np.uint16), g["A"].reshape(-1)]))
+    B = dev(np.concatenate([np.zeros(1, np.uint16), g["B"].reshape(-1)]))
+    ldc = g["ldc"]
+    C = torch.empty(M * ldc * 2, dtype=torch.uint8, device="cuda")
+    ws_n = sbt.gemm_bounded_workspace_size(ctx, M, N, K, g["lda"], g["ldb"])
+    ws = torch.empty(ws_n, dtype=torch.uint8, device="cuda")
+    before = ctx.launch_count
+    sbt.gemm_bounded(ctx, A.data_ptr() + 2, g["lda"], B.data_ptr() + 2, g["ldb"], C, ldc, M, N, K, ws, ws_n)
+    sync()
+    ctx.check_status()
+    assert ctx.launch_count - before == 3  # both staging kernels and the tensor-core kernel
+    got = synth.bf16_bits_to_f32(host(C, np.uint16, (M, ldc))[:, :N]).astype(np.float64)
+    ref = oracle.gemm_f64(g["A"], g["lda"], g["B"], g["ldb"], M, N, K)
+    ref_b = synth.bf16_bits_to_f32(oracle.round_bf16(ref)).astype(np.float64)
+    assert rel_fro(got, ref_b) <= TOL
+
+
 def test_many_tiles_with_m_tail(ctx):
     """M = 384 fills one and a half 256-row tiles; 2 x 118 tiles run on CTA pairs, each pair
     taking several tiles, so the persistent loop, both TMEM accumulators and the masked
