@@ -610,6 +610,55 @@ __global__ void __launch_bounds__(256) k_stage_bt(const uint16_t* __restrict__ B
     sbt_st_v4(Bp + (int64_t)(n0 + 2 * np + 1) * Kp + k0 + kv, make_uint4(o1[0], o1[1], o1[2], o1[3]));
 }
 
+// One padded operand copy: dst [rows_p][cols_p] <- src [rows][cols] (row stride ld),
+// zero past rows or cols; cols_p is a multiple of 8, so every 16-byte vector of dst
+// is aligned.  The source rows are only 2-byte aligned when ld is odd: whole
+// vectors come from aligned 8-byte words (each holds an element of the vector),
+// the ragged end of a row element by element.
+struct RowCopy {
+    const uint16_t* src;
+    int64_t ld;
+    int rows, cols;
+    uint16_t* dst;
+    int cols_p;
+    int64_t vecs;  // rows_p * cols_p / 8
+};
+
+__device__ __forceinline__ void row_copy_vector(const RowCopy& c, int64_t v) {
+    const int kv = c.cols_p / 8;
+    const int64_t r = v / kv;
+    const int k0 = (int)(v - r * kv) * 8;
+    uint32_t w[4] = {0, 0, 0, 0};
+    if (r < c.rows && k0 < c.cols) {
+        const uint16_t* row = c.src + r * c.ld;
+        if (k0 + 8 <= c.cols) {
+            const uint64_t lo = sbt_load8_any(row + k0), hi = sbt_load8_any(row + k0 + 4);
+            w[0] = (uint32_t)lo;
+            w[1] = (uint32_t)(lo >> 32);
+            w[2] = (uint32_t)hi;
+            w[3] = (uint32_t)(hi >> 32);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e)
+                if (k0 + e < c.cols) w[e >> 1] |= (uint32_t)__ldg(row + k0 + e) << (16 * (e & 1));
+        }
+    }
+    sbt_st_v4(c.dst + r * c.cols_p + k0, make_uint4(w[0], w[1], w[2], w[3]));
+}
+
+// Both operand copies of one GEMM call in one launch: A' [Mp][Kp] (K-major) and
+// B'' [Kp][Np] (B's own layout, read MN-major by the tensor-core kernel); either
+// may be empty (vecs = 0) when TMA reads that operand where it lies.
+__global__ void __launch_bounds__(256) k_stage_ab(const RowCopy a, const RowCopy b) {
+    const int64_t total = a.vecs + b.vecs;
+    for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < total; v += (int64_t)gridDim.x * blockDim.x) {
+        if (v < a.vecs)
+            row_copy_vector(a, v);
+        else
+            row_copy_vector(b, v - a.vecs);
+    }
+}
+
 // C[m][n] = acc[m][n] (fp32 C), or 0 without acc, for m < M, n < N: the K = 0 result.
 __global__ void k_zero_c(char* C, int64_t ldc, int M, int N, int es, const float* acc, int64_t ld_acc) {
     const int64_t total = (int64_t)M * N;
@@ -710,34 +759,46 @@ sbt_status sbt_launch_gemm(sbt_context* ctx, const void* A, int64_t lda, const v
     uint16_t* Ap = (uint16_t*)workspace;
     uint16_t* Bp = (uint16_t*)((char*)workspace + d.a_bytes);
 
-    // 1. operand staging.  An operand whose rows are 16-byte aligned is read by TMA where it
-    //    lies (unless the caller forces the staged path with SBT_PATH_SCALAR or SBT_PATH_VECTOR).
-    const bool tma_ok = ctx->path == SBT_PATH_AUTO || ctx->path == SBT_PATH_TMA;
-    const bool direct_a = tma_ok && lda % 8 == 0 && (reinterpret_cast<uintptr_t>(A) & 15u) == 0;
-    const bool direct_b = tma_ok && ldb % 8 == 0 && (reinterpret_cast<uintptr_t>(B) & 15u) == 0;
-    CUtensorMap tmA;
-    if (direct_a) {
-        sbt_status st = encode_direct_a(ctx, &tmA, A, lda, M, K);
-        if (st) return st;
-    } else {
+    if (ctx->path == SBT_PATH_SCALAR) {
+        // 1'. the transposing staging: A' [Mp][Kp] and B'^T [Np][Kp], both K-major
         const int64_t vecs = d.Mp * (d.Kp / 8);
         const int grid = (int)std::min<int64_t>(sbt_cdiv(vecs, 256), (int64_t)ctx->sm_count * 8);
         k_stage_a<<<grid, 256, 0, stream>>>((const uint16_t*)A, lda, (int)M, (int)K, Ap, (int)d.Kp, vecs);
         sbt_status st = sbt_after_launch(ctx, "gemm_bounded (stage A)");
         if (st) return st;
-    }
-    CUtensorMap tmB;
-    if (direct_b) {
-        sbt_status st = encode_direct_b(ctx, &tmB, B, ldb, K, N);
-        if (st) return st;
-    } else {
         dim3 g2((unsigned)(d.Kp / 64), (unsigned)(d.Np / 64));
         k_stage_bt<<<g2, 256, 0, stream>>>((const uint16_t*)B, ldb, (int)K, (int)N, Bp, (int)d.Kp);
-        sbt_status st = sbt_after_launch(ctx, "gemm_bounded (stage B)");
-        if (st) return st;
+        if ((st = sbt_after_launch(ctx, "gemm_bounded (stage B)"))) return st;
+        return launch_main(ctx, nullptr, nullptr, Ap, Bp, d, C, ldc, c_dtype == SBT_F32, nullptr, 0, M, N, K, stream);
     }
-    return launch_main(ctx, direct_a ? &tmA : nullptr, direct_b ? &tmB : nullptr, Ap, Bp, d, C, ldc,
-                       c_dtype == SBT_F32, nullptr, 0, M, N, K, stream);
+    // 1. operand staging.  An operand whose rows are 16-byte aligned is read by TMA where it
+    //    lies (SBT_PATH_AUTO / SBT_PATH_TMA); the others are copied, realigned and zero-padded,
+    //    by one launch: A' [Mp][Kp], and B'' [Kp][Np] in B's own orientation (the tensor-core
+    //    kernel reads B MN-major in both cases, so B needs no transpose).
+    const bool tma_ok = ctx->path == SBT_PATH_AUTO || ctx->path == SBT_PATH_TMA;
+    const bool direct_a = tma_ok && lda % 8 == 0 && (reinterpret_cast<uintptr_t>(A) & 15u) == 0;
+    const bool direct_b = tma_ok && ldb % 8 == 0 && (reinterpret_cast<uintptr_t>(B) & 15u) == 0;
+    CUtensorMap tmA, tmB;
+    sbt_status st = SBT_OK;
+    RowCopy ca = {}, cb = {};
+    if (direct_a) {
+        if ((st = encode_direct_a(ctx, &tmA, A, lda, M, K))) return st;
+    } else {
+        ca = {(const uint16_t*)A, lda, (int)M, (int)K, Ap, (int)d.Kp, d.Mp * (d.Kp / 8)};
+    }
+    if (direct_b) {
+        if ((st = encode_direct_b(ctx, &tmB, B, ldb, K, N))) return st;
+    } else {
+        cb = {(const uint16_t*)B, ldb, (int)K, (int)N, Bp, (int)d.Np, d.Kp * (d.Np / 8)};
+        if ((st = encode_direct_b(ctx, &tmB, Bp, d.Np, d.Kp, d.Np))) return st;
+    }
+    if (ca.vecs + cb.vecs > 0) {
+        const int grid = (int)std::min<int64_t>(sbt_cdiv(ca.vecs + cb.vecs, 256), (int64_t)ctx->sm_count * 8);
+        k_stage_ab<<<grid, 256, 0, stream>>>(ca, cb);
+        if ((st = sbt_after_launch(ctx, "gemm_bounded (stage A, B)"))) return st;
+    }
+    return launch_main(ctx, direct_a ? &tmA : nullptr, &tmB, Ap, Bp, d, C, ldc, c_dtype == SBT_F32, nullptr, 0, M, N,
+                       K, stream);
 }
 
 sbt_status sbt_launch_gemm_main(sbt_context* ctx, const uint16_t* Ap, const uint16_t* Bp, const sbt_gemm_layout& d,

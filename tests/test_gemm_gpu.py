@@ -106,14 +106,14 @@ ALIGNED_SHAPES = [(65, 97, 73), (1000, 1000, 1000), (300, 257, 129), (129, 600, 
                   (2304, 2500, 200), (4096, 2560, 128), (1, 8, 8), (200, 16, 1000)]
 
 
-@pytest.mark.parametrize("path", ["auto", "scalar"])
+@pytest.mark.parametrize("path", ["auto", "vector", "scalar"])
 @pytest.mark.parametrize("align", [(1, 0), (0, 1), (1, 1)])
 @pytest.mark.parametrize("mnk", ALIGNED_SHAPES)
 def test_aligned_rows_vs_oracle(ctx, mnk, align, path):
     """16-byte-aligned rows: under "auto" TMA reads that operand where it lies (A K-major,
     B MN-major in 64-column boxes; the K, M and N tails come from TMA's zero fill, the NaN
-    padding columns stay unread), under "scalar" both operands are staged.  Both meet the
-    gate, on the single-CTA and the CTA-pair kernel."""
+    padding columns stay unread), under "vector" both operands are copied realigned and under
+    "scalar" transposed.  All meet the gate, on the single-CTA and the CTA-pair kernel."""
     M, N, K = mnk
     ctx.set_path(path)
     g = gemm_aligned(M, N, K, tag=21, align_a=align[0], align_b=align[1], extra=8 if M == 300 else 0)
@@ -161,11 +161,28 @@ def test_aligned_stride_misaligned_pointers(ctx):
     sbt.gemm_bounded(ctx, A.data_ptr() + 2, g["lda"], B.data_ptr() + 2, g["ldb"], C, ldc, M, N, K, ws, ws_n)
     sync()
     ctx.check_status()
-    assert ctx.launch_count - before == 3  # both staging kernels and the tensor-core kernel
+    assert ctx.launch_count - before == 2  # one staging launch for both operands, then the tensor-core kernel
     got = synth.bf16_bits_to_f32(host(C, np.uint16, (M, ldc))[:, :N]).astype(np.float64)
     ref = oracle.gemm_f64(g["A"], g["lda"], g["B"], g["ldb"], M, N, K)
     ref_b = synth.bf16_bits_to_f32(oracle.round_bf16(ref)).astype(np.float64)
     assert rel_fro(got, ref_b) <= TOL
+
+
+@pytest.mark.parametrize("mnk", [(1000, 1000, 1000), (2304, 2500, 200), (65, 97, 73)])
+def test_staging_paths(ctx, mnk):
+    """Odd leading dimensions, three ways to stage: "auto" and "vector" copy A and B realigned
+    (B kept in its own orientation, read MN-major), so their C is identical bit for bit;
+    "scalar" transposes B into K-major rows first.  All three meet the gate."""
+    M, N, K = mnk
+    g = wl.gemm_bf16(M=M, N=N, K=K, tag=25)
+    ref = oracle.gemm_f64(g["A"], g["lda"], g["B"], g["ldb"], M, N, K)
+    ref_b = synth.bf16_bits_to_f32(oracle.round_bf16(ref)).astype(np.float64)
+    bits = {}
+    for path in ("auto", "vector", "scalar"):
+        ctx.set_path(path)
+        got, bits[path] = run_gemm(ctx, g, "bf16")
+        assert rel_fro(got, ref_b) <= TOL, path
+    assert np.array_equal(bits["auto"], bits["vector"])
 
 
 def test_many_tiles_with_m_tail(ctx):
