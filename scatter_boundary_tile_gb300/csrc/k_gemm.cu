@@ -91,16 +91,24 @@ __device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, 
 // round (or keep fp32) and store rows row0.. of C through a padded shared
 // transpose so that each store instruction covers 32 consecutive columns.
 // A bf16 C is rounded before the transpose, which then moves half the bytes
-// (shared memory is the resource the main loop competes for).
+// (shared memory is the resource the main loop competes for).  The TMEM load
+// of the next 32 columns is in flight while the current ones are stored, and
+// the 32 rows of a chunk are read from shared memory and stored with
+// independent, unrolled instructions (rows past M and columns past N masked).
 template <int BN_>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tmem_acc, int q, int lane, float* buf,
                                               int row0, int n0) {
     const int n_valid = min(BN_, p.N - n0);
     const int chunks = (n_valid + 31) / 32;
+    const int rows = p.M - row0;  // rows of this warp's 32 that lie inside C (may be <= 0)
+    const uint32_t taddr = tmem_acc + ((uint32_t)(q * 32) << 16);
+    uint32_t r[32], rn[32];
+    if (chunks > 0) tmem_ld_32x32b_x32(taddr, r);
+#pragma unroll 1
     for (int c = 0; c < chunks; ++c) {
-        uint32_t r[32];
-        tmem_ld_32x32b_x32(tmem_acc + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
         tmem_ld_wait();
+        const int col = n0 + c * 32 + lane;
+        const bool col_ok = col < p.N;
         if (!p.c_f32) {
             // [32 rows][17 words]: row `lane` packs its 32 columns as bf16 pairs; odd padding keeps
             // the row-wise writes and the column-wise reads free of bank conflicts.
@@ -110,39 +118,49 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tmem
                 const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
                 wb[lane * 17 + j] = *reinterpret_cast<const uint32_t*>(&v);
             }
+            if (c + 1 < chunks) tmem_ld_32x32b_x32(taddr + (uint32_t)((c + 1) * 32), rn);
             __syncwarp();
-            const int col = n0 + c * 32 + lane;
-            if (col < p.N) {
-                uint16_t* Cp = reinterpret_cast<uint16_t*>(p.C);
-                for (int rr = 0; rr < 32 && row0 + rr < p.M; ++rr) {
-                    const uint32_t w = wb[rr * 17 + (lane >> 1)];
-                    Cp[(int64_t)(row0 + rr) * p.ldc + col] = (uint16_t)((lane & 1) ? (w >> 16) : (w & 0xFFFFu));
+            uint16_t* Cp = reinterpret_cast<uint16_t*>(p.C) + (int64_t)row0 * p.ldc + col;
+            const int sh = (lane & 1) * 16;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                uint32_t w[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) w[i] = wb[(16 * h + i) * 17 + (lane >> 1)];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    if (col_ok && 16 * h + i < rows) *Cp = (uint16_t)(w[i] >> sh);
+                    Cp += p.ldc;
                 }
             }
-            __syncwarp();
-            continue;
-        }
+        } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) buf[lane * 33 + j] = __uint_as_float(r[j]);
-        __syncwarp();
-        const int col = n0 + c * 32 + lane;
-        if (col < p.N) {  // fp32 C
-            float* Cp = reinterpret_cast<float*>(p.C);
-            if (p.acc) {
-                for (int rr = 0; rr < 32 && row0 + rr < p.M; ++rr)
-                    Cp[(int64_t)(row0 + rr) * p.ldc + col] =
-                        buf[rr * 33 + lane] + __ldg(p.acc + (int64_t)(row0 + rr) * p.ld_acc + col);
-            } else {
-                for (int rr = 0; rr < 32 && row0 + rr < p.M; ++rr)
-                    Cp[(int64_t)(row0 + rr) * p.ldc + col] = buf[rr * 33 + lane];
+            for (int j = 0; j < 32; ++j) buf[lane * 33 + j] = __uint_as_float(r[j]);
+            if (c + 1 < chunks) tmem_ld_32x32b_x32(taddr + (uint32_t)((c + 1) * 32), rn);
+            __syncwarp();
+            float* Cp = reinterpret_cast<float*>(p.C) + (int64_t)row0 * p.ldc + col;
+            const float* Ap = p.acc ? p.acc + (int64_t)row0 * p.ld_acc + col : nullptr;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                float v[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = buf[(16 * h + i) * 33 + lane];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    if (col_ok && 16 * h + i < rows) *Cp = Ap ? v[i] + __ldg(Ap) : v[i];
+                    Cp += p.ldc;
+                    if (Ap) Ap += p.ld_acc;
+                }
             }
         }
         __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = rn[j];
     }
 }
 
 template <int BN_>
-__global__ void __launch_bounds__(kGemmThreads, 1)
+__global__ void __maxnreg__(168)
     k_gemm_bf16_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p) {
     typedef TcShape<BN_> S;
@@ -355,7 +373,7 @@ constexpr int kNumBars2 = 2 * kStages2 + 5;
 constexpr size_t kGemmSmem2 = 1024 + (size_t)kStages2 * kStageBytes2 + (size_t)kEpiWarps * kEpiWords * 4 +
                               kNumBars2 * 8 + 16;
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
     k_gemm_bf16_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -527,6 +545,198 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc_pair(tmem_base, kTmemCols2);
+    }
+}
+
+// ---------------------------------------------------------------------------- CTA-pair kernel, 512 x 256 tiles
+//
+// The 256 x 256 pair tile above asks each SM for 512 B of operands per K
+// element (128 rows of A, 128 columns of B); measured per-stage timelines show
+// an SM taking in about 45 B per cycle from L2 through TMA whatever the stage
+// size, against 64 B per cycle for the tensor pipe at full rate, so that
+// kernel waits on its loads ~30% of the time.  Here each CTA of the pair holds
+// 256 rows of A and 128 columns of B (768 B per K element for twice the
+// MMAs, 48 B per cycle at full rate): every K = 16 step issues two
+// tcgen05.mma.cta_group::2 of M = 256, N = 256 (the pair's row halves h = 0,
+// 1), accumulating into TMEM columns h*256 .. h*256 + 255 of each CTA.  The
+// two accumulators fill TMEM, so the epilogue of a tile (eight warps, two per
+// TMEM lane quarter) runs between tiles instead of under the next main loop.
+
+#ifndef SBT_GEMM_PAIR512
+#define SBT_GEMM_PAIR512 1
+#endif
+constexpr bool kPair512 = SBT_GEMM_PAIR512 != 0;  // build switch for measuring the two pair kernels against each other
+constexpr int kStages3 = 4;
+constexpr uint32_t kA3Bytes = 2 * kHalfBytes;            // this CTA's 256 rows of A, one K step
+constexpr uint32_t kStageBytes3 = kA3Bytes + kHalfBytes; // + its 128 columns of B: 48 KB
+constexpr int kEpiWarps3 = 8;
+constexpr int kGemmThreads3 = 64 + 32 * kEpiWarps3;
+constexpr int kNumBars3 = 2 * kStages3 + 3;
+constexpr size_t kGemmSmem3 = 1024 + (size_t)kStages3 * kStageBytes3 + (size_t)kEpiWarps3 * kEpiWords * 4 +
+                              kNumBars3 * 8 + 16;
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads3, 1)
+    k_gemm_bf16_tc_pair512(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                           const GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    float* epi = reinterpret_cast<float*>(smem + (size_t)kStages3 * kStageBytes3);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(epi + kEpiWarps3 * kEpiWords);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars3);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const uint32_t bar0 = smem_u32(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (kStages3 + s); };
+    const uint32_t tfull_bar = bar0 + 8u * (2 * kStages3);
+    const uint32_t tempty_bar = bar0 + 8u * (2 * kStages3 + 1);
+    const uint32_t mma_done_bar = bar0 + 8u * (2 * kStages3 + 2);
+
+    const int warp = __shfl_sync(0xffffffffu, (int)(threadIdx.x / 32), 0);
+    const int lane = threadIdx.x % 32;
+    const uint32_t rank = cluster_ctarank();
+    const int cluster = blockIdx.x >> 1, nclusters = gridDim.x >> 1;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages3; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        mbar_init(tfull_bar, 1);
+        mbar_init(tempty_bar, 2 * kEpiWarps3 * 32);
+        mbar_init(mma_done_bar, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(tmem_slot), 512);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    cluster_sync();  // both CTAs' barriers are initialised before any remote arrival
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_slot;
+    griddep_wait();
+    const int num_tiles = p.m_tiles * p.n_tiles;  // 512 x 256 tiles
+
+    if (warp == 0) {
+        // ------------------------------------------------------------ TMA producer (each CTA, own rows and columns)
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            bool ok = true;
+            int64_t issued = 0;
+            for (int tile = cluster; ok && tile < num_tiles; tile += nclusters) {
+                int mt, nt;
+                tile_coords(tile, p.m_tiles, p.n_tiles, &mt, &nt);
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait_bounded(empty_bar(stage), phase ^ 1u, p.wait_ns, abort_flag, p.status,
+                                           kCodeProducer)) {
+                        ok = false;
+                        break;
+                    }
+                    const bool withhold = p.withhold_first_load && blockIdx.x == 0 && issued == 0;
+                    ++issued;
+                    if (!withhold) {
+                        const uint32_t sa = smem_u32(smem + (size_t)stage * kStageBytes3);
+                        const uint32_t leader_full = mapa_shared(full_bar(stage), 0);
+                        if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * kStageBytes3);
+                        for (int h = 0; h < 2; ++h)
+                            tma_load_2d_pair(sa + h * kHalfBytes, &tmA, kb * BK, mt * 512 + (int)rank * 256 + h * 128,
+                                             leader_full);
+                        if (p.b_mn) {
+                            for (int a = 0; a < 2; ++a)
+                                tma_load_2d_pair(sa + kA3Bytes + a * kMnAtomBytes, &tmB, nt * 256 + (int)rank * 128 + 64 * a,
+                                                 kb * BK, leader_full);
+                        } else {
+                            tma_load_2d_pair(sa + kA3Bytes, &tmB, kb * BK, nt * 256 + (int)rank * 128, leader_full);
+                        }
+                    }
+                    if (++stage == kStages3) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------------------ MMA issuer (leader CTA only)
+        if (lane == 0 && rank == 0) {
+            uint32_t stage = 0, phase = 0;
+            int local = 0;
+            bool ok = true;
+            const uint32_t idesc = idesc_bf16_f32(256, 256) | (p.b_mn ? kIdescBMnMajor : 0u);
+            for (int tile = cluster; ok && tile < num_tiles; tile += nclusters, ++local) {
+                // both accumulators are free once the previous tile's epilogue has read them
+                if (!mbar_wait_bounded(tempty_bar, ((uint32_t)local & 1u) ^ 1u, p.wait_ns, abort_flag, p.status,
+                                       kCodeMma)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait_bounded(full_bar(stage), phase, p.wait_ns, abort_flag, p.status, kCodeMma)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const int k_rem = p.K - kb * BK;
+                    const int k_steps = k_rem >= BK ? BK / 16 : (k_rem + 15) / 16;
+                    const uint32_t sa = smem_u32(smem + (size_t)stage * kStageBytes3);
+                    const uint32_t sb = sa + kA3Bytes;
+                    for (int ks = 0; ks < k_steps; ++ks) {
+                        const uint64_t bd = p.b_mn ? smem_desc_mn_sw128(sb + kMnKStepBytes * ks, kMnAtomBytes)
+                                                   : smem_desc_sw128(sb + 32u * ks);
+                        for (int h = 0; h < 2; ++h)
+                            tc_mma_f16_pair(tmem_base + (uint32_t)(h * 256), smem_desc_sw128(sa + h * kHalfBytes + 32u * ks),
+                                            bd, idesc, (kb | ks) != 0 ? 1u : 0u);
+                    }
+                    tc_commit_pair_multicast(empty_bar(stage), 0x3);
+                    if (++stage == kStages3) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (ok) tc_commit_pair_multicast(tfull_bar, 0x3);
+            }
+            tc_commit_pair_multicast(mma_done_bar, 0x1);
+            const uint64_t t0 = globaltimer();
+            while (!mbar_try_wait(mma_done_bar, 0)) {
+                if (globaltimer() - t0 > p.wait_ns) {
+                    atomicOr(p.status, (unsigned int)kCodeTeardown);
+                    break;
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ epilogue (warps 2..9 of each CTA)
+        // warp w reads TMEM lane quarter w % 4 (rows q*32 .. q*32 + 31 of each row half) and
+        // columns half*128 .. half*128 + 127 of both accumulators
+        const int q = warp & 3;
+        const int half = (warp - 2) >> 2;
+        float* buf = epi + (warp - 2) * kEpiWords;
+        int local = 0;
+        for (int tile = cluster; tile < num_tiles; tile += nclusters, ++local) {
+            int mt, nt;
+            tile_coords(tile, p.m_tiles, p.n_tiles, &mt, &nt);
+            if (!mbar_wait_bounded(tfull_bar, (uint32_t)local & 1u, p.wait_ns, abort_flag, p.status, kCodeEpilogue))
+                break;
+            tc_fence_after();
+            for (int h = 0; h < 2; ++h)
+                epilogue_tile<128>(p, tmem_base + (uint32_t)(h * 256 + half * 128), q, lane, buf,
+                                   mt * 512 + (int)rank * 256 + h * 128 + q * 32, nt * 256 + half * 128);
+            tc_fence_before();
+            mbar_arrive_cluster(mapa_shared(tempty_bar, 0));
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync();  // the leader's MMAs into the peer's TMEM are complete before either CTA frees it
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, 512);
     }
 }
 
@@ -862,15 +1072,21 @@ sbt_status launch_main(sbt_context* ctx, const CUtensorMap* tmA_direct, const CU
                                      (int)TcShape<64>::kSmem);
         if (e != cudaSuccess) return sbt_cuda_check(e, "cudaFuncSetAttribute(gemm smem)");
         e = cudaFuncSetAttribute(k_gemm_bf16_tc_pair, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem2);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k_gemm_bf16_tc_pair512, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kGemmSmem3);
         if (e != cudaSuccess) return sbt_cuda_check(e, "cudaFuncSetAttribute(gemm pair smem)");
         attr_set[ctx->device & 63] = true;
     }
     if (pair) {
-        p.m_tiles = (int)(d.Mp / 256);
+        // 512 x 256 tiles (two row halves per CTA) unless that leaves fewer tiles than CTA pairs
+        const bool wide = sbt_cdiv(d.Mp, 512) * (d.Np / 256) >= ctx->sm_count / 2 && kPair512;
+        p.m_tiles = (int)(wide ? sbt_cdiv(d.Mp, 512) : d.Mp / 256);
         const int tiles = p.m_tiles * p.n_tiles;
-        // as many CTA pairs as can be resident at once (queried once per device)
-        static int max_clusters[64] = {0};
-        if (!max_clusters[ctx->device & 63]) {
+        // as many CTA pairs as can be resident at once (queried once per device and kernel)
+        static int max_clusters[2][64] = {{0}};
+        int& mc = max_clusters[wide ? 1 : 0][ctx->device & 63];
+        if (!mc) {
             cudaLaunchConfig_t cfg = {};
             cudaLaunchAttribute attr;
             attr.id = cudaLaunchAttributeClusterDimension;
@@ -878,20 +1094,25 @@ sbt_status launch_main(sbt_context* ctx, const CUtensorMap* tmA_direct, const CU
             attr.val.clusterDim.y = 1;
             attr.val.clusterDim.z = 1;
             cfg.gridDim = dim3(2 * (unsigned)(ctx->sm_count / 2), 1, 1);
-            cfg.blockDim = dim3(kGemmThreads, 1, 1);
-            cfg.dynamicSmemBytes = kGemmSmem2;
+            cfg.blockDim = dim3(wide ? kGemmThreads3 : kGemmThreads, 1, 1);
+            cfg.dynamicSmemBytes = wide ? kGemmSmem3 : kGemmSmem2;
             cfg.attrs = &attr;
             cfg.numAttrs = 1;
             int n = 0;
-            if (cudaOccupancyMaxActiveClusters(&n, k_gemm_bf16_tc_pair, &cfg) != cudaSuccess || n < 1) {
+            const cudaError_t qe = wide ? cudaOccupancyMaxActiveClusters(&n, k_gemm_bf16_tc_pair512, &cfg)
+                                        : cudaOccupancyMaxActiveClusters(&n, k_gemm_bf16_tc_pair, &cfg);
+            if (qe != cudaSuccess || n < 1) {
                 (void)cudaGetLastError();
                 n = ctx->sm_count / 2;
             }
-            max_clusters[ctx->device & 63] = n;
+            mc = n;
         }
-        const int clusters = std::min(tiles, max_clusters[ctx->device & 63]);
-        const cudaError_t e = sbt_launch_dependent(k_gemm_bf16_tc_pair, dim3(2 * clusters), dim3(kGemmThreads),
-                                                   kGemmSmem2, stream, tmA, tmB, p);
+        const int clusters = std::min(tiles, mc);
+        const cudaError_t e =
+            wide ? sbt_launch_dependent(k_gemm_bf16_tc_pair512, dim3(2 * clusters), dim3(kGemmThreads3), kGemmSmem3,
+                                        stream, tmA, tmB, p)
+                 : sbt_launch_dependent(k_gemm_bf16_tc_pair, dim3(2 * clusters), dim3(kGemmThreads), kGemmSmem2,
+                                        stream, tmA, tmB, p);
         if (e != cudaSuccess) return sbt_cuda_check(e, "gemm_bounded (tcgen05, CTA pairs)");
         return sbt_after_launch(ctx, "gemm_bounded (tcgen05, CTA pairs)");
     }

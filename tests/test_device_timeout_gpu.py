@@ -36,7 +36,8 @@ def expect_timeout(ctx, launch):
     ctx.check_status()  # the flag was cleared by the read above
 
 
-@pytest.mark.parametrize("mnk", [(1000, 1000, 1000), (2048, 2560, 256)], ids=["single_cta", "cta_pair"])
+@pytest.mark.parametrize("mnk", [(1000, 1000, 1000), (2048, 2560, 256), (4096, 2560, 256)],
+                         ids=["single_cta", "cta_pair", "cta_pair_512_rows"])
 def test_gemm_wait_runs_out_then_recovers(ctx, mnk):
     M, N, K = mnk
     g = wl.gemm_bf16(M=M, N=N, K=K, tag=21)
