@@ -1079,8 +1079,10 @@ sbt_status launch_main(sbt_context* ctx, const CUtensorMap* tmA_direct, const CU
         attr_set[ctx->device & 63] = true;
     }
     if (pair) {
-        // 512 x 256 tiles (two row halves per CTA) unless that leaves fewer tiles than CTA pairs
-        const bool wide = sbt_cdiv(d.Mp, 512) * (d.Np / 256) >= ctx->sm_count / 2 && kPair512;
+        // 512 x 256 tiles (two row halves per CTA) for a bf16 C, unless that leaves fewer tiles than
+        // CTA pairs.  Their epilogue runs between tiles; an fp32 C (twice the bytes to store, an odd
+        // row stride) measured faster on the 256 x 256 kernel, whose epilogue overlaps the next tile.
+        const bool wide = kPair512 && !c_f32 && sbt_cdiv(d.Mp, 512) * (d.Np / 256) >= ctx->sm_count / 2;
         p.m_tiles = (int)(wide ? sbt_cdiv(d.Mp, 512) : d.Mp / 256);
         const int tiles = p.m_tiles * p.n_tiles;
         // as many CTA pairs as can be resident at once (queried once per device and kernel)
