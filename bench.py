@@ -641,6 +641,19 @@ def run_ops(ctx, pk):
     return ops
 
 
+def box_record(device_index: int):
+    """Which machine and GPU produced this line (host-link and clock behaviour differ by box)."""
+    import socket
+    import torch
+    rec = {"host": socket.gethostname()}
+    try:
+        pr = torch.cuda.get_device_properties(device_index)
+        rec.update(gpu=pr.name, gpu_uuid=str(pr.uuid), pci_bus_id=int(pr.pci_bus_id), sm_count=pr.multi_processor_count)
+    except Exception:
+        pass
+    return rec
+
+
 def clocks_record(smi: ClockSampler, nvml: NvmlClockSampler):
     """nvidia-smi samples (100 ms) of the timed region, refined by NVML samples taken every
     0.5 ms when the region is too short for nvidia-smi: the SM clock median and the
@@ -828,6 +841,7 @@ def run_sbt(args, dist):
                 "note": "inputs copied host->device and the output device->host every step; steps pipelined "
                         "over two buffer sets (upload of step i+1 overlaps download of step i)"},
         "clocks": clocks_record(sampler, fine),
+        "box": box_record(torch.cuda.current_device()),
     }
     if not args.no_ops:
         del out, t_dev

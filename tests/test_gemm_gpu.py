@@ -197,6 +197,25 @@ def test_many_tiles_with_m_tail(ctx):
     assert rel_fro(got, ref_b) <= TOL
 
 
+@pytest.mark.parametrize("mnk,c_dtype", [((200, 19500, 72), "bf16"), ((600, 12000, 100), "bf16"),
+                                         ((4096, 2560, 128), "f32"), ((2500, 2560, 300), "f32")])
+def test_pair_kernels_edges(ctx, mnk, c_dtype):
+    """CTA-pair shapes at the edges of the 512 x 256 kernel: (200, 19500) has one 512-row tile
+    whose second CTA holds no row < M at all; (600, 12000) a second row tile with 88 valid rows;
+    an fp32 C takes the 256 x 256 kernel (its epilogue overlaps the next tile)."""
+    M, N, K = mnk
+    g = wl.gemm_bf16(M=M, N=N, K=K, tag=26)
+    got, _ = run_gemm(ctx, g, c_dtype)
+    rng = np.random.default_rng(2)
+    ms = np.concatenate([rng.integers(0, M, 3000), np.arange(M - 8, M)])
+    ns = np.concatenate([rng.integers(0, N, 3000), np.arange(N - 8, N)])
+    ref = oracle.gemm_f64_at(g["A"], g["lda"], g["B"], g["ldb"], K, ms, ns)
+    if c_dtype == "bf16":
+        ref = synth.bf16_bits_to_f32(oracle.round_bf16(ref)).astype(np.float64)
+    assert rel_fro(got[ms, ns], ref) <= TOL
+    assert not np.isnan(got).any()
+
+
 def test_many_tiles_per_block(ctx):
     """CTA-pair kernel (M, N >= 512) with more 256 x 256 tiles than CTA pairs: the persistent
     loop and both TMEM accumulators are used."""
