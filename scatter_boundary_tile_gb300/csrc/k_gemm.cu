@@ -562,10 +562,6 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
 // two accumulators fill TMEM, so the epilogue of a tile (eight warps, two per
 // TMEM lane quarter) runs between tiles instead of under the next main loop.
 
-#ifndef SBT_GEMM_PAIR512
-#define SBT_GEMM_PAIR512 1
-#endif
-constexpr bool kPair512 = SBT_GEMM_PAIR512 != 0;  // build switch for measuring the two pair kernels against each other
 constexpr int kStages3 = 4;
 constexpr uint32_t kA3Bytes = 2 * kHalfBytes;            // this CTA's 256 rows of A, one K step
 constexpr uint32_t kStageBytes3 = kA3Bytes + kHalfBytes; // + its 128 columns of B: 48 KB
@@ -1082,7 +1078,7 @@ sbt_status launch_main(sbt_context* ctx, const CUtensorMap* tmA_direct, const CU
         // 512 x 256 tiles (two row halves per CTA) for a bf16 C, unless that leaves fewer tiles than
         // CTA pairs.  Their epilogue runs between tiles; an fp32 C (twice the bytes to store, an odd
         // row stride) measured faster on the 256 x 256 kernel, whose epilogue overlaps the next tile.
-        const bool wide = kPair512 && !c_f32 && sbt_cdiv(d.Mp, 512) * (d.Np / 256) >= ctx->sm_count / 2;
+        const bool wide = !c_f32 && sbt_cdiv(d.Mp, 512) * (d.Np / 256) >= ctx->sm_count / 2;
         p.m_tiles = (int)(wide ? sbt_cdiv(d.Mp, 512) : d.Mp / 256);
         const int tiles = p.m_tiles * p.n_tiles;
         // as many CTA pairs as can be resident at once (queried once per device and kernel)
