@@ -69,7 +69,6 @@ struct GemmParams {
     unsigned int* status;
     uint64_t wait_ns;
     int withhold_first_load;  // test hook: block 0 never issues its first stage
-    int b_mn;                 // B read by TMA where it lies (MN-major boxes of 64 columns), not from B'^T
 };
 
 // Tile order: groups of kGroupM M-tiles are walked N column by N column, so the
@@ -91,24 +90,19 @@ __device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, 
 // round (or keep fp32) and store rows row0.. of C through a padded shared
 // transpose so that each store instruction covers 32 consecutive columns.
 // A bf16 C is rounded before the transpose, which then moves half the bytes
-// (shared memory is the resource the main loop competes for).  The TMEM load
-// of the next 32 columns is in flight while the current ones are stored, and
-// the 32 rows of a chunk are read from shared memory and stored with
-// independent, unrolled instructions (rows past M and columns past N masked).
+// (shared memory is the resource the main loop competes for).  This epilogue
+// runs under the next tile's main loop; a version that stored 16 rows at a
+// time with the next TMEM load in flight slowed the 256 x 256 pair kernel
+// with an fp32 C from 0.338 to 0.375 ms (its stores contend with the loop).
 template <int BN_>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tmem_acc, int q, int lane, float* buf,
                                               int row0, int n0) {
     const int n_valid = min(BN_, p.N - n0);
     const int chunks = (n_valid + 31) / 32;
-    const int rows = p.M - row0;  // rows of this warp's 32 that lie inside C (may be <= 0)
-    const uint32_t taddr = tmem_acc + ((uint32_t)(q * 32) << 16);
-    uint32_t r[32], rn[32];
-    if (chunks > 0) tmem_ld_32x32b_x32(taddr, r);
-#pragma unroll 1
     for (int c = 0; c < chunks; ++c) {
+        uint32_t r[32];
+        tmem_ld_32x32b_x32(tmem_acc + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
         tmem_ld_wait();
-        const int col = n0 + c * 32 + lane;
-        const bool col_ok = col < p.N;
         if (!p.c_f32) {
             // [32 rows][17 words]: row `lane` packs its 32 columns as bf16 pairs; odd padding keeps
             // the row-wise writes and the column-wise reads free of bank conflicts.
@@ -118,49 +112,42 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tmem
                 const __nv_bfloat162 v = __floats2bfloat162_rn(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
                 wb[lane * 17 + j] = *reinterpret_cast<const uint32_t*>(&v);
             }
-            if (c + 1 < chunks) tmem_ld_32x32b_x32(taddr + (uint32_t)((c + 1) * 32), rn);
             __syncwarp();
-            uint16_t* Cp = reinterpret_cast<uint16_t*>(p.C) + (int64_t)row0 * p.ldc + col;
-            const int sh = (lane & 1) * 16;
-#pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                uint32_t w[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) w[i] = wb[(16 * h + i) * 17 + (lane >> 1)];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    if (col_ok && 16 * h + i < rows) *Cp = (uint16_t)(w[i] >> sh);
-                    Cp += p.ldc;
+            const int col = n0 + c * 32 + lane;
+            if (col < p.N) {
+                uint16_t* Cp = reinterpret_cast<uint16_t*>(p.C);
+                for (int rr = 0; rr < 32 && row0 + rr < p.M; ++rr) {
+                    const uint32_t w = wb[rr * 17 + (lane >> 1)];
+                    Cp[(int64_t)(row0 + rr) * p.ldc + col] = (uint16_t)((lane & 1) ? (w >> 16) : (w & 0xFFFFu));
                 }
             }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) buf[lane * 33 + j] = __uint_as_float(r[j]);
-            if (c + 1 < chunks) tmem_ld_32x32b_x32(taddr + (uint32_t)((c + 1) * 32), rn);
             __syncwarp();
-            float* Cp = reinterpret_cast<float*>(p.C) + (int64_t)row0 * p.ldc + col;
-            const float* Ap = p.acc ? p.acc + (int64_t)row0 * p.ld_acc + col : nullptr;
+            continue;
+        }
 #pragma unroll
-            for (int h = 0; h < 2; ++h) {
-                float v[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = buf[(16 * h + i) * 33 + lane];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    if (col_ok && 16 * h + i < rows) *Cp = Ap ? v[i] + __ldg(Ap) : v[i];
-                    Cp += p.ldc;
-                    if (Ap) Ap += p.ld_acc;
-                }
+        for (int j = 0; j < 32; ++j) buf[lane * 33 + j] = __uint_as_float(r[j]);
+        __syncwarp();
+        const int col = n0 + c * 32 + lane;
+        if (col < p.N) {  // fp32 C
+            float* Cp = reinterpret_cast<float*>(p.C);
+            if (p.acc) {
+                for (int rr = 0; rr < 32 && row0 + rr < p.M; ++rr)
+                    Cp[(int64_t)(row0 + rr) * p.ldc + col] =
+                        buf[rr * 33 + lane] + __ldg(p.acc + (int64_t)(row0 + rr) * p.ld_acc + col);
+            } else {
+                for (int rr = 0; rr < 32 && row0 + rr < p.M; ++rr)
+                    Cp[(int64_t)(row0 + rr) * p.ldc + col] = buf[rr * 33 + lane];
             }
         }
         __syncwarp();
-#pragma unroll
-        for (int j = 0; j < 32; ++j) r[j] = rn[j];
     }
 }
 
-template <int BN_>
-__global__ void __maxnreg__(168)
+// BMN: B is read MN-major (TMA boxes of 64 columns), else K-major rows of B'^T.  A template
+// parameter, not a kernel argument: a branch on it in the single-thread TMA and MMA issue
+// loops measured ~6% slower on the 256 x 256 pair kernel.
+template <int BN_, bool BMN>
+__global__ void __launch_bounds__(kGemmThreads, 1)
     k_gemm_bf16_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const GemmParams p) {
     typedef TcShape<BN_> S;
@@ -239,7 +226,7 @@ __global__ void __maxnreg__(168)
                     }
                     mbar_arrive_expect_tx(full_bar(stage), kStageBytes);
                     tma_load_2d(sa, &tmA, kb * BK, mt * BM, full_bar(stage));
-                    if (p.b_mn) {
+                    if (BMN) {
 #pragma unroll
                         for (int a = 0; a < BN_ / 64; ++a)
                             tma_load_2d(sa + kABytes + a * kMnAtomBytes, &tmB, nt * BN_ + 64 * a, kb * BK,
@@ -283,7 +270,7 @@ __global__ void __maxnreg__(168)
                 tile_coords(tile, p.m_tiles, p.n_tiles, &mt_unused, &nt);
                 const int n_valid = min(BN_, p.N - nt * BN_);
                 const uint32_t idesc =
-                    idesc_bf16_f32(BM, (uint32_t)((n_valid + 15) & ~15)) | (p.b_mn ? kIdescBMnMajor : 0u);
+                    idesc_bf16_f32(BM, (uint32_t)((n_valid + 15) & ~15)) | (BMN ? kIdescBMnMajor : 0u);
                 if (!mbar_wait_bounded(tempty_bar(acc), (use & 1u) ^ 1u, p.wait_ns, abort_flag, p.status,
                                        kCodeMma)) {
                     ok = false;
@@ -302,7 +289,7 @@ __global__ void __maxnreg__(168)
                     const uint32_t sa = smem_u32(smem + (size_t)stage * kStageBytes);
                     const uint32_t sb = sa + kABytes;
                     for (int ks = 0; ks < k_steps; ++ks) {
-                        const uint64_t bd = p.b_mn ? smem_desc_mn_sw128(sb + kMnKStepBytes * ks, kMnAtomBytes)
+                        const uint64_t bd = BMN ? smem_desc_mn_sw128(sb + kMnKStepBytes * ks, kMnAtomBytes)
                                                    : smem_desc_sw128(sb + 32u * ks);
                         tc_mma_f16(d_tmem, smem_desc_sw128(sa + 32u * ks), bd, idesc,
                                    (kb | ks) != 0 ? 1u : 0u);
@@ -373,7 +360,8 @@ constexpr int kNumBars2 = 2 * kStages2 + 5;
 constexpr size_t kGemmSmem2 = 1024 + (size_t)kStages2 * kStageBytes2 + (size_t)kEpiWarps * kEpiWords * 4 +
                               kNumBars2 * 8 + 16;
 
-__global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
+template <bool BMN>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads, 1)
     k_gemm_bf16_tc_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const GemmParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -447,7 +435,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
                         if (rank == 0) mbar_arrive_expect_tx(full_bar(stage), 2 * nkb * 2 * kHalfBytes);
                         for (int j = 0; j < nkb; ++j) {
                             tma_load_2d_pair(sa + j * kHalfBytes, &tmA, (kb0 + j) * BK, mt * 256 + (int)rank * 128, leader_full);
-                            if (p.b_mn) {
+                            if (BMN) {
                                 for (int a = 0; a < 2; ++a)
                                     tma_load_2d_pair(sa + (kKB2 + j) * kHalfBytes + a * kMnAtomBytes, &tmB,
                                                      nt * 256 + (int)rank * 128 + 64 * a, (kb0 + j) * BK, leader_full);
@@ -470,7 +458,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
             uint32_t stage = 0, phase = 0;
             int local = 0;
             bool ok = true;
-            const uint32_t idesc = idesc_bf16_f32(256, 256) | (p.b_mn ? kIdescBMnMajor : 0u);
+            const uint32_t idesc = idesc_bf16_f32(256, 256) | (BMN ? kIdescBMnMajor : 0u);
             for (int tile = cluster; ok && tile < num_tiles; tile += nclusters, ++local) {
                 const int acc = local & 1;
                 const uint32_t use = (uint32_t)(local >> 1);
@@ -496,7 +484,7 @@ __global__ void __cluster_dims__(2, 1, 1) __maxnreg__(168)
                     const uint32_t sa = sa0 + j * kHalfBytes;
                     const uint32_t sb = sa0 + (kKB2 + j) * kHalfBytes;
                     for (int ks = 0; ks < k_steps; ++ks) {
-                        const uint64_t bd = p.b_mn ? smem_desc_mn_sw128(sb + kMnKStepBytes * ks, kMnAtomBytes)
+                        const uint64_t bd = BMN ? smem_desc_mn_sw128(sb + kMnKStepBytes * ks, kMnAtomBytes)
                                                    : smem_desc_sw128(sb + 32u * ks);
                         tc_mma_f16_pair(d_tmem, smem_desc_sw128(sa + 32u * ks), bd,
                                         idesc, (kb | ks) != 0 ? 1u : 0u);
@@ -573,6 +561,7 @@ constexpr int kNumBars3 = 2 * kStages3 + 3;
 constexpr size_t kGemmSmem3 = 1024 + (size_t)kStages3 * kStageBytes3 + (size_t)kEpiWarps3 * kEpiWords3 * 4 +
                               kNumBars3 * 8 + 16;
 
+template <bool BMN>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads3, 1)
     k_gemm_bf16_tc_pair512(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                            const GemmParams p) {
@@ -643,7 +632,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads3, 1)
                         for (int h = 0; h < 2; ++h)
                             tma_load_2d_pair(sa + h * kHalfBytes, &tmA, kb * BK, mt * 512 + (int)rank * 256 + h * 128,
                                              leader_full);
-                        if (p.b_mn) {
+                        if (BMN) {
                             for (int a = 0; a < 2; ++a)
                                 tma_load_2d_pair(sa + kA3Bytes + a * kMnAtomBytes, &tmB, nt * 256 + (int)rank * 128 + 64 * a,
                                                  kb * BK, leader_full);
@@ -664,7 +653,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads3, 1)
             uint32_t stage = 0, phase = 0;
             int local = 0;
             bool ok = true;
-            const uint32_t idesc = idesc_bf16_f32(256, 256) | (p.b_mn ? kIdescBMnMajor : 0u);
+            const uint32_t idesc = idesc_bf16_f32(256, 256) | (BMN ? kIdescBMnMajor : 0u);
             for (int tile = cluster; ok && tile < num_tiles; tile += nclusters, ++local) {
                 // both accumulators are free once the previous tile's epilogue has read them
                 if (!mbar_wait_bounded(tempty_bar, ((uint32_t)local & 1u) ^ 1u, p.wait_ns, abort_flag, p.status,
@@ -684,7 +673,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kGemmThreads3, 1)
                     const uint32_t sa = smem_u32(smem + (size_t)stage * kStageBytes3);
                     const uint32_t sb = sa + kA3Bytes;
                     for (int ks = 0; ks < k_steps; ++ks) {
-                        const uint64_t bd = p.b_mn ? smem_desc_mn_sw128(sb + kMnKStepBytes * ks, kMnAtomBytes)
+                        const uint64_t bd = BMN ? smem_desc_mn_sw128(sb + kMnKStepBytes * ks, kMnAtomBytes)
                                                    : smem_desc_sw128(sb + 32u * ks);
                         for (int h = 0; h < 2; ++h)
                             tc_mma_f16_pair(tmem_base + (uint32_t)(h * 256), smem_desc_sw128(sa + h * kHalfBytes + 32u * ks),
@@ -1088,23 +1077,24 @@ sbt_status launch_main(sbt_context* ctx, const CUtensorMap* tmA_direct, const CU
     p.status = ctx->status;
     p.wait_ns = ctx->wait_limit_ns;
     p.withhold_first_load = ctx->test_hook == SBT_TEST_WITHHOLD_LOAD;
-    p.b_mn = tmB_direct != nullptr;
+    const bool bmn = tmB_direct != nullptr;
     static bool attr_set[64] = {false};
     if (!attr_set[ctx->device & 63]) {
-        cudaError_t e = cudaFuncSetAttribute(k_gemm_bf16_tc<256>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)TcShape<256>::kSmem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(k_gemm_bf16_tc<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)TcShape<128>::kSmem);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(k_gemm_bf16_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)TcShape<64>::kSmem);
+        cudaError_t e = cudaSuccess;
+        auto smem = [&](const void* f, size_t bytes) {
+            if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+        };
+        smem((const void*)k_gemm_bf16_tc<256, false>, TcShape<256>::kSmem);
+        smem((const void*)k_gemm_bf16_tc<128, false>, TcShape<128>::kSmem);
+        smem((const void*)k_gemm_bf16_tc<64, false>, TcShape<64>::kSmem);
+        smem((const void*)k_gemm_bf16_tc<256, true>, TcShape<256>::kSmem);
+        smem((const void*)k_gemm_bf16_tc<128, true>, TcShape<128>::kSmem);
+        smem((const void*)k_gemm_bf16_tc<64, true>, TcShape<64>::kSmem);
+        smem((const void*)k_gemm_bf16_tc_pair<false>, kGemmSmem2);
+        smem((const void*)k_gemm_bf16_tc_pair<true>, kGemmSmem2);
+        smem((const void*)k_gemm_bf16_tc_pair512<false>, kGemmSmem3);
+        smem((const void*)k_gemm_bf16_tc_pair512<true>, kGemmSmem3);
         if (e != cudaSuccess) return sbt_cuda_check(e, "cudaFuncSetAttribute(gemm smem)");
-        e = cudaFuncSetAttribute(k_gemm_bf16_tc_pair, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kGemmSmem2);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(k_gemm_bf16_tc_pair512, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)kGemmSmem3);
-        if (e != cudaSuccess) return sbt_cuda_check(e, "cudaFuncSetAttribute(gemm pair smem)");
         attr_set[ctx->device & 63] = true;
     }
     if (pair) {
@@ -1130,8 +1120,8 @@ sbt_status launch_main(sbt_context* ctx, const CUtensorMap* tmA_direct, const CU
             cfg.attrs = &attr;
             cfg.numAttrs = 1;
             int n = 0;
-            const cudaError_t qe = wide ? cudaOccupancyMaxActiveClusters(&n, k_gemm_bf16_tc_pair512, &cfg)
-                                        : cudaOccupancyMaxActiveClusters(&n, k_gemm_bf16_tc_pair, &cfg);
+            const cudaError_t qe = wide ? cudaOccupancyMaxActiveClusters(&n, k_gemm_bf16_tc_pair512<true>, &cfg)
+                                        : cudaOccupancyMaxActiveClusters(&n, k_gemm_bf16_tc_pair<true>, &cfg);
             if (qe != cudaSuccess || n < 1) {
                 (void)cudaGetLastError();
                 n = ctx->sm_count / 2;
@@ -1139,11 +1129,17 @@ sbt_status launch_main(sbt_context* ctx, const CUtensorMap* tmA_direct, const CU
             mc = n;
         }
         const int clusters = std::min(tiles, mc);
-        const cudaError_t e =
-            wide ? sbt_launch_dependent(k_gemm_bf16_tc_pair512, dim3(2 * clusters), dim3(kGemmThreads3), kGemmSmem3,
-                                        stream, tmA, tmB, p)
-                 : sbt_launch_dependent(k_gemm_bf16_tc_pair, dim3(2 * clusters), dim3(kGemmThreads), kGemmSmem2,
-                                        stream, tmA, tmB, p);
+        cudaError_t e;
+        if (wide)
+            e = bmn ? sbt_launch_dependent(k_gemm_bf16_tc_pair512<true>, dim3(2 * clusters), dim3(kGemmThreads3),
+                                           kGemmSmem3, stream, tmA, tmB, p)
+                    : sbt_launch_dependent(k_gemm_bf16_tc_pair512<false>, dim3(2 * clusters), dim3(kGemmThreads3),
+                                           kGemmSmem3, stream, tmA, tmB, p);
+        else
+            e = bmn ? sbt_launch_dependent(k_gemm_bf16_tc_pair<true>, dim3(2 * clusters), dim3(kGemmThreads),
+                                           kGemmSmem2, stream, tmA, tmB, p)
+                    : sbt_launch_dependent(k_gemm_bf16_tc_pair<false>, dim3(2 * clusters), dim3(kGemmThreads),
+                                           kGemmSmem2, stream, tmA, tmB, p);
         if (e != cudaSuccess) return sbt_cuda_check(e, "gemm_bounded (tcgen05, CTA pairs)");
         return sbt_after_launch(ctx, "gemm_bounded (tcgen05, CTA pairs)");
     }
@@ -1153,15 +1149,15 @@ sbt_status launch_main(sbt_context* ctx, const CUtensorMap* tmA_direct, const CU
     const int tiles = p.m_tiles * p.n_tiles;
     const int grid = std::min(tiles, ctx->sm_count);
     cudaError_t e;
+    auto launch1 = [&](auto kern, size_t smem_bytes) {
+        return sbt_launch_dependent(kern, dim3(grid), dim3(kGemmThreads), smem_bytes, stream, tmA, tmB, p);
+    };
     if (bn1 == 256)
-        e = sbt_launch_dependent(k_gemm_bf16_tc<256>, dim3(grid), dim3(kGemmThreads), TcShape<256>::kSmem, stream,
-                                 tmA, tmB, p);
+        e = bmn ? launch1(k_gemm_bf16_tc<256, true>, TcShape<256>::kSmem) : launch1(k_gemm_bf16_tc<256, false>, TcShape<256>::kSmem);
     else if (bn1 == 128)
-        e = sbt_launch_dependent(k_gemm_bf16_tc<128>, dim3(grid), dim3(kGemmThreads), TcShape<128>::kSmem, stream,
-                                 tmA, tmB, p);
+        e = bmn ? launch1(k_gemm_bf16_tc<128, true>, TcShape<128>::kSmem) : launch1(k_gemm_bf16_tc<128, false>, TcShape<128>::kSmem);
     else
-        e = sbt_launch_dependent(k_gemm_bf16_tc<64>, dim3(grid), dim3(kGemmThreads), TcShape<64>::kSmem, stream,
-                                 tmA, tmB, p);
+        e = bmn ? launch1(k_gemm_bf16_tc<64, true>, TcShape<64>::kSmem) : launch1(k_gemm_bf16_tc<64, false>, TcShape<64>::kSmem);
     if (e != cudaSuccess) return sbt_cuda_check(e, "gemm_bounded (tcgen05)");
     return sbt_after_launch(ctx, "gemm_bounded (tcgen05)");
 }
