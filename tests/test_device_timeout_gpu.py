@@ -56,9 +56,11 @@ def test_gemm_wait_runs_out_then_recovers(ctx, mnk):
     assert np.linalg.norm(got - ref_b) / np.linalg.norm(ref) <= 1e-3
 
 
-def test_block_scaled_mma_wait_runs_out_then_recovers(ctx):
-    # E4M3 operands with E8M0 scales per 32: the tcgen05 block-scaled CTA-pair kernel
-    M, N, K = 600, 700, 256
+@pytest.mark.parametrize("mnk", [(600, 700, 256), (600, 8320, 128)], ids=["few_tiles", "many_tiles"])
+def test_block_scaled_mma_wait_runs_out_then_recovers(ctx, mnk):
+    # E4M3 operands with E8M0 scales per 32: the tcgen05 block-scaled CTA-pair kernel, with
+    # fewer tiles than CTA pairs and with several tiles per pair
+    M, N, K = mnk
     g = wl.gemm_block_scaled(M=M, N=N, K=K, block=32, tag=22)
     A, B, SA, SB = (dev(g[k]) for k in ("A", "B", "SA", "SB"))
     D = torch.empty(M * g["ldd"] * 4, dtype=torch.uint8, device="cuda")

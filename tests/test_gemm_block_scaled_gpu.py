@@ -157,6 +157,47 @@ def test_nan_codes_propagate_to_their_row_and_column(ctx):
     np.testing.assert_array_equal(np.isnan(got), nan)
 
 
+def sampled_check(got, g, rows, cols, acc=None):
+    """The oracle on the sampled rows and columns only, held to the same bound as check()."""
+    K, block = g["K"], g["block"]
+    Ar, SAr = np.ascontiguousarray(g["A"][rows]), np.ascontiguousarray(g["SA"][rows])
+    Bc = np.ascontiguousarray(g["B"][:, cols]) if g["bfmt"] != "e2m1" else None
+    if Bc is None:  # packed E2M1 columns cannot be sliced bytewise: unpack, slice, repack
+        codes = np.stack([g["B"] & 15, g["B"] >> 4], axis=-1).reshape(g["B"].shape[0], -1)[:, cols]
+        codes = np.pad(codes, ((0, 0), (0, len(cols) % 2)))
+        Bc = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    SBc = np.ascontiguousarray(g["SB"][:, cols])
+    R, C = len(rows), len(cols)
+    ldb = C + (C % 2 if g["bfmt"] == "e2m1" else 0)
+    accs = None if acc is None else np.ascontiguousarray(acc[np.ix_(rows, cols)])
+    ref = oracle.gemm_block_scaled_f64(Ar, g["lda"], SAr, g["ld_sa"], Bc, ldb, SBc, C, R, C, K, block,
+                                       afmt=g["afmt"], bfmt=g["bfmt"], sfmt=g["sfmt"], acc=accs, ld_acc=C)
+    bound = oracle.gemm_block_scaled_f64(abs_codes(Ar, g["afmt"]), g["lda"], SAr, g["ld_sa"],
+                                         abs_codes(Bc, g["bfmt"]), ldb, SBc, C, R, C, K, block,
+                                         afmt=g["afmt"], bfmt=g["bfmt"], sfmt=g["sfmt"])
+    d = got[np.ix_(rows, cols)]
+    slack = (K + 2) * 2.0 ** -23 * bound + (np.abs(accs) * 2.0 ** -23 if accs is not None else 0) + 1e-30
+    assert np.all(np.abs(d - ref) <= slack)
+
+
+@pytest.mark.parametrize("case", ["e4m3_tail_rows", "e2m1_acc_in_place", "e5m2_acc"])
+def test_many_tiles_sampled(ctx, case):
+    """CTA-pair kernel over many tiles, checked on sampled rows and columns: (600, 8320) has a
+    last row tile of 88 rows, one of its CTAs wholly past M; acc is added (also in place,
+    D = acc); E2M1 and E5M2 operands."""
+    M, N, K = {"e4m3_tail_rows": (600, 8320, 256), "e2m1_acc_in_place": (600, 8320, 256),
+               "e5m2_acc": (1100, 8400, 384)}[case]
+    fmt = {"e4m3_tail_rows": "e4m3", "e2m1_acc_in_place": "e2m1", "e5m2_acc": "e5m2"}[case]
+    g = wl.gemm_block_scaled(M=M, N=N, K=K, block=32, afmt=fmt, bfmt=fmt, tag=8)
+    acc = None
+    if case != "e4m3_tail_rows":
+        acc = synth.uniform_f32(synth.stream_seed(wl.SEED_GEMM_SCALED, 92), (M, g["ldd"]), -10.0, 10.0)
+    got = run(ctx, g, acc=acc, in_place=case == "e2m1_acc_in_place")
+    rows = np.concatenate([[0, 1, 127, 128, 255, 256, 511, 512, 513, M - 2, M - 1], synth.int_below(622, 30, M)])
+    cols = np.concatenate([[0, 1, 207, 208, 415, 416, N - 2, N - 1], synth.int_below(623, 24, N)])
+    sampled_check(got, g, rows, cols, acc=None if acc is None else acc[:, :N])
+
+
 def test_full_size_sampled_rows_and_columns(ctx):
     # 8191 x 8193 x 4096, E4M3 operands, E8M0 scales over blocks of 32: the
     # launch configuration the benchmark times (CTA pairs), checked on 48 rows
