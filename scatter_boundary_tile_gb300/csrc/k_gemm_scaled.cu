@@ -5,9 +5,9 @@
 // block of K / K_s elements along K (a_scale (M,K_s), b_scale (K_s,N), in
 // E8M0 or E4M3), fp32 accumulator and acc.
 //
-// E4M3 / E5M2 / E2M1 operands with E8M0 scales over blocks of 32 run on the
-// tensor cores' block scaling (k_gemm_mx.cu).  Every other combination takes this
-// path: the operand staging of the boundary-tile GEMM, with the scale folded
+// E4M3 / E5M2 / E2M1 operands with E8M0 scales over blocks of 32, and E2M1 x
+// E2M1 with E4M3 scales over blocks of 16, run on the tensor cores' block
+// scaling (k_gemm_mx.cu).  Every other combination takes this path: the operand staging of the boundary-tile GEMM, with the scale folded
 // in.  Each element is decoded from its format and multiplied by its block's
 // scale in fp32, rounded to bf16 and written into the same padded K-major
 // copies A' [Mp][Kp] and B'^T [Np][Kp] (zero past M, N, K) that the bf16
@@ -203,11 +203,13 @@ sbt_status sbt_launch_gemm_block_scaled(sbt_context* ctx, int a_fmt, const void*
     if (M > INT32_MAX / 2 || N > INT32_MAX / 2 || K > INT32_MAX / 2)
         return sbt_fail(SBT_ERR_INVALID_ARG, "gemm_block_scaled: extents must be below 2^30");
     if (K == 0) return sbt_launch_gemm_zero_k(ctx, D, ldd, true, acc, ld_acc, M, N, stream);
-    // kind::mxf8f6f4 takes E4M3, E5M2 and (one code per byte) E2M1 operands
-    if (s_fmt == kFmtE8M0 && K == 32 * Ks &&
-        (ctx->path == SBT_PATH_AUTO || ctx->path == SBT_PATH_TMA))
-        return sbt_launch_gemm_mx(ctx, a_fmt, A, lda, b_fmt, B, ldb, SA, ld_sa, SB, ld_sb, acc, ld_acc, D, ldd, M, N,
-                                  K, workspace, stream);
+    // the tensor cores' block scaling: E8M0 scales over blocks of 32 with any of the operand
+    // formats, and E4M3 scales over blocks of 16 with E2M1 x E2M1
+    const bool mx = (s_fmt == kFmtE8M0 && K == 32 * Ks) ||
+                    (s_fmt == kFmtE4M3 && K == 16 * Ks && a_fmt == kFmtE2M1 && b_fmt == kFmtE2M1);
+    if (mx && (ctx->path == SBT_PATH_AUTO || ctx->path == SBT_PATH_TMA))
+        return sbt_launch_gemm_mx(ctx, a_fmt, A, lda, b_fmt, B, ldb, s_fmt, SA, ld_sa, SB, ld_sb, acc, ld_acc, D, ldd,
+                                  M, N, K, workspace, stream);
     const sbt_gemm_layout d = sbt_gemm_layout_of(M, N, K);
     if (d.Np / 64 > 65535) return sbt_fail(SBT_ERR_INVALID_ARG, "gemm_block_scaled: N too large for the staging grid");
     const int block = (int)(K / Ks);

@@ -113,15 +113,17 @@ sbt_status sbt_launch_gemm_main(sbt_context* ctx, const uint16_t* Ap, const uint
 // C = acc (or 0): the K = 0 result.
 sbt_status sbt_launch_gemm_zero_k(sbt_context* ctx, void* C, int64_t ldc, bool c_f32, const float* acc,
                                   int64_t ld_acc, int64_t M, int64_t N, cudaStream_t stream);
-// Block-scaled GEMM on tcgen05's own block scaling (E4M3/E5M2 operands, E8M0
-// scales per 32 along K): 8-bit staging + kind::mxf8f6f4 kernel.
+// Block-scaled GEMM on tcgen05's own block scaling: E4M3 / E5M2 / E2M1
+// operands with E8M0 scales per 32 along K (kind::mxf8f6f4, or kind::mxf4
+// when both are E2M1), and E2M1 x E2M1 with E4M3 scales per 16
+// (kind::mxf4nvf4); the caller checks that the call is one of these.
 size_t sbt_gemm_mx_workspace_bytes(int64_t M, int64_t N, int64_t K);
 sbt_status sbt_launch_gemm_mx(sbt_context* ctx, int a_fmt, const void* A, int64_t lda, int b_fmt, const void* B,
-                              int64_t ldb, const void* SA, int64_t ld_sa, const void* SB, int64_t ld_sb,
+                              int64_t ldb, int s_fmt, const void* SA, int64_t ld_sa, const void* SB, int64_t ld_sb,
                               const float* acc, int64_t ld_acc, float* D, int64_t ldd, int64_t M, int64_t N,
                               int64_t K, void* workspace, cudaStream_t stream);
-// Block-scaled GEMM (formats as sbt_lowp_format): the kind::mxf8f6f4 kernel
-// where it applies (AUTO / TMA path), else bf16 staging of the scaled operands.
+// Block-scaled GEMM (formats as sbt_lowp_format): the block-scaled tensor-core
+// kernel where it applies (AUTO / TMA path), else bf16 staging of the scaled operands.
 sbt_status sbt_launch_gemm_block_scaled(sbt_context* ctx, int a_fmt, const void* A, int64_t lda, int b_fmt,
                                         const void* B, int64_t ldb, int s_fmt, const void* SA, int64_t ld_sa,
                                         const void* SB, int64_t ld_sb, int64_t Ks, const float* acc, int64_t ld_acc,

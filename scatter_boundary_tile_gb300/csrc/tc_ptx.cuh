@@ -332,6 +332,45 @@ __device__ __forceinline__ void tc_mma_mx_pair(uint32_t d_tmem, uint64_t a_desc,
         : "memory");
 }
 
+// D[tmem of both CTAs] (+)= (A .* SFA) * (B .* SFB)^T over one K = 64 step of
+// packed E2M1 operands (two codes per byte), kind::mxf4: two E8M0 scales per
+// row of A / column of B (blocks of 32), bytes sf_id and sf_id + 1 of the
+// scale column (sf_id 0 or 2).
+__device__ __forceinline__ void tc_mma_mxf4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                 uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// The same over one K = 64 step with four scales per row / column (blocks of
+// 16), kind::mxf4nvf4: all four bytes of the scale column (sf_id 0).
+__device__ __forceinline__ void tc_mma_mxf4nvf4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                                     uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                     uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X [%0], %1, %2, %3, [%4], [%5], p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Instruction descriptor of kind::mxf4 / kind::mxf4nvf4: both operands E2M1
+// (type code 1 in these kinds), K-major, fp32 accumulator, M x N, K = 64 per
+// instruction; scales E8M0 (`e8m0` true) or unsigned E4M3 (false).  The scale
+// bytes (sf_id) are or-ed in per step as for kind::mxf8f6f4.
+__host__ __device__ __forceinline__ uint32_t idesc_mxf4(uint32_t m, uint32_t n, bool e8m0) {
+    return (1u << 7)                // A: E2M1
+           | (1u << 10)             // B: E2M1
+           | ((n >> 3) << 17)       // N / 8
+           | ((e8m0 ? 1u : 0u) << 23)  // scale type
+           | ((m >> 4) << 24);      // M / 16
+}
+
 // Instruction descriptor, kind::mxf8f6f4 with E8M0 scales: operand formats
 // (0 = E4M3, 1 = E5M2, 5 = E2M1), K-major A and B, fp32 accumulator, M x N; `sf_id`
 // selects the byte of each 32-bit scale column used by this K = 32 step.

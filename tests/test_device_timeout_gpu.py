@@ -56,25 +56,30 @@ def test_gemm_wait_runs_out_then_recovers(ctx, mnk):
     assert np.linalg.norm(got - ref_b) / np.linalg.norm(ref) <= 1e-3
 
 
-@pytest.mark.parametrize("mnk", [(600, 700, 256), (600, 8320, 128)], ids=["few_tiles", "many_tiles"])
-def test_block_scaled_mma_wait_runs_out_then_recovers(ctx, mnk):
-    # E4M3 operands with E8M0 scales per 32: the tcgen05 block-scaled CTA-pair kernel, with
-    # fewer tiles than CTA pairs and with several tiles per pair
+@pytest.mark.parametrize("mnk,fmts", [((600, 700, 256), ("e4m3", "e8m0", 32)), ((600, 8320, 128), ("e4m3", "e8m0", 32)),
+                                      ((600, 8320, 512), ("e2m1", "e8m0", 32)), ((600, 700, 512), ("e2m1", "e4m3", 16))],
+                         ids=["few_tiles", "many_tiles", "mxf4_many_tiles", "mxf4nvf4_few_tiles"])
+def test_block_scaled_mma_wait_runs_out_then_recovers(ctx, mnk, fmts):
+    # the tcgen05 block-scaled CTA-pair kernel in its three forms (E4M3 with E8M0 scales per 32;
+    # packed E2M1 with E8M0 per 32 or E4M3 per 16), with fewer tiles than CTA pairs and with
+    # several tiles per pair
     M, N, K = mnk
-    g = wl.gemm_block_scaled(M=M, N=N, K=K, block=32, tag=22)
+    fmt, sfmt, block = fmts
+    g = wl.gemm_block_scaled(M=M, N=N, K=K, block=block, afmt=fmt, bfmt=fmt, sfmt=sfmt, tag=22)
     A, B, SA, SB = (dev(g[k]) for k in ("A", "B", "SA", "SB"))
     D = torch.empty(M * g["ldd"] * 4, dtype=torch.uint8, device="cuda")
     ws_n = sbt.gemm_block_scaled_workspace_size(ctx, M, N, K)
     ws = torch.empty(ws_n, dtype=torch.uint8, device="cuda")
     run = lambda: sbt.gemm_block_scaled(ctx, A, g["lda"], B, g["ldb"], SA, g["ld_sa"], SB, g["ld_sb"], g["Ks"], D,
-                                        g["ldd"], M, N, K, workspace=ws, workspace_bytes=ws_n)
+                                        g["ldd"], M, N, K, workspace=ws, workspace_bytes=ws_n, a_fmt=fmt, b_fmt=fmt,
+                                        s_fmt=sfmt)
     expect_timeout(ctx, run)
     run()
     sync()
     ctx.check_status()
     got = host(D, np.float32, (M, g["ldd"]))[:, :N].astype(np.float64)
     ref = oracle.gemm_block_scaled_f64(g["A"], g["lda"], g["SA"], g["ld_sa"], g["B"], g["ldb"], g["SB"], g["ld_sb"],
-                                       M, N, K, 32)
+                                       M, N, K, block, afmt=fmt, bfmt=fmt, sfmt=sfmt)
     assert np.linalg.norm(got - ref) / np.linalg.norm(ref) <= 1e-5
 
 

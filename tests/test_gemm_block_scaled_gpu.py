@@ -67,7 +67,7 @@ def check(got, g, acc=None):
 
 
 FORMATS = [("e4m3", "e4m3", "e8m0"), ("e5m2", "e5m2", "e8m0"), ("e4m3", "e5m2", "e4m3"), ("e2m1", "e2m1", "e8m0"),
-           ("e2m1", "e4m3", "e4m3")]
+           ("e2m1", "e4m3", "e4m3"), ("e2m1", "e2m1", "e4m3")]
 SHAPES = [(1, 1, 32, 32), (3, 5, 64, 32), (65, 97, 96, 32), (128, 256, 64, 16), (129, 257, 160, 32),
           (300, 17, 48, 1), (17, 300, 200, 200)]
 
@@ -91,9 +91,10 @@ MX_SHAPES = [(1, 1, 32), (7, 9, 96), (65, 97, 160), (256, 224, 128), (257, 225, 
 @pytest.mark.parametrize("shape", MX_SHAPES, ids=lambda s: "x".join(map(str, s)))
 def test_e8m0_block32_both_paths_vs_oracle(ctx, path, fmts, shape):
     # E4M3/E5M2/E2M1 with E8M0 scales per 32 along K: "auto" takes the
-    # tcgen05 kind::mxf8f6f4 kernel (256 x 224 tiles, 128-deep K blocks, so
-    # these shapes cut tiles and K blocks at every kind of edge), "scalar"
-    # forces the bf16 staging path; both must meet the same bounds.
+    # tcgen05 block-scaled kernel (kind::mxf8f6f4 with 128-deep K blocks, or
+    # kind::mxf4 with 256-deep ones for E2M1 x E2M1; 256 x 208 tiles, so these
+    # shapes cut tiles and K blocks at every kind of edge), "scalar" forces the
+    # bf16 staging path; both must meet the same bounds.
     M, N, K = shape
     ctx.set_path(path)
     g = wl.gemm_block_scaled(M=M, N=N, K=K, block=32, afmt=fmts[0], bfmt=fmts[1], sfmt="e8m0", tag=8)
