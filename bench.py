@@ -47,13 +47,14 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=8.0, help="CPU-baseline sample budget")
     ap.add_argument("--profile", default=None,
                     choices=["gather", "scatter", "scatter_add", "ragged", "ragged_store", "tile_load_tma", "tile_load", "tile_store", "tile_load_unaligned",
-                             "tile_store_unaligned", "gemm", "gemm_scaled", "gather_cols"],
+                             "tile_store_unaligned", "gemm", "gemm_scaled", "gemm_mxf4", "gemm_nvf4", "gather_cols"],
                     help="only launch one operation's workload (warmup + steps launches) for ncu")
     ap.add_argument("--scale", type=float, default=1.0, help="--profile: fraction of the workload's rows")
     return ap.parse_args()
 
 
 FP8_NOMINAL_TFLOPS = 4500.0  # dense fp8 tensor rate, nominal (no measured fp8 peak is available)
+FP4_NOMINAL_TFLOPS = 13500.0  # dense fp4 tensor rate, nominal (no measured fp4 peak is available)
 
 
 def peaks():
@@ -614,8 +615,7 @@ def run_ops(ctx, pk):
             ctx.set_path(path)
             med, _, _ = time_launches(fn, 10)
             tf = flops / med / 1e9
-            entry = {"ms": med, "TFLOP/s": tf, "frac_bf16": tf / pk["bf16_tflops"],
-                     "frac_fp8_nominal": tf / FP8_NOMINAL_TFLOPS,
+            entry = {"ms": med, "TFLOP/s": tf, "frac_fp8_nominal": tf / FP8_NOMINAL_TFLOPS,
                      "workload": "E4M3 x E4M3, E8M0 scales per 32 along K, fp32 D, no acc", "note": note}
             split = kernel_split(fn, 5)
             if split:
@@ -623,21 +623,29 @@ def run_ops(ctx, pk):
             ops[f"gemm_block_scaled_{M}x{N}x{K}" + ("" if path == "auto" else "_bf16_staging")] = entry
         ctx.set_path("auto")
         del A, B, SA, SB, D, ws
-        # MXFP4: E2M1 operands (two per byte), E8M0 scales per 32, on the tensor path
-        g = wl.gemm_block_scaled(M=M, N=N, K=K, block=32, afmt="e2m1", bfmt="e2m1")
-        A, B, SA, SB = (dev_bytes(g[k]) for k in ("A", "B", "SA", "SB"))
-        D = torch.empty(M * g["ldd"] * 4, dtype=torch.uint8, device="cuda")
-        ws = torch.empty(max(ws_n, 256), dtype=torch.uint8, device="cuda")
-        fn = lambda: sbt.gemm_block_scaled(ctx, A, g["lda"], B, g["ldb"], SA, g["ld_sa"], SB, g["ld_sb"], g["Ks"],
-                                           D, g["ldd"], M, N, K, workspace=ws, workspace_bytes=ws_n,
-                                           a_fmt="e2m1", b_fmt="e2m1")
-        med, _, _ = time_launches(fn, 10)
-        tf = flops / med / 1e9
-        ops[f"gemm_block_scaled_{M}x{N}x{K}_e2m1"] = {
-            "ms": med, "TFLOP/s": tf, "frac_bf16": tf / pk["bf16_tflops"], "frac_fp8_nominal": tf / FP8_NOMINAL_TFLOPS,
-            "workload": "E2M1 x E2M1 (packed), E8M0 scales per 32 along K, fp32 D, no acc",
-            "note": "whole call: staging to the 16-code + 8-byte-pad pieces kind::mxf8f6f4 reads, tcgen05 block-scaled kernel"}
-        del A, B, SA, SB, D, ws
+        # 4-bit operands (E2M1, two per byte) on the packed forms of the tensor path:
+        # E8M0 scales per 32 (kind::mxf4) and E4M3 scales per 16 (kind::mxf4nvf4)
+        for sfmt, block, tag, note in [
+                ("e8m0", 32, "e2m1", "whole call: packed 4-bit staging + tcgen05 kind::mxf4 block-scaled kernel"),
+                ("e4m3", 16, "e2m1_e4m3_per16",
+                 "whole call: packed 4-bit staging (E4M3 scale signs onto the codes) + tcgen05 kind::mxf4nvf4 kernel")]:
+            g = wl.gemm_block_scaled(M=M, N=N, K=K, block=block, afmt="e2m1", bfmt="e2m1", sfmt=sfmt)
+            A, B, SA, SB = (dev_bytes(g[k]) for k in ("A", "B", "SA", "SB"))
+            D = torch.empty(M * g["ldd"] * 4, dtype=torch.uint8, device="cuda")
+            ws = torch.empty(max(ws_n, 256), dtype=torch.uint8, device="cuda")
+            fn = lambda: sbt.gemm_block_scaled(ctx, A, g["lda"], B, g["ldb"], SA, g["ld_sa"], SB, g["ld_sb"], g["Ks"],
+                                               D, g["ldd"], M, N, K, workspace=ws, workspace_bytes=ws_n,
+                                               a_fmt="e2m1", b_fmt="e2m1", s_fmt=sfmt)
+            med, _, _ = time_launches(fn, 10)
+            tf = flops / med / 1e9
+            entry = {"ms": med, "TFLOP/s": tf, "frac_fp4_nominal": tf / FP4_NOMINAL_TFLOPS,
+                     "workload": f"E2M1 x E2M1 (packed), {sfmt.upper()} scales per {block} along K, fp32 D, no acc",
+                     "note": note}
+            split = kernel_split(fn, 5)
+            if split:
+                entry["kernels_ms"] = split
+            ops[f"gemm_block_scaled_{M}x{N}x{K}_{tag}"] = entry
+            del A, B, SA, SB, D, ws
     return ops
 
 
@@ -926,15 +934,19 @@ def run_profile(args):
         ad, cid = dev_bytes(a), dev_bytes(ci)
         outc = torch.empty(rows_ * 4096 * 2, dtype=torch.uint8, device="cuda")
         fn = lambda: sbt.gather_cols(ctx, ad, rows_, 100_003, 100_003, cid, 4096, outc, 4096, rows_, dtype="bf16")
-    elif op == "gemm_scaled":  # (8191, 8193, 4096) E4M3 / E8M0 per 32, scaled along M
+    elif op in ("gemm_scaled", "gemm_mxf4", "gemm_nvf4"):
+        # (8191, 8193, 4096) scaled along M: E4M3 / E8M0 per 32, E2M1 / E8M0 per 32, E2M1 / E4M3 per 16
         M, N, K = max(1, int(8191 * f)), 8193, 4096
-        g = wl.gemm_block_scaled(M=M, N=N, K=K, block=32)
+        fmt, sfmt, block = {"gemm_scaled": ("e4m3", "e8m0", 32), "gemm_mxf4": ("e2m1", "e8m0", 32),
+                            "gemm_nvf4": ("e2m1", "e4m3", 16)}[op]
+        g = wl.gemm_block_scaled(M=M, N=N, K=K, block=block, afmt=fmt, bfmt=fmt, sfmt=sfmt)
         A, B, SA, SB = (dev_bytes(g[k]) for k in ("A", "B", "SA", "SB"))
         D = torch.empty(M * g["ldd"] * 4, dtype=torch.uint8, device="cuda")
         ws_n = sbt.gemm_block_scaled_workspace_size(ctx, M, N, K)
         ws = torch.empty(max(ws_n, 256), dtype=torch.uint8, device="cuda")
         fn = lambda: sbt.gemm_block_scaled(ctx, A, g["lda"], B, g["ldb"], SA, g["ld_sa"], SB, g["ld_sb"], g["Ks"],
-                                           D, g["ldd"], M, N, K, workspace=ws, workspace_bytes=ws_n)
+                                           D, g["ldd"], M, N, K, workspace=ws, workspace_bytes=ws_n, a_fmt=fmt,
+                                           b_fmt=fmt, s_fmt=sfmt)
     else:  # gemm: (8191, 8193, 4097) scaled along M
         M, N, K = max(1, int(8191 * f)), 8193, 4097
         g = wl.gemm_bf16(M=M, N=N, K=K)

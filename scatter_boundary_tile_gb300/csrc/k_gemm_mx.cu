@@ -75,13 +75,11 @@ constexpr int kMxFmtE8M0 = 2;  // sbt_lowp_format code of E8M0
 // Operand type field of the kind::mxf8f6f4 instruction descriptor.
 uint32_t mma_format(int fmt) { return fmt == kMxFmtE2M1 ? 5u : (uint32_t)fmt; }
 constexpr int MX_BK = 128;   // bytes of one operand row per K block (one 128-byte swizzle row)
-constexpr int kMxThreads = 192;  // warp 0: TMA, warp 1: MMA, warps 2..5: epilogue
 constexpr uint32_t kMxABytes = 128 * MX_BK;
 constexpr uint32_t kMxBBytes = (MX_BN / 2) * MX_BK;
 constexpr uint32_t kMxSfCol0 = 2 * MX_BN;              // scale slots after the two accumulators
 constexpr uint32_t kMxSfCols = 12;                      // per chunk: 4 columns of A scales + 8 of B scales
-constexpr int kMxEpiWarps = 4;
-constexpr int kMxEpiWords = 32 * 33;
+constexpr int kMxEpiWords = 32 * 33;  // one epilogue warp's transpose buffer (32 x 32 fp32, padded)
 
 // The three MMA forms (see the top of the file).
 enum { kKindF8F6F4 = 0, kKindF4 = 1, kKindNvF4 = 2 };
@@ -101,9 +99,17 @@ struct MxCfg {
     static constexpr uint32_t kSfaOff = kSfbOff + kKB * kChunks * 4096;
     static constexpr uint32_t kTxBytes = kMxABytes + kMxBBytes + kChunks * (4096 + 512);  // one CTA, one K block
     static constexpr uint32_t kStageBytes = (kSfaOff + kKB * kChunks * 512 + 1023u) & ~1023u;
+    // Epilogue: kEpiSlices warps per TMEM lane quarter, each draining every kEpiSlices-th
+    // 32-column chunk; warp 0 loads, warp 1 issues the MMAs.
+    // (Three for the packed forms: their main loop is short enough for four warps' fp32 stores to
+    // set the pace, 0.206 -> 0.188 ms for the 8191 x 8193 x 4096 mxf4 kernel; the 8-bit form has
+    // no shared memory left for more, and two stages with twelve warps were slower.)
+    static constexpr int kEpiSlices = KIND == kKindF8F6F4 ? 1 : 3;
+    static constexpr int kEpiWarps = 4 * kEpiSlices;
+    static constexpr int kThreads = 64 + 32 * kEpiWarps;
     static constexpr int kNumBars = 2 * kStages + 5;
     static constexpr size_t kSmemUsed =
-        1024 + (size_t)kStages * kStageBytes + (size_t)kMxEpiWarps * kMxEpiWords * 4 + kNumBars * 8 + 16;
+        1024 + (size_t)kStages * kStageBytes + (size_t)kEpiWarps * kMxEpiWords * 4 + kNumBars * 8 + 16;
     // Every CTA allocates all 512 TMEM columns, so two CTAs of different pairs on one SM could each
     // hold one half of the other's pair waiting: ask for more than half the SM's shared memory
     // (228 KB, 1 KB of it reserved per CTA) so that only one fits.
@@ -148,13 +154,13 @@ __device__ __forceinline__ void tile_coords(int tile, int m_tiles, int n_tiles, 
 // 32-column segment per store instruction).  mxf4nvf4: NaN in the rows and
 // columns whose scales held a NaN.
 template <int KIND>
-__device__ __forceinline__ void mx_epilogue_tile(const MxParams& p, uint32_t tmem_acc, int q, int lane, float* buf,
-                                                 int row0, int n0) {
+__device__ __forceinline__ void mx_epilogue_tile(const MxParams& p, uint32_t tmem_acc, int q, int slice, int lane,
+                                                 float* buf, int row0, int n0) {
     const int n_valid = min(MX_BN, p.N - n0);  // columns of this tile inside N (MX_BN is not a multiple of 32)
     const int chunks = (n_valid + 31) / 32;
     uint32_t nan_rows = 0;  // bit rr: row row0 + rr (< Mp) had a NaN scale
     if constexpr (KIND == kKindNvF4) nan_rows = __ballot_sync(0xffffffffu, p.nan_a[row0 + lane] != 0);
-    for (int c = 0; c < chunks; ++c) {
+    for (int c = slice; c < chunks; c += MxCfg<KIND>::kEpiSlices) {
         uint32_t r[32];
         tmem_ld_32x32b_x32(tmem_acc + ((uint32_t)(q * 32) << 16) + (uint32_t)(c * 32), r);
         tmem_ld_wait();
@@ -165,20 +171,29 @@ __device__ __forceinline__ void mx_epilogue_tile(const MxParams& p, uint32_t tme
         if (c * 32 + lane < n_valid) {
             bool nan_col = false;
             if constexpr (KIND == kKindNvF4) nan_col = p.nan_b[col] != 0;
-            if (KIND == kKindNvF4 && (nan_rows != 0 || nan_col)) {
-                for (int rr = 0; rr < 32 && row0 + rr < p.M; ++rr) {
-                    float v = buf[rr * 33 + lane];
-                    if (p.acc) v += __ldg(p.acc + (int64_t)(row0 + rr) * p.ld_acc + col);
-                    if (nan_col || ((nan_rows >> rr) & 1u)) v = __uint_as_float(0x7FC00000u);
-                    p.D[(int64_t)(row0 + rr) * p.ldd + col] = v;
+            const int rows = min(32, p.M - row0);
+            // two halves of 16 rows: all loads of a half issue before its stores (a loop carrying
+            // each store behind its own shared load ran at ~90 cycles a row)
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                float v[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = buf[(16 * h + i) * 33 + lane];
+                if (p.acc) {
+                    const float* a = p.acc + (int64_t)(row0 + 16 * h) * p.ld_acc + col;
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (16 * h + i < rows) v[i] += __ldg(a + (int64_t)i * p.ld_acc);
                 }
-            } else if (p.acc) {
-                for (int rr = 0; rr < 32 && row0 + rr < p.M; ++rr)
-                    p.D[(int64_t)(row0 + rr) * p.ldd + col] =
-                        buf[rr * 33 + lane] + __ldg(p.acc + (int64_t)(row0 + rr) * p.ld_acc + col);
-            } else {
-                for (int rr = 0; rr < 32 && row0 + rr < p.M; ++rr)
-                    p.D[(int64_t)(row0 + rr) * p.ldd + col] = buf[rr * 33 + lane];
+                if constexpr (KIND == kKindNvF4) {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        if (nan_col || ((nan_rows >> (16 * h + i)) & 1u)) v[i] = __uint_as_float(0x7FC00000u);
+                }
+                float* d = p.D + (int64_t)(row0 + 16 * h) * p.ldd + col;
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    if (16 * h + i < rows) d[(int64_t)i * p.ldd] = v[i];
             }
         }
         __syncwarp();
@@ -186,7 +201,7 @@ __device__ __forceinline__ void mx_epilogue_tile(const MxParams& p, uint32_t tme
 }
 
 template <int KIND>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MxCfg<KIND>::kThreads, 1)
     k_gemm_mx_pair(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                    const __grid_constant__ CUtensorMap tmSA, const __grid_constant__ CUtensorMap tmSB,
                    const MxParams p) {
@@ -195,7 +210,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     float* epi = reinterpret_cast<float*>(smem + (size_t)kMxStages * C::kStageBytes);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(epi + kMxEpiWarps * kMxEpiWords);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(epi + C::kEpiWarps * kMxEpiWords);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + C::kNumBars);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -218,7 +233,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
         }
         for (int a = 0; a < 2; ++a) {
             mbar_init(tfull_bar(a), 1);
-            mbar_init(tempty_bar(a), 2 * kMxEpiWarps * 32);
+            mbar_init(tempty_bar(a), 2 * C::kEpiWarps * 32);
         }
         mbar_init(mma_done_bar, 1);
         *abort_flag = 0;
@@ -358,8 +373,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
             }
         }
     } else {
-        // ------------------------------------------------------------ epilogue (warps 2..5 of each CTA)
-        const int q = warp & 3;
+        // ------------------------------------------------------------ epilogue (warps 2.. of each CTA)
+        const int q = warp & 3, slice = (warp - 2) >> 2;  // TMEM lane quarter (warp % 4), chunk slice
         float* buf = epi + (warp - 2) * kMxEpiWords;
         const uint32_t leader_tempty0 = mapa_shared(tempty_bar(0), 0);
         int local = 0;
@@ -370,7 +385,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kMxThreads, 1)
             tile_coords(tile, p.m_tiles, p.n_tiles, &mt, &nt);
             if (!mbar_wait_bounded(tfull_bar(acc), use & 1u, p.wait_ns, abort_flag, p.status, kCodeEpilogue)) break;
             tc_fence_after();
-            mx_epilogue_tile<KIND>(p, tmem_base + (uint32_t)(acc * MX_BN), q, lane, buf, mt * 256 + (int)rank * 128 + q * 32,
+            mx_epilogue_tile<KIND>(p, tmem_base + (uint32_t)(acc * MX_BN), q, slice, lane, buf, mt * 256 + (int)rank * 128 + q * 32,
                              nt * MX_BN);
             tc_fence_before();
             mbar_arrive_cluster(leader_tempty0 + 8u * acc);
@@ -721,7 +736,7 @@ sbt_status mx_kernel_setup(sbt_context* ctx, int* clusters_out) {
         attr.val.clusterDim.y = 1;
         attr.val.clusterDim.z = 1;
         cfg.gridDim = dim3(2 * (unsigned)(ctx->sm_count / 2), 1, 1);
-        cfg.blockDim = dim3(kMxThreads, 1, 1);
+        cfg.blockDim = dim3(MxCfg<KIND>::kThreads, 1, 1);
         cfg.dynamicSmemBytes = smem;
         cfg.attrs = &attr;
         cfg.numAttrs = 1;
@@ -743,7 +758,7 @@ sbt_status mx_launch(sbt_context* ctx, const CUtensorMap& tmA, const CUtensorMap
     sbt_status st = mx_kernel_setup<KIND>(ctx, &max_clusters);
     if (st) return st;
     const int clusters = std::min(p.m_tiles * p.n_tiles, max_clusters);
-    const cudaError_t e = sbt_launch_dependent(k_gemm_mx_pair<KIND>, dim3(2 * clusters), dim3(kMxThreads),
+    const cudaError_t e = sbt_launch_dependent(k_gemm_mx_pair<KIND>, dim3(2 * clusters), dim3(MxCfg<KIND>::kThreads),
                                                MxCfg<KIND>::kSmem, stream, tmA, tmB, tmSA, tmSB, p);
     if (e != cudaSuccess) return sbt_cuda_check(e, "gemm_block_scaled (tcgen05 block-scaled, CTA pairs)");
     return sbt_after_launch(ctx, "gemm_block_scaled (tcgen05 block-scaled, CTA pairs)");
