@@ -92,13 +92,17 @@ struct MxCfg {
     static constexpr int kKPerBlock = 4 * kKPerStep;                   // elements of K per K block
     static constexpr int kStages = KIND == kKindF8F6F4 ? 3 : KIND == kKindF4 ? 4 : 2;
     static constexpr int kKB = KIND == kKindF8F6F4 ? 2 : 1;           // K blocks per stage
+    // A's scales: with two or more chunks per K block, pairs of chunks travel in one
+    // 4 KB tcgen05.cp 128x256b source (see the staging); else one 512 B chunk each.
+    static constexpr bool kPairA = kChunks >= 2;
+    static constexpr uint32_t kSfaBytes = kPairA ? (kChunks / 2) * 4096 : kChunks * 512;  // per K block
     // Stage layout per CTA: the K blocks' A atoms, then their B atoms, then their
-    // B scale chunks (4 KB each) and A scale chunks (512 B each); every piece 1024-aligned.
+    // B scale chunks (4 KB each) and A scale chunks; every piece 1024-aligned.
     static constexpr uint32_t kBOff = kKB * kMxABytes;
     static constexpr uint32_t kSfbOff = kBOff + kKB * kMxBBytes;
     static constexpr uint32_t kSfaOff = kSfbOff + kKB * kChunks * 4096;
-    static constexpr uint32_t kTxBytes = kMxABytes + kMxBBytes + kChunks * (4096 + 512);  // one CTA, one K block
-    static constexpr uint32_t kStageBytes = (kSfaOff + kKB * kChunks * 512 + 1023u) & ~1023u;
+    static constexpr uint32_t kTxBytes = kMxABytes + kMxBBytes + kChunks * 4096 + kSfaBytes;  // one CTA, one K block
+    static constexpr uint32_t kStageBytes = (kSfaOff + kKB * kSfaBytes + 1023u) & ~1023u;
     // Epilogue: kEpiSlices warps per TMEM lane quarter, each draining every kEpiSlices-th
     // 32-column chunk; warp 0 loads, warp 1 issues the MMAs.
     // (Three for the packed forms: their main loop is short enough for four warps' fp32 stores to
@@ -289,8 +293,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MxCfg<KIND>::kThread
                             // (128-row group, chunk); the K block's chunks are adjacent
                             tma_load_2d_pair(sa + C::kSfbOff + j * C::kChunks * 4096, &tmSB, 0,
                                              (nt * p.n_chunks + c0) * 16, leader_full);
-                            tma_load_2d_pair(sa + C::kSfaOff + j * C::kChunks * 512, &tmSA, 0,
-                                             ((mt * 2 + (int)rank) * p.n_chunks + c0) * 2, leader_full);
+                            if constexpr (C::kPairA)
+                                tma_load_2d_pair(sa + C::kSfaOff + j * C::kSfaBytes, &tmSA, 0,
+                                                 ((mt * 2 + (int)rank) * (p.n_chunks / 2) + c0 / 2) * 16,
+                                                 leader_full);
+                            else
+                                tma_load_2d_pair(sa + C::kSfaOff + j * C::kSfaBytes, &tmSA, 0,
+                                                 ((mt * 2 + (int)rank) * p.n_chunks + c0) * 2, leader_full);
                         }
                     }
                     if (++stage == kMxStages) {
@@ -332,27 +341,41 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(MxCfg<KIND>::kThread
                         const int n_ch = (k_steps * C::kScalesPerStep + 3) / 4;  // chunks these steps read
                         const uint32_t slot0 =
                             tmem_base + kMxSfCol0 + kMxSfCols * (uint32_t)((stage * kMxKB + j) * C::kChunks);
+                        // slot of chunk c: A's four columns at sf_a(c), B's eight at sf_b(c); paired
+                        // chunks keep A's eight columns (two chunks) first, then B's two sets of eight
+                        auto sf_a = [&](int c) {
+                            return C::kPairA ? slot0 + 24u * (uint32_t)(c >> 1) + 4u * (uint32_t)(c & 1)
+                                             : slot0 + kMxSfCols * (uint32_t)c;
+                        };
+                        auto sf_b = [&](int c) {
+                            return C::kPairA ? slot0 + 24u * (uint32_t)(c >> 1) + 8u + 8u * (uint32_t)(c & 1)
+                                             : slot0 + kMxSfCols * (uint32_t)c + 4u;
+                        };
                         for (int c = 0; c < n_ch; ++c) {
                             const uint32_t ch = (uint32_t)(j * C::kChunks + c);
-                            tc_cp_pair_32x128b_warpx4(slot0 + kMxSfCols * c,
-                                                      smem_desc_rows16(sa + C::kSfaOff + ch * 512));
-                            tc_cp_pair_128x256b(slot0 + kMxSfCols * c + 4,
-                                                smem_desc_rows32(sa + C::kSfbOff + ch * 4096));
+                            if constexpr (C::kPairA) {
+                                if ((c & 1) == 0)
+                                    tc_cp_pair_128x256b(sf_a(c), smem_desc_rows32(sa + C::kSfaOff + j * C::kSfaBytes +
+                                                                                  (uint32_t)(c >> 1) * 4096));
+                            } else {
+                                tc_cp_pair_32x128b_warpx4(sf_a(c), smem_desc_rows16(sa + C::kSfaOff + ch * 512));
+                            }
+                            tc_cp_pair_128x256b(sf_b(c), smem_desc_rows32(sa + C::kSfbOff + ch * 4096));
                         }
                         const uint32_t a_s = sa + j * kMxABytes, b_s = sa + C::kBOff + j * kMxBBytes;
                         for (int ks = 0; ks < k_steps; ++ks) {
                             const int e = ks * C::kScalesPerStep;  // first scale entry of this step
-                            const uint32_t sfa = slot0 + kMxSfCols * (uint32_t)(e >> 2);
+                            const uint32_t sfa = sf_a(e >> 2), sfb = sf_b(e >> 2);
                             const uint32_t sf_id = (uint32_t)(e & 3);
                             const uint32_t idesc = p.idesc | (sf_id << 4) | (sf_id << 29);
                             const uint64_t ad = smem_desc_sw128(a_s + 32u * ks), bd = smem_desc_sw128(b_s + 32u * ks);
                             const uint32_t accum = (kb | ks) != 0 ? 1u : 0u;
                             if constexpr (KIND == kKindF8F6F4)
-                                tc_mma_mx_pair(d_tmem, ad, bd, idesc, sfa, sfa + 4, accum);
+                                tc_mma_mx_pair(d_tmem, ad, bd, idesc, sfa, sfb, accum);
                             else if constexpr (KIND == kKindF4)
-                                tc_mma_mxf4_pair(d_tmem, ad, bd, idesc, sfa, sfa + 4, accum);
+                                tc_mma_mxf4_pair(d_tmem, ad, bd, idesc, sfa, sfb, accum);
                             else
-                                tc_mma_mxf4nvf4_pair(d_tmem, ad, bd, idesc, sfa, sfa + 4, accum);
+                                tc_mma_mxf4nvf4_pair(d_tmem, ad, bd, idesc, sfa, sfb, accum);
                         }
                     }
                     tc_commit_pair_multicast(empty_bar(stage), 0x3);
@@ -584,10 +607,15 @@ __global__ void __launch_bounds__(kBtThreads) k_mx_stage_bt(const uint8_t* __res
 //    lane r, 8 columns of 4 scale bytes; byte b of row r at (r / 8) * 256 +
 //    (b / 16) * 128 + (r % 8) * 16 + b % 16): every lane quarter alike, row
 //    32 q + i column c' holding the scales of B column 208 t + 32 c' + i.
+//  PAIR_A (forms with two or more chunks per K block): A's chunks 2 cp and
+//    2 cp + 1 of row group g share one 4 KB source of that same form, so one
+//    copy fills eight columns: lane 32 q + i, column j (j < 4) holds chunk
+//    2 cp's entries of A row 128 g + 32 j + i, column 4 + j chunk 2 cp + 1's.
 // E8M0 scales are copied; UE4M3 (mxf4nvf4) takes the magnitude of an E4M3
 // scale (its sign went to the operand codes), zero for NaN with the row of A
 // or column of B marked in nan_a / nan_b.  Past the extents 2^0 (127, or 0x38
-// in UE4M3): those operand codes are zero.  One 16-byte store per task.
+// in UE4M3): those operand codes are zero.  A task forms one lane's 16 bytes;
+// the 4 KB sources repeat them for the four lane quarters.
 template <bool UE4M3>
 __device__ __forceinline__ uint32_t stage_scale(uint32_t code, bool* nan) {
     if (!UE4M3) return code;
@@ -598,7 +626,7 @@ __device__ __forceinline__ uint32_t stage_scale(uint32_t code, bool* nan) {
     return code & 0x7Fu;
 }
 
-template <bool UE4M3>
+template <bool UE4M3, bool PAIR_A>
 __global__ void __launch_bounds__(256) k_mx_stage_scales(const uint8_t* __restrict__ SA, int64_t ld_sa,
                                                          const uint8_t* __restrict__ SB, int64_t ld_sb, int M, int N,
                                                          int Ks, int n_chunks, uint8_t* __restrict__ SAp,
@@ -610,10 +638,25 @@ __global__ void __launch_bounds__(256) k_mx_stage_scales(const uint8_t* __restri
         uint32_t w[4];
         uint8_t* dst;
         if (t < tasks_a) {
-            const int r = (int)(t & 31);
-            const int64_t chunk = t >> 5;
-            const int64_t g = chunk / n_chunks;
-            const int kb = (int)(chunk - g * n_chunks);
+            int r;
+            int64_t g;
+            int kb;
+            int half = 0;
+            int64_t pair = 0;
+            if (PAIR_A) {  // lane i (of every quarter), columns 4 half .. + 3 of the source of chunks 2 cp, 2 cp + 1
+                pair = t >> 6;
+                const int n_pairs = n_chunks / 2;
+                g = pair / n_pairs;
+                const int cp = (int)(pair - g * n_pairs);
+                r = (int)(t & 31);
+                half = (int)((t >> 5) & 1);
+                kb = 2 * cp + half;
+            } else {
+                r = (int)(t & 31);
+                const int64_t chunk = t >> 5;
+                g = chunk / n_chunks;
+                kb = (int)(chunk - g * n_chunks);
+            }
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
                 const int64_t m = 128 * g + 32 * j + r;
@@ -628,14 +671,23 @@ __global__ void __launch_bounds__(256) k_mx_stage_scales(const uint8_t* __restri
                 if (UE4M3 && nan) nan_a[m] = 1;
                 w[j] = v;
             }
+            if (PAIR_A) {  // the same 16 bytes for lane r of each of the four quarters
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    const int lane = 32 * q + r;
+                    sbt_st_v4(SAp + pair * 4096 + ((lane >> 3) * 256 + half * 128 + (lane & 7) * 16),
+                              make_uint4(w[0], w[1], w[2], w[3]));
+                }
+                continue;
+            }
             dst = SAp + t * 16;
         } else {
+            // lane i (of every quarter), columns c0 .. c0 + 3 of the 4 KB chunk
             const int64_t u = t - tasks_a;
-            const int unit = (int)(u & 255);               // 16-byte unit within the 4 KB chunk
-            const int64_t chunk = u >> 8;
-            const int r = (unit >> 4) * 8 + (unit & 7);    // row (lane)
-            const int c0 = ((unit >> 3) & 1) * 4;          // first of the unit's 4 columns
-            const int i = r & 31;
+            const int64_t chunk = u >> 6;
+            const int i = (int)(u & 31);
+            const int half = (int)((u >> 5) & 1);
+            const int c0 = 4 * half;
             const int64_t tile = chunk / n_chunks;
             const int kb = (int)(chunk - tile * n_chunks);
 #pragma unroll
@@ -653,7 +705,13 @@ __global__ void __launch_bounds__(256) k_mx_stage_scales(const uint8_t* __restri
                 if (UE4M3 && nan) nan_b[n] = 1;
                 w[e] = v;
             }
-            dst = SBp + u * 16;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {  // the same 16 bytes for lane i of each of the four quarters
+                const int lane = 32 * q + i;
+                sbt_st_v4(SBp + chunk * 4096 + ((lane >> 3) * 256 + half * 128 + (lane & 7) * 16),
+                          make_uint4(w[0], w[1], w[2], w[3]));
+            }
+            continue;
         }
         sbt_st_v4(dst, make_uint4(w[0], w[1], w[2], w[3]));
     }
@@ -683,7 +741,8 @@ MxLayout mx_layout(int64_t M, int64_t N, int64_t K, int kind) {
     L.a_off = 0;
     L.b_off = round256((size_t)L.Mp * L.Kb);
     L.sa_off = L.b_off + round256((size_t)L.Np * L.Kb);
-    L.sb_off = L.sa_off + round256((size_t)(L.Mp / 128) * L.n_chunks * 512);
+    // A's chunks: 512 B each, or (two or more per K block) 4 KB per pair
+    L.sb_off = L.sa_off + round256((size_t)(L.Mp / 128) * L.n_chunks * (chunks >= 2 ? 2048 : 512));
     L.nan_off = L.sb_off + round256((size_t)L.n_tiles * L.n_chunks * 4096);
     L.total = L.nan_off + (kind == kKindNvF4 ? round256((size_t)(L.Mp + L.Np)) : 0);
     return L;
@@ -817,14 +876,21 @@ sbt_status sbt_launch_gemm_mx(sbt_context* ctx, int a_fmt, const void* A, int64_
             k_mx_stage_bt<false, false, false><<<g2, kBtThreads, 0, stream>>>(B8, ldb, (int)K, (int)N, Bp, (int)Kp,
                                                                              nullptr, 0);
         if ((st = sbt_after_launch(ctx, "gemm_block_scaled (stage B)"))) return st;
-        const int64_t ta = (L.Mp / 128) * L.n_chunks * 32, tb = L.n_tiles * L.n_chunks * 256;
+        // one task per lane of a quarter and half of a 4 KB source (stored to all four quarters),
+        // or per lane of a 512 B A chunk
+        const int64_t ta = (L.Mp / 128) * L.n_chunks * 32, tb = L.n_tiles * L.n_chunks * 64;
         const int g3 = (int)std::min<int64_t>(sbt_cdiv(ta + tb, 256), (int64_t)ctx->sm_count * 8);
         if (kind == kKindNvF4)
-            k_mx_stage_scales<true><<<g3, 256, 0, stream>>>(SA8, ld_sa, SB8, ld_sb, (int)M, (int)N, Ks,
-                                                            (int)L.n_chunks, SAp, ta, SBp, tb, nan_a, nan_b);
+            k_mx_stage_scales<true, true><<<g3, 256, 0, stream>>>(SA8, ld_sa, SB8, ld_sb, (int)M, (int)N, Ks,
+                                                                  (int)L.n_chunks, SAp, ta, SBp, tb, nan_a, nan_b);
+        else if (kind == kKindF4)
+            k_mx_stage_scales<false, true><<<g3, 256, 0, stream>>>(SA8, ld_sa, SB8, ld_sb, (int)M, (int)N, Ks,
+                                                                   (int)L.n_chunks, SAp, ta, SBp, tb, nullptr,
+                                                                   nullptr);
         else
-            k_mx_stage_scales<false><<<g3, 256, 0, stream>>>(SA8, ld_sa, SB8, ld_sb, (int)M, (int)N, Ks,
-                                                             (int)L.n_chunks, SAp, ta, SBp, tb, nullptr, nullptr);
+            k_mx_stage_scales<false, false><<<g3, 256, 0, stream>>>(SA8, ld_sa, SB8, ld_sb, (int)M, (int)N, Ks,
+                                                                    (int)L.n_chunks, SAp, ta, SBp, tb, nullptr,
+                                                                    nullptr);
         if ((st = sbt_after_launch(ctx, "gemm_block_scaled (stage scales)"))) return st;
     }
 
@@ -834,7 +900,12 @@ sbt_status sbt_launch_gemm_mx(sbt_context* ctx, int a_fmt, const void* A, int64_
     sbt_status st = encode_u8(ctx, &tmA, Ap, L.Kb, L.Mp, MX_BK, 128, true);
     if (st) return st;
     if ((st = encode_u8(ctx, &tmB, Bp, L.Kb, L.Np, MX_BK, MX_BN / 2, true))) return st;
-    if ((st = encode_u8(ctx, &tmSA, SAp, 256, (L.Mp / 128) * L.n_chunks * 2, 256, 2 * chunks, false))) return st;
+    if (chunks >= 2) {  // 4 KB per pair of A's chunks, as 16 rows of 256 B
+        if ((st = encode_u8(ctx, &tmSA, SAp, 256, (L.Mp / 128) * (L.n_chunks / 2) * 16, 256, 8 * chunks, false)))
+            return st;
+    } else if ((st = encode_u8(ctx, &tmSA, SAp, 256, (L.Mp / 128) * L.n_chunks * 2, 256, 2 * chunks, false))) {
+        return st;
+    }
     if ((st = encode_u8(ctx, &tmSB, SBp, 256, L.n_tiles * L.n_chunks * 16, 256, 16 * chunks, false))) return st;
     MxParams p;
     p.D = D;
