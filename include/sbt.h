@@ -301,12 +301,16 @@ SBT_API sbt_status sbt_gemm_bounded(sbt_context* ctx, const void* A, int64_t lda
  * 2^119 with E4M3 operands; any E4M3 scale).  NaN codes propagate to the row
  * (A, a_scale) or column (B, b_scale) of D they feed.
  *
- * Paths: with E4M3/E5M2/E2M1 operands, E8M0 scales and K / K_s = 32 the call
- * runs on the tensor cores' block scaling (tcgen05.mma kind::mxf8f6f4, 8-bit
- * staging) under SBT_PATH_AUTO or SBT_PATH_TMA; every other combination, and
- * any combination under SBT_PATH_SCALAR or SBT_PATH_VECTOR, stages the scaled
- * operands as bf16 for the bf16 tensor-core kernel.  The two paths meet the
- * same accuracy statement; they may differ in the order of the fp32 sums.
+ * Paths: under SBT_PATH_AUTO or SBT_PATH_TMA the call runs on the tensor
+ * cores' block scaling when the formats allow it: E2M1 x E2M1 with E8M0 scales
+ * and K / K_s = 32 on tcgen05.mma kind::mxf4 (packed 4-bit operands), E2M1 x
+ * E2M1 with E4M3 scales and K / K_s = 16 on kind::mxf4nvf4 (the scales' signs
+ * are moved onto the operand codes first), and any other mix of E4M3 / E5M2 /
+ * E2M1 with E8M0 scales and K / K_s = 32 on kind::mxf8f6f4 (8-bit staging).
+ * Every other combination, and any combination under SBT_PATH_SCALAR or
+ * SBT_PATH_VECTOR, stages the scaled operands as bf16 for the bf16
+ * tensor-core kernel.  The paths meet the same accuracy statement; they may
+ * differ in the order of the fp32 sums.
  *
  * workspace: device scratch of at least sbt_gemm_block_scaled_workspace_size()
  * bytes (enough for either path), 256-byte aligned, owned by the caller
