@@ -748,10 +748,12 @@ MxLayout mx_layout(int64_t M, int64_t N, int64_t K, int kind) {
     return L;
 }
 
+// Bytes [rows][inner] with row stride `stride` (0: inner), read in boxes of
+// box_rows x box_inner; reads past the extents fill zeros.
 sbt_status encode_u8(sbt_context* ctx, CUtensorMap* map, void* base, int64_t inner, int64_t rows, int box_inner,
-                     int box_rows, bool swizzle) {
+                     int box_rows, bool swizzle, int64_t stride = 0) {
     cuuint64_t dims[2] = {(cuuint64_t)inner, (cuuint64_t)rows};
-    cuuint64_t strides[1] = {(cuuint64_t)inner};
+    cuuint64_t strides[1] = {(cuuint64_t)(stride ? stride : inner)};
     cuuint32_t box[2] = {(cuuint32_t)box_inner, (cuuint32_t)box_rows};
     cuuint32_t estr[2] = {1, 1};
     CUresult r = ctx->encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, estr,
@@ -844,6 +846,10 @@ sbt_status sbt_launch_gemm_mx(sbt_context* ctx, int a_fmt, const void* A, int64_
     const int Ks = (int)(K / block);
     const uint8_t *A8 = (const uint8_t*)A, *B8 = (const uint8_t*)B, *SA8 = (const uint8_t*)SA,
                   *SB8 = (const uint8_t*)SB;
+    // kind::mxf4 reads packed A where it lies when its rows start on 16-byte boundaries (the
+    // tensor map zero-fills past K and M, as the staging would); kind::mxf4nvf4 must stage A to
+    // move scale signs onto its codes, and kind::mxf8f6f4's 8-bit A is staged as before
+    const bool direct_a = kind == kKindF4 && lda % 32 == 0 && (reinterpret_cast<uintptr_t>(A) & 15u) == 0;
 
     // 1. staging
     {
@@ -853,14 +859,14 @@ sbt_status sbt_launch_gemm_mx(sbt_context* ctx, int a_fmt, const void* A, int64_
         if (kind == kKindNvF4)
             k_mx4_stage_a<true><<<grid, 256, 0, stream>>>(A8, lda, SA8, ld_sa, (int)M, (int)K, Ap, (int)L.Kb, tasks,
                                                           nan_a, nan_n);
-        else if (kind == kKindF4)
+        else if (kind == kKindF4 && !direct_a)
             k_mx4_stage_a<false><<<grid, 256, 0, stream>>>(A8, lda, SA8, ld_sa, (int)M, (int)K, Ap, (int)L.Kb, tasks,
                                                            nullptr, 0);
-        else if (a_fmt == kMxFmtE2M1)
+        else if (kind == kKindF8F6F4 && a_fmt == kMxFmtE2M1)
             k_mx_stage_a<true><<<grid, 256, 0, stream>>>(A8, lda, (int)M, (int)K, Ap, (int)L.Kb, tasks);
-        else
+        else if (kind == kKindF8F6F4)
             k_mx_stage_a<false><<<grid, 256, 0, stream>>>(A8, lda, (int)M, (int)K, Ap, (int)L.Kb, tasks);
-        sbt_status st = sbt_after_launch(ctx, "gemm_block_scaled (stage A)");
+        sbt_status st = direct_a ? SBT_OK : sbt_after_launch(ctx, "gemm_block_scaled (stage A)");
         if (st) return st;
         dim3 g2((unsigned)sbt_cdiv(Kp, kBtK), (unsigned)(L.Np / kBtN));
         if (kind == kKindNvF4)
@@ -897,7 +903,8 @@ sbt_status sbt_launch_gemm_mx(sbt_context* ctx, int a_fmt, const void* A, int64_
     // 2. block-scaled tensor-core kernel
     const int chunks = (int)(L.n_chunks / L.k_blocks);
     CUtensorMap tmA, tmB, tmSA, tmSB;
-    sbt_status st = encode_u8(ctx, &tmA, Ap, L.Kb, L.Mp, MX_BK, 128, true);
+    sbt_status st = direct_a ? encode_u8(ctx, &tmA, const_cast<void*>(A), K / 2, M, MX_BK, 128, true, lda / 2)
+                             : encode_u8(ctx, &tmA, Ap, L.Kb, L.Mp, MX_BK, 128, true);
     if (st) return st;
     if ((st = encode_u8(ctx, &tmB, Bp, L.Kb, L.Np, MX_BK, MX_BN / 2, true))) return st;
     if (chunks >= 2) {  // 4 KB per pair of A's chunks, as 16 rows of 256 B

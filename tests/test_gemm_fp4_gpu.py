@@ -164,3 +164,39 @@ def test_full_size_sampled_rows_and_columns(ctx, form):
     rows = np.concatenate([[0, 1, 127, 128, 255, 256, M - 2, M - 1], synth.int_below(660, 40, M)])
     cols = np.concatenate([[0, 1, 207, 208, 415, 416, N - 2, N - 1], synth.int_below(661, 32, N)])
     sampled_check(got, g, rows, cols)
+
+
+@pytest.mark.parametrize("lda_extra,offset,launches", [(0, 0, 3), (0, 16, 3), (2, 0, 4), (0, 2, 4)],
+                         ids=["aligned_rows_in_place", "offset_16_in_place", "row_stride_staged",
+                              "offset_2_staged"])
+def test_mxf4_a_read_in_place_or_staged(ctx, lda_extra, offset, launches):
+    # kind::mxf4 reads packed A where it lies when its rows start on 16-byte boundaries (lda a
+    # multiple of 32 codes, base 16-byte aligned): three launches (B, scales, tensor kernel);
+    # otherwise A is staged first (four).  M, N and K cut tiles, K blocks and the 128-byte box.
+    import torch
+    import scatter_boundary_tile_gb300 as sbt
+    from gpu_helpers import Canvas, dev, sync
+    M, N, K = 300, 230, 544
+    g = packed(M, N, K, ("e8m0", 32), tag=36)
+    lda = K + lda_extra
+    codes = np.stack([g["A"] & 15, g["A"] >> 4], axis=-1).reshape(M, -1)[:, :K]
+    A = np.zeros((M, lda // 2), np.uint8)
+    A[:, :K // 2] = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    if lda_extra:
+        A[:, K // 2:] = 0x77  # padding codes 6.0: a read past K would show
+    g["A"], g["lda"] = A, lda
+    buf = torch.zeros(A.size + 64, dtype=torch.uint8, device="cuda")
+    buf[offset:offset + A.size] = dev(A.reshape(-1))
+    canvas = Canvas(M * g["ldd"] * 4)
+    ws_n = sbt.gemm_block_scaled_workspace_size(ctx, M, N, K)
+    ws = torch.empty(ws_n, dtype=torch.uint8, device="cuda")
+    before = ctx.launch_count
+    sbt.gemm_block_scaled(ctx, buf[offset:], lda, dev(g["B"]), g["ldb"], dev(g["SA"]), g["ld_sa"], dev(g["SB"]),
+                          g["ld_sb"], g["Ks"], canvas.ptr, g["ldd"], M, N, K, workspace=ws, workspace_bytes=ws_n,
+                          a_fmt="e2m1", b_fmt="e2m1", s_fmt="e8m0")
+    sync()
+    ctx.check_status()
+    assert ctx.launch_count - before == launches
+    assert canvas.guards_intact()
+    got = canvas.inner(np.float32, (M, g["ldd"]))[:, :N].astype(np.float64)
+    check(got, g)
