@@ -19,6 +19,8 @@ C ABI and check:
 
 This file is collected last on purpose.
 """
+import gc
+
 import numpy as np
 import pytest
 import torch
@@ -137,14 +139,23 @@ def test_call_allocates_nothing(ctx):
     sbt.gemm_bounded(ctx, A, g["lda"], B, g["ldb"], C, g["ldc"], M, N, K, ws, ws_n)
     sync()
     per_call = ctx.launch_count - n0
-    free0, _ = torch.cuda.mem_get_info()
-    alloc0 = torch.cuda.memory_allocated()
-    n0 = ctx.launch_count
-    for _ in range(3):
-        sbt.gemm_bounded_noalloc(ctx, A, g["lda"], B, g["ldb"], C, g["ldc"], M, N, K)
+    # tensors of earlier tests freed by the garbage collector inside the window would move the
+    # counters: collect first and keep the collector off while measuring
+    gc.collect()
     sync()
-    ctx.check_status()
-    free1, _ = torch.cuda.mem_get_info()
+    gc.disable()
+    try:
+        free0, _ = torch.cuda.mem_get_info()
+        alloc0 = torch.cuda.memory_allocated()
+        n0 = ctx.launch_count
+        for _ in range(3):
+            sbt.gemm_bounded_noalloc(ctx, A, g["lda"], B, g["ldb"], C, g["ldc"], M, N, K)
+        sync()
+        ctx.check_status()
+        free1, _ = torch.cuda.mem_get_info()
+        alloc1 = torch.cuda.memory_allocated()
+    finally:
+        gc.enable()
     assert ctx.launch_count - n0 == 3 * per_call
     assert free1 == free0
-    assert torch.cuda.memory_allocated() == alloc0
+    assert alloc1 == alloc0
