@@ -14,14 +14,16 @@
 //    flips its bit 3, exactly), writes a NaN scale as zero and marks its row
 //    of A or column of B; the epilogue writes NaN there.
 // The packed forms carry half the operand bytes of the 8-bit form per element
-// of K, and the kernel is bound by the bytes each SM takes in (below).
+// of K; what bounds each form is noted with its constants below.
 //
 // Pipeline (all on the caller's stream):
 //  1. Staging (the bounded copy of Tylo.jl "Boundary tiles"): A -> A8 [Mp][Kb]
 //     and B -> B8^T [Np][Kb], K-major, Kb bytes per row (8-bit codes or packed
 //     E2M1 pairs), zero past M, N, K; the scales packed per (row or column
 //     tile, four scales along K) into chunks in the order the tensor memory
-//     wants them (below), neutral past the extents.
+//     wants them (below), neutral past the extents.  kind::mxf4 reads a packed
+//     A whose rows start on 16-byte boundaries where it lies instead (the
+//     tensor map's fill gives the zeros past M and K).
 //  2. A persistent kernel on clusters of two CTAs (M = 256 per pair, N = 208
 //     per tile): warp 0 of each CTA TMA-loads its 128 rows of A8, its 104 rows
 //     of B8^T and the scale chunks of the stage's K blocks into a ring (a K
@@ -29,8 +31,9 @@
 //     256 packed E2M1 codes); the leader's warp 1 copies the scale chunks into
 //     TMEM (tcgen05.cp.cta_group::2, each CTA's own chunk to its own TMEM) and
 //     issues four block-scaled MMAs per K block, 32 bytes of K each, each
-//     choosing its chunk and scale bytes; four epilogue warps per CTA add acc
-//     and store fp32 D inside M x N.
+//     choosing its chunk and scale bytes; the epilogue warps of each CTA (four
+//     for the 8-bit form, twelve for the packed ones) add acc and store fp32 D
+//     inside M x N.
 //
 // Scale placement in TMEM (per CTA, 32-bit columns, 4 scale bytes each): a
 // chunk holds four consecutive scales along K (entries 4c .. 4c + 3 of chunk
@@ -40,9 +43,10 @@
 // instruction reads byte sf_id (1X), bytes sf_id and sf_id + 1 (2X) or all
 // four (4X).  Scale addresses must be multiples of 4 columns.  A's chunk comes
 // with one tcgen05.cp 32x128b.warpx4 (row r of a [32][16-byte] chunk to lane r
-// of every quarter: byte 16 r + 4 j + s = entry s of row 32 j + r); B's with
-// one tcgen05.cp 128x256b from a 4 KB chunk that repeats the same 32 rows for
-// the four quarters.  Each copy costs about the same in the MMA stream
+// of every quarter: byte 16 r + 4 j + s = entry s of row 32 j + r), or, in the
+// packed forms, two chunks at once with one tcgen05.cp 128x256b; B's with one
+// tcgen05.cp 128x256b from a 4 KB chunk that repeats the same 32 rows for the
+// four quarters.  Each copy costs about the same in the MMA stream
 // whatever its size (three 512-byte copies per 8-bit K block cost ~57 us of
 // the 8191 x 8193 x 4096 call, two copies ~39 us), so B's eight columns take
 // one larger copy.
