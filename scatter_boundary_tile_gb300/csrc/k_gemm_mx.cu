@@ -201,41 +201,41 @@ __device__ __forceinline__ void mx_epilogue_tile(const MxParams& p, uint32_t tme
                 }
                 __syncwarp();
             }
-            continue;
-        }
+        } else {
 #pragma unroll
-        for (int j = 0; j < 32; ++j) buf[lane * 33 + j] = __uint_as_float(r[j]);
-        __syncwarp();
-        const int col = n0 + c * 32 + lane;
-        if (c * 32 + lane < n_valid) {
-            bool nan_col = false;
-            if constexpr (KIND == kKindNvF4) nan_col = p.nan_b[col] != 0;
-            const int rows = min(32, p.M - row0);
-            // two halves of 16 rows: all loads of a half issue before its stores (a loop carrying
-            // each store behind its own shared load ran at ~90 cycles a row)
+            for (int j = 0; j < 32; ++j) buf[lane * 33 + j] = __uint_as_float(r[j]);
+            __syncwarp();
+            const int col = n0 + c * 32 + lane;
+            if (c * 32 + lane < n_valid) {
+                bool nan_col = false;
+                if constexpr (KIND == kKindNvF4) nan_col = p.nan_b[col] != 0;
+                const int rows = min(32, p.M - row0);
+                // two halves of 16 rows: all loads of a half issue before its stores (a loop carrying
+                // each store behind its own shared load ran at ~90 cycles a row)
 #pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
-                float v[16];
+                for (int h = 0; h < 2; ++h) {
+                    float v[16];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) v[i] = buf[(16 * h + i) * 33 + lane];
-                if (p.acc) {
-                    const float* a = p.acc + (int64_t)(row0 + 16 * h) * p.ld_acc + col;
+                    for (int i = 0; i < 16; ++i) v[i] = buf[(16 * h + i) * 33 + lane];
+                    if (p.acc) {
+                        const float* a = p.acc + (int64_t)(row0 + 16 * h) * p.ld_acc + col;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (16 * h + i < rows) v[i] += __ldg(a + (int64_t)i * p.ld_acc);
+                    }
+                    if constexpr (KIND == kKindNvF4) {
+#pragma unroll
+                        for (int i = 0; i < 16; ++i)
+                            if (nan_col || ((nan_rows >> (16 * h + i)) & 1u)) v[i] = __uint_as_float(0x7FC00000u);
+                    }
+                    float* d = p.D + (int64_t)(row0 + 16 * h) * p.ldd + col;
 #pragma unroll
                     for (int i = 0; i < 16; ++i)
-                        if (16 * h + i < rows) v[i] += __ldg(a + (int64_t)i * p.ld_acc);
+                        if (16 * h + i < rows) d[(int64_t)i * p.ldd] = v[i];
                 }
-                if constexpr (KIND == kKindNvF4) {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        if (nan_col || ((nan_rows >> (16 * h + i)) & 1u)) v[i] = __uint_as_float(0x7FC00000u);
-                }
-                float* d = p.D + (int64_t)(row0 + 16 * h) * p.ldd + col;
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    if (16 * h + i < rows) d[(int64_t)i * p.ldd] = v[i];
             }
+            __syncwarp();
         }
-        __syncwarp();
     }
 }
 
