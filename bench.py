@@ -596,7 +596,7 @@ def run_ops(ctx, pk):
             entry["kernels_ms"] = split
         ops[f"gemm_bounded_{M}x{N}x{K}_aligned"] = entry
         del Ad, Bd, C, ws
-    except Exception as e:  # the GEMM may be unavailable in this build
+    except Exception as e:  # a library built without the GEMM
         ops["gemm_bounded"] = {"unavailable": str(e).splitlines()[0][:200]}
 
     # block-scaled GEMM: E4M3 operands, E8M0 scales over blocks of 32 along K, fp32 out;
