@@ -325,3 +325,15 @@ def test_workspace_errors(ctx):
         sbt.gemm_bounded(ctx, A, g["lda"], B, g["ldb"], C, g["ldc"], 65, 97, 73, ws, n, c_dtype=sbt.SBT_F16)
     assert e.value.status == sbt.SBT_ERR_UNSUPPORTED
     assert ctx.launch_count == before
+
+
+@pytest.mark.parametrize("mnk,c_dtype", [((1000, 1000, 1000), "bf16"), ((4096, 2560, 512), "bf16"),
+                                         ((4096, 2560, 256), "f32")],
+                         ids=["single_cta", "cta_pair_512_rows", "cta_pair_fp32"])
+def test_repeated_calls_bit_identical(ctx, mnk, c_dtype):
+    # each tile's K order is fixed by the kernel, so the same inputs give the same bits on every call
+    M, N, K = mnk
+    g = wl.gemm_bf16(M=M, N=N, K=K, tag=26)
+    first, _ = run_gemm(ctx, g, c_dtype)  # C widened to float64 exactly
+    again, _ = run_gemm(ctx, g, c_dtype)
+    assert np.array_equal(first.view(np.uint64), again.view(np.uint64))
