@@ -286,6 +286,24 @@ def time_launches(fn, reps: int, warmup: int = 3, flush=None):
     return statistics.median(times), statistics.fmean(times), min(times)
 
 
+def time_back_to_back(fn, reps: int = 200):
+    """Mean device time (ms) per call of fn() over reps calls queued back to back behind one
+    spin (steady-state launch throughput: no call waits for a fresh launch after a gate)."""
+    import torch
+    for _ in range(5):
+        fn()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    torch.cuda._sleep(4 * GATE_CYCLES)  # keeps the host's queueing ahead of the device
+    a.record()
+    for _ in range(reps):
+        fn()
+    b.record()
+    b.synchronize()
+    return a.elapsed_time(b) / reps
+
+
 def kernel_split(fn, reps: int):
     """Mean device time (ms) per launch of each kernel fn() launches, from CUPTI kernel
     records (torch.profiler); {} if the profiler is unavailable."""
@@ -566,6 +584,8 @@ def run_ops(ctx, pk):
                      "frac_bf16_sustained": tf / pk["bf16_tflops_sustained"], "flops": flops,
                      "lda": g["lda"], "ldb": g["ldb"], "ldc": g["ldc"],
                      "note": "whole call: one realigning staging launch (odd leading dimensions) + tensor-core kernel"}
+            if flops < 1e10:  # small shapes: per-call time with the launches of consecutive calls overlapped
+                entry["ms_back_to_back"] = time_back_to_back(fn)
             split = kernel_split(fn, 5)
             if split:
                 entry["kernels_ms"] = split
@@ -586,6 +606,28 @@ def run_ops(ctx, pk):
         ws = torch.empty(max(ws_n, 1), dtype=torch.uint8, device="cuda")
         fn = lambda: sbt.gemm_bounded(ctx, Ad, K, Bd, N, C, N, M, N, K, ws, ws_n)
         med, _, _ = time_launches(fn, 10)
+        # (1000, 1000, 1000) with rows 16-byte aligned: one launch per call
+        m1, n1, k1 = 1000, 1000, 1000
+        g1 = wl.gemm_bf16(M=m1, N=n1, K=k1)
+        A1 = np.zeros((m1, 1000), np.uint16)
+        A1[:, :k1] = g1["A"][:, :k1]
+        B1 = np.zeros((k1, 1000), np.uint16)
+        B1[:, :n1] = g1["B"][:, :n1]
+        A1d, B1d = dev_bytes(A1), dev_bytes(B1)
+        C1 = torch.empty(m1 * 1000 * 2, dtype=torch.uint8, device="cuda")
+        ws1_n = sbt.gemm_bounded_workspace_size(ctx, m1, n1, k1, 1000, 1000)
+        ws1 = torch.empty(max(ws1_n, 1), dtype=torch.uint8, device="cuda")
+        f1 = lambda: sbt.gemm_bounded(ctx, A1d, 1000, B1d, 1000, C1, 1000, m1, n1, k1, ws1, ws1_n)
+        n0 = ctx.launch_count
+        f1()
+        launches1 = ctx.launch_count - n0
+        ms1, _, _ = time_launches(f1, 30)
+        ops["gemm_bounded_1000x1000x1000_aligned"] = {
+            "ms": ms1, "ms_back_to_back": time_back_to_back(f1), "launches_per_call": launches1,
+            "lda": 1000, "ldb": 1000, "ldc": 1000,
+            "note": "rows 16-byte aligned: TMA reads A and B where they lie; ms is one call behind a device "
+                    "spin, ms_back_to_back the steady-state time per call"}
+        del A1d, B1d, C1, ws1
         flops = 2.0 * M * N * K
         tf = flops / med / 1e9
         entry = {"ms": med, "TFLOP/s": tf, "frac_bf16": tf / pk["bf16_tflops"],
