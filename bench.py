@@ -295,7 +295,9 @@ def time_back_to_back(fn, reps: int = 200):
     torch.cuda.synchronize()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
-    torch.cuda._sleep(4 * GATE_CYCLES)  # keeps the host's queueing ahead of the device
+    # a spin long enough (~50 us of device time per call) for the host to queue every call before
+    # the first one runs, so that the events time the device alone
+    torch.cuda._sleep(100_000 * reps)
     a.record()
     for _ in range(reps):
         fn()
