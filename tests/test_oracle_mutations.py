@@ -108,6 +108,14 @@ MUTATIONS = {
     "a_scale_decoded_in_the_operand_format": (
         "oracle_fp8_decode(sfmt, SA[m * ldsa + k / block])",
         "oracle_fp8_decode(afmt, SA[m * ldsa + k / block])"),
+    "b_scale_sign_ignored": (
+        "oracle_fp8_decode(sfmt, SB[(k / block) * ldsb + n])",
+        "fabs(oracle_fp8_decode(sfmt, SB[(k / block) * ldsb + n]))"),
+    "a_scale_sign_ignored": (
+        "oracle_fp8_decode(sfmt, SA[m * ldsa + k / block])",
+        "fabs(oracle_fp8_decode(sfmt, SA[m * ldsa + k / block]))"),
+    "b_scale_read_with_the_a_scale_stride": ("SB[(k / block) * ldsb + n]", "SB[(k / block) * ldsa + n]"),
+    "scale_block_fixed_at_32": ("SA[m * ldsa + k / block]", "SA[m * ldsa + k / 32]"),
     # more movement mistakes
     "gather_cols_column_bound_dropped": (
         "if (r >= 0 && r < rows && c >= 0 && c < cols)\n                put(out, i * ld_out + k",

@@ -575,6 +575,31 @@ def test_block_scaled_e4m3_scales_equal_broadcast_matmul():
     np.testing.assert_allclose(C, a @ b, rtol=1e-12, atol=1e-9)
 
 
+def test_block_scaled_e2m1_with_signed_e4m3_scales_equal_broadcast_matmul():
+    # The NVFP4 combination: packed E2M1 operands, E4M3 scales per 16, the scale codes drawn
+    # over the whole format (negative, +0 and -0, subnormal, up to 448; NaN excluded), and
+    # a different leading dimension for every array. The expected value is the definition
+    # in numpy: operand values from the E2M1 table, scale values from torch's E4M3 decode,
+    # the scales repeated over their blocks of 16, then one matmul.
+    M, N, K, bs = 9, 14, 96, 16
+    Ks = K // bs
+    lda, ldb, ldsa, ldsb = K + 10, N + 4, Ks + 3, N + 1
+    ca = synth.int_below(89, M * lda, 16).astype(np.uint8).reshape(M, lda)
+    cb = synth.int_below(90, K * ldb, 16).astype(np.uint8).reshape(K, ldb)
+    pack = lambda c: (c[:, 0::2] | (c[:, 1::2] << 4)).astype(np.uint8)
+    SA, SB = _fp8_codes(91, (M, ldsa)), _fp8_codes(92, (Ks, ldsb))
+    SA[0, :3] = [0x00, 0x80, 0x01]   # +0, -0, the smallest subnormal
+    SB[1, :3] = [0xFE, 0x7E, 0x81]   # -448, 448, the smallest negative subnormal
+    table = np.array(E2M1_VALUES + [-v for v in E2M1_VALUES])
+    C = oracle.gemm_block_scaled_f64(pack(ca), lda, SA, ldsa, pack(cb), ldb, SB, ldsb, M, N, K, bs,
+                                     afmt="e2m1", bfmt="e2m1", sfmt="e4m3")
+    a = table[ca[:, :K]] * np.repeat(_e4m3(SA[:, :Ks]), bs, axis=1)
+    b = table[cb[:, :N]] * np.repeat(_e4m3(SB[:, :N]), bs, axis=0)
+    assert (a < 0).any() and (_e4m3(SA[:, :Ks]) < 0).any() and (_e4m3(SB[:, :N]) < 0).any()
+    # every product is exact in double; the two sums differ only in their order of addition
+    np.testing.assert_array_less(np.abs(C - a @ b), 1e-13 * (np.abs(a) @ np.abs(b)) + 1e-300)
+
+
 def test_block_scaled_e2m1_packed_equal_table_matmul():
     # E2M1 operands, two per byte along each row, even element in the low nibble.
     M, N, K, bs = 6, 10, 64, 32
