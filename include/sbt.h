@@ -14,6 +14,9 @@
  *  - All array pointers are DEVICE pointers (cudaMalloc'd or otherwise
  *    device-addressable).  `pad_value` is a HOST pointer to one element's bits.
  *    The caller owns every buffer; the library allocates no device memory.
+ *  - Every array pointer is a multiple of its element size (int32 indices and
+ *    cu_seqlens: 4 bytes; 8-bit codes, scales and masks: any address); a call
+ *    given one that is not returns SBT_ERR_ALIGNMENT before any launch.
  *  - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
  *    default stream) and returns after enqueueing.  Arguments are validated on
  *    the host before anything is launched; on error nothing is launched and
@@ -46,7 +49,8 @@ typedef enum {
     SBT_OK = 0,
     SBT_ERR_INVALID_ARG = 1,    /* null pointer, negative extent, bad stride, tile too large, ... */
     SBT_ERR_UNSUPPORTED = 2,    /* dtype or combination this op does not take */
-    SBT_ERR_ALIGNMENT = 3,      /* workspace not 256-byte aligned or too small */
+    SBT_ERR_ALIGNMENT = 3,      /* array pointer not on a multiple of its element size; workspace not
+                                   256-byte aligned or too small */
     SBT_ERR_TENSOR_MAP = 4,     /* the driver refused a TMA descriptor (Mojo "RaggedTMA3DTile": create raises) */
     SBT_ERR_CUDA = 5,           /* a CUDA runtime/driver call failed */
     SBT_ERR_DEVICE_TIMEOUT = 6  /* a bounded device-side wait ran out (see sbt_check_status) */

@@ -63,6 +63,15 @@ sbt_status sbt_after_launch(sbt_context* ctx, const char* what) {
         if (!(cond)) return sbt_fail(SBT_ERR_INVALID_ARG, (msg));       \
     } while (0)
 
+// Every array starts on a multiple of its element size (int32 indices and
+// cu_seqlens on 4 bytes): the kernels' element accesses are naturally aligned,
+// so a pointer that is not is refused here, before anything touches the device.
+#define SBT_REQUIRE_ALIGNED(ptr, bytes, msg)                                                    \
+    do {                                                                                        \
+        if ((reinterpret_cast<uintptr_t>(ptr) % (uintptr_t)(bytes)) != 0)                       \
+            return sbt_fail(SBT_ERR_ALIGNMENT, (msg));                                          \
+    } while (0)
+
 extern "C" {
 
 const char* sbt_last_error_message(void) { return t_last_error.c_str(); }
@@ -174,6 +183,8 @@ sbt_status sbt_tile_load_padded(sbt_context* ctx, sbt_dtype dtype, const void* s
     SBT_REQUIRE(dst_tiles, "tile_load_padded: dst_tiles is NULL");
     SBT_REQUIRE(stride_r != 0 && stride_c != 0, "tile_load_padded: strides must be nonzero");
     SBT_REQUIRE(rows * cols == 0 || src, "tile_load_padded: src is NULL");
+    SBT_REQUIRE_ALIGNED(src, es, "tile_load_padded: src is not aligned to its element size");
+    SBT_REQUIRE_ALIGNED(dst_tiles, es, "tile_load_padded: dst_tiles is not aligned to its element size");
     if ((st = sbt_use_device(ctx))) return st;
     return sbt_launch_tile_load(ctx, es, src, rows, cols, stride_r, stride_c, origin_r, origin_c, step_r, step_c,
                                 grid_r, grid_c, tile_r, tile_c, dst_tiles, sbt_pad_word(pad_value, es),
@@ -194,6 +205,8 @@ sbt_status sbt_tile_store_clipped(sbt_context* ctx, sbt_dtype dtype, const void*
     if ((int64_t)grid_r * grid_c == 0 || rows * cols == 0) return SBT_OK;
     SBT_REQUIRE(src_tiles && dst, "tile_store_clipped: NULL pointer");
     SBT_REQUIRE(stride_r != 0 && stride_c != 0, "tile_store_clipped: strides must be nonzero");
+    SBT_REQUIRE_ALIGNED(src_tiles, es, "tile_store_clipped: src_tiles is not aligned to its element size");
+    SBT_REQUIRE_ALIGNED(dst, es, "tile_store_clipped: dst is not aligned to its element size");
     if ((st = sbt_use_device(ctx))) return st;
     if (sbt_tile_store_runs_ok(ctx, es, src_tiles, grid_r, grid_c, tile_r, tile_c, dst, stride_r, stride_c, origin_c,
                                step_c))
@@ -219,6 +232,9 @@ sbt_status sbt_gather_rows(sbt_context* ctx, sbt_dtype dtype, const void* src, i
     SBT_REQUIRE(rows * cols == 0 || src, "gather_rows: src is NULL");
     SBT_REQUIRE(rows * cols == 0 || ld_src >= cols, "gather_rows: ld_src < cols");
     SBT_REQUIRE(!mask || ld_mask >= tile_c, "gather_rows: ld_mask < tile_c");
+    SBT_REQUIRE_ALIGNED(src, es, "gather_rows: src is not aligned to its element size");
+    SBT_REQUIRE_ALIGNED(out, es, "gather_rows: out is not aligned to its element size");
+    SBT_REQUIRE_ALIGNED(idx, 4, "gather_rows: idx is not 4-byte aligned");
     if ((st = sbt_use_device(ctx))) return st;
     return sbt_launch_gather(ctx, es, src, rows, cols, ld_src, idx, n_idx, row_offset, col_offset, tile_c, mask,
                              ld_mask, out, ld_out, sbt_pad_word(pad_value, es), (cudaStream_t)stream);
@@ -238,6 +254,9 @@ sbt_status sbt_gather_cols(sbt_context* ctx, sbt_dtype dtype, const void* src, i
     SBT_REQUIRE(idx && out, "gather_cols: NULL idx or out");
     SBT_REQUIRE(rows * cols == 0 || src, "gather_cols: src is NULL");
     SBT_REQUIRE(rows * cols == 0 || ld_src >= cols, "gather_cols: ld_src < cols");
+    SBT_REQUIRE_ALIGNED(src, es, "gather_cols: src is not aligned to its element size");
+    SBT_REQUIRE_ALIGNED(out, es, "gather_cols: out is not aligned to its element size");
+    SBT_REQUIRE_ALIGNED(idx, 4, "gather_cols: idx is not 4-byte aligned");
     if ((st = sbt_use_device(ctx))) return st;
     return sbt_launch_gather_cols(ctx, es, src, rows, cols, ld_src, idx, n_idx, row_offset, col_offset, tile_r, out,
                                   ld_out, sbt_pad_word(pad_value, es), (cudaStream_t)stream);
@@ -258,6 +277,9 @@ sbt_status sbt_scatter_rows_masked(sbt_context* ctx, sbt_dtype dtype, void* dst,
     SBT_REQUIRE(ld_dst >= cols, "scatter_rows_masked: ld_dst < cols");
     SBT_REQUIRE(ld_src >= tile_c, "scatter_rows_masked: ld_src < tile_c");
     SBT_REQUIRE(!mask || ld_mask >= tile_c, "scatter_rows_masked: ld_mask < tile_c");
+    SBT_REQUIRE_ALIGNED(dst, es, "scatter_rows_masked: dst is not aligned to its element size");
+    SBT_REQUIRE_ALIGNED(src, es, "scatter_rows_masked: src is not aligned to its element size");
+    SBT_REQUIRE_ALIGNED(idx, 4, "scatter_rows_masked: idx is not 4-byte aligned");
     if ((st = sbt_use_device(ctx))) return st;
     return sbt_launch_scatter(ctx, es, dst, rows, cols, ld_dst, idx, n_idx, row_offset, col_offset, src, ld_src,
                               tile_c, mask, ld_mask, (cudaStream_t)stream);
@@ -276,6 +298,9 @@ sbt_status sbt_ragged_tile_load(sbt_context* ctx, sbt_dtype dtype, const void* x
     SBT_REQUIRE(out && cu_seqlens, "ragged_tile_load: NULL out or cu_seqlens");
     SBT_REQUIRE(total_rows == 0 || x, "ragged_tile_load: x is NULL");
     SBT_REQUIRE(ld_row > 0 && ld_head > 0, "ragged_tile_load: strides must be positive");
+    SBT_REQUIRE_ALIGNED(x, es, "ragged_tile_load: x is not aligned to its element size");
+    SBT_REQUIRE_ALIGNED(out, es, "ragged_tile_load: out is not aligned to its element size");
+    SBT_REQUIRE_ALIGNED(cu_seqlens, 4, "ragged_tile_load: cu_seqlens is not 4-byte aligned");
     if ((st = sbt_use_device(ctx))) return st;
     return sbt_launch_ragged(ctx, es, x, total_rows, heads, depth, ld_row, ld_head, cu_seqlens, batch, t_pad, out,
                              (cudaStream_t)stream);
@@ -293,6 +318,10 @@ sbt_status sbt_scatter_add_rows(sbt_context* ctx, sbt_dtype dtype, void* dst, in
     SBT_REQUIRE(dst && idx && src, "scatter_add_rows: NULL pointer");
     SBT_REQUIRE(ld_dst >= cols, "scatter_add_rows: ld_dst < cols");
     SBT_REQUIRE(ld_src >= tile_c, "scatter_add_rows: ld_src < tile_c");
+    const int es = kind == 4 ? 4 : 2;
+    SBT_REQUIRE_ALIGNED(dst, es, "scatter_add_rows: dst is not aligned to its element size");
+    SBT_REQUIRE_ALIGNED(src, es, "scatter_add_rows: src is not aligned to its element size");
+    SBT_REQUIRE_ALIGNED(idx, 4, "scatter_add_rows: idx is not 4-byte aligned");
     sbt_status st = sbt_use_device(ctx);
     if (st) return st;
     return sbt_launch_scatter_add(ctx, kind, dst, rows, cols, ld_dst, idx, n_idx, row_offset, col_offset, src, ld_src,
@@ -311,6 +340,9 @@ sbt_status sbt_ragged_tile_store(sbt_context* ctx, sbt_dtype dtype, const void* 
     if ((int64_t)batch * heads * t_pad * depth == 0 || total_rows == 0) return SBT_OK;
     SBT_REQUIRE(tiles && cu_seqlens && x, "ragged_tile_store: NULL pointer");
     SBT_REQUIRE(ld_row > 0 && ld_head > 0, "ragged_tile_store: strides must be positive");
+    SBT_REQUIRE_ALIGNED(tiles, es, "ragged_tile_store: tiles is not aligned to its element size");
+    SBT_REQUIRE_ALIGNED(x, es, "ragged_tile_store: x is not aligned to its element size");
+    SBT_REQUIRE_ALIGNED(cu_seqlens, 4, "ragged_tile_store: cu_seqlens is not 4-byte aligned");
     if ((st = sbt_use_device(ctx))) return st;
     return sbt_launch_ragged_store(ctx, es, tiles, batch, heads, depth, t_pad, cu_seqlens, x, total_rows, ld_row,
                                    ld_head, (cudaStream_t)stream);
@@ -336,6 +368,9 @@ sbt_status sbt_gemm_bounded(sbt_context* ctx, const void* A, int64_t lda, const 
     if (M == 0 || N == 0) return SBT_OK;
     SBT_REQUIRE(C, "gemm_bounded: C is NULL");
     SBT_REQUIRE(K == 0 || (A && B), "gemm_bounded: NULL A or B");
+    SBT_REQUIRE_ALIGNED(A, 2, "gemm_bounded: A is not 2-byte aligned");
+    SBT_REQUIRE_ALIGNED(B, 2, "gemm_bounded: B is not 2-byte aligned");
+    SBT_REQUIRE_ALIGNED(C, c_dtype == SBT_F32 ? 4 : 2, "gemm_bounded: C is not aligned to its element size");
     size_t need = sbt_gemm_workspace_bytes(M, N, K);
     if (need > 0) {
         if (!workspace || workspace_bytes < need)
@@ -382,6 +417,8 @@ sbt_status sbt_gemm_block_scaled(sbt_context* ctx, sbt_lowp_format a_fmt, const 
     if (M == 0 || N == 0) return SBT_OK;
     SBT_REQUIRE(D, "gemm_block_scaled: D is NULL");
     SBT_REQUIRE(K == 0 || (A && B && a_scale && b_scale), "gemm_block_scaled: NULL operand or scale");
+    SBT_REQUIRE_ALIGNED(acc, 4, "gemm_block_scaled: acc is not 4-byte aligned");
+    SBT_REQUIRE_ALIGNED(D, 4, "gemm_block_scaled: D is not 4-byte aligned");
     const size_t need = std::max(sbt_gemm_workspace_bytes(M, N, K), sbt_gemm_mx_workspace_bytes(M, N, K));
     if (need > 0) {
         if (!workspace || workspace_bytes < need)

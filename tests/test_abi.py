@@ -67,3 +67,51 @@ def test_noalloc_scratch_size_matches_header():
     m = re.search(r"#define\s+SBT_GEMM_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", text)
     assert m, "SBT_GEMM_NOALLOC_SCRATCH_BYTES not found in include/sbt.h"
     assert int(m.group(1)) << int(m.group(2)) == sbt.GEMM_NOALLOC_SCRATCH_BYTES
+
+
+# --------------------------------------------------------------------------- pointer alignment
+# Every call refuses an array pointer that is not a multiple of its element size before it
+# touches the device.  The calls are made with a zero-filled host buffer standing in for the
+# context (the calls test it only for NULL before validating) and addresses that are never
+# dereferenced; with a GPU present the test does not run, so a stand-in context never
+# reaches a device.
+F32, BF16 = 0, 1
+E4M3, E8M0 = 0, 2
+X = 1 << 20  # an address on a 1 MiB boundary; every pointer below is X + a multiple of 4096
+
+
+def _alignment_cases():
+    p = lambda k: X + 4096 * k
+    return {  # call: (positional arguments after ctx, {argument index: required alignment})
+        "sbt_tile_load_padded": ([F32, p(0), 4, 4, 4, 1, 0, 0, 4, 4, 1, 1, 4, 4, p(1), None, None], {1: 4, 14: 4}),
+        "sbt_tile_store_clipped": ([F32, p(0), 1, 1, 4, 4, p(1), 4, 4, 4, 1, 0, 0, 4, 4, None], {1: 4, 6: 4}),
+        "sbt_gather_rows": ([F32, p(0), 4, 4, 4, p(1), 2, 0, 0, 4, None, 0, p(2), 4, None, None],
+                            {1: 4, 5: 4, 12: 4}),
+        "sbt_scatter_rows_masked": ([F32, p(0), 4, 4, 4, p(1), 2, 0, 0, p(2), 4, 4, None, 0, None],
+                                    {1: 4, 5: 4, 9: 4}),
+        "sbt_gather_cols": ([F32, p(0), 4, 4, 4, p(1), 2, 0, 0, 4, p(2), 2, None, None], {1: 4, 5: 4, 10: 4}),
+        "sbt_scatter_add_rows": ([BF16, p(0), 4, 4, 4, p(1), 2, 0, 0, p(2), 4, 4, None], {1: 2, 5: 4, 9: 2}),
+        "sbt_ragged_tile_load": ([BF16, p(0), 8, 2, 4, 8, 4, p(1), 2, 4, p(2), None], {1: 2, 7: 4, 10: 2}),
+        "sbt_ragged_tile_store": ([BF16, p(0), 2, 2, 4, 4, p(1), p(2), 8, 8, 4, None], {1: 2, 6: 4, 7: 2}),
+        "sbt_gemm_bounded": ([p(0), 8, p(1), 8, p(2), 8, F32, 4, 4, 4, p(16), 1 << 30, None], {0: 2, 2: 2, 4: 4}),
+        "sbt_gemm_block_scaled": ([E4M3, p(0), 32, E4M3, p(1), 4, E8M0, p(2), 1, p(3), 4, 1, p(4), 4, p(5), 4,
+                                   4, 4, 32, p(16), 1 << 30, None], {12: 4, 14: 4}),
+    }
+
+
+@pytest.mark.parametrize("name", sorted(_alignment_cases()))
+def test_misaligned_pointers_are_refused_before_the_device(lib, name):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("CPU-only check: a stand-in context must never reach a device")
+    ctx = ctypes.create_string_buffer(4096)
+    args, align = _alignment_cases()[name]
+    fn = getattr(lib, name)
+    for i, a in align.items():
+        for off in range(1, a):
+            bad = list(args)
+            bad[i] = args[i] + off
+            assert fn(ctx, *bad) == sbt.SBT_ERR_ALIGNMENT, (i, off)
+            assert b"aligned" in lib.sbt_last_error_message()
+    # aligned pointers pass validation and stop only at device selection (no GPU here)
+    assert fn(ctx, *args) == sbt.SBT_ERR_CUDA, lib.sbt_last_error_message()
