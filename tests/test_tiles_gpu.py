@@ -41,7 +41,7 @@ def same_bits(a, b):
     return a.shape == b.shape and np.array_equal(a.view(np.uint8), b.view(np.uint8))
 
 
-@pytest.mark.parametrize("path", ["auto", "tma", "scalar"])
+@pytest.mark.parametrize("path", ["auto", "tma", "vector", "scalar"])
 def test_small_fp32_grid_load_and_store(ctx, path):
     a = wl.tiles_small()["a"]
     got = gpu_load(ctx, a, 65, 73, 73, 1, 0, 0, 64, 32, 2, 3, 64, 32, "f32", pad=0.0, path=path)
@@ -116,6 +116,8 @@ STORE_CASES = [
     (40, 300, 301, 1, (1, 3), (8, 128), (5, 3), (8, 128)),      # 32 (fp32) / 16 (bf16) vectors per tile row
     (33, 37, 37, 1, (0, 1), (3, 8), (11, 5), (3, 8)),           # 2 (fp32) / 1 (bf16) vectors per tile row
     (40, 100, 101, 1, (0, 0), (8, 48), (5, 3), (8, 48)),        # 12 / 6 vectors per row: element rows
+    (5, 8200, 8201, 1, (-1, -9), (2, 256), (3, 33), (2, 256)),  # runs of 2,112 (fp32) / 1,056 vectors: chunks
+    (3, 5000, 5003, 1, (0, 0), (1, 256), (3, 20), (1, 256)),    # 1,280 / 640 vectors per run
 ]
 
 
@@ -131,7 +133,7 @@ def test_store_edge_cases(ctx, case, dtype):
         dst = np.full((rows, ld), 0xDEAD, np.uint16)
     want = dst.copy()
     oracle.tile_store_clipped(tiles, want, rows, cols, ld, sc, r0, c0, str_, stc)
-    for path in ("auto", "tma", "scalar"):
+    for path in ("auto", "tma", "vector", "scalar"):  # unaligned rows: bulk copies, lane-shifted runs, elements
         got = gpu_store(ctx, tiles, dst, rows, cols, ld, sc, r0, c0, str_, stc, dtype, path=path)
         assert same_bits(got, want), path
 
@@ -158,7 +160,8 @@ def test_validation(ctx):
     assert ctx.launch_count == before
 
 
-@pytest.mark.parametrize("shape,path", [((16381, 16411, 16411), "auto"), ((16384, 16416, 16416), "auto"),
+@pytest.mark.parametrize("shape,path", [((16381, 16411, 16411), "auto"), ((16381, 16411, 16411), "vector"),
+                                        ((16384, 16416, 16416), "auto"),
                                         ((16384, 16416, 16416), "tma"), ((16384, 16416, 16416), "vector"),
                                         ((16381, 16411, 16416), "auto")])
 def test_large_fp32_grid(ctx, shape, path):
