@@ -61,7 +61,10 @@ typedef enum { SBT_F32 = 0, SBT_BF16 = 1, SBT_F16 = 2 } sbt_dtype;
 /* Which copy path the host may pick.  AUTO chooses per call from alignment:
  * TMA for aligned interior tiles, 16-byte vectors where the addresses allow,
  * scalar bounds-checked elements otherwise.  The others force one path where
- * the call allows it (tests and measurements); results are identical. */
+ * the call allows it (tests and measurements); results are identical.  The
+ * clipped store into rows that are not 16-byte aligned (tiles side by side
+ * along the row) writes realigned row chunks with TMA bulk copies under AUTO
+ * and TMA, and lane-shifted 16-byte stores under VECTOR. */
 typedef enum { SBT_PATH_AUTO = 0, SBT_PATH_SCALAR = 1, SBT_PATH_VECTOR = 2, SBT_PATH_TMA = 3 } sbt_path;
 
 typedef struct sbt_context sbt_context;
