@@ -29,9 +29,7 @@ constexpr int kThreads = 256;
 //               byte span, so nothing outside the caller's buffer is read);
 //   kElem    -- element by element (column stride != 1, odd tile widths, or
 //               unaligned stores; the store's element path is one warp per
-//               tile, k_tile_store_rows).  Stores into unaligned rows whose
-//               tiles sit side by side along the row take the row-run kernels
-//               of k_tiles_runs.cu instead.
+//               tile, k_tile_store_rows).
 enum TileMode { kAligned = 0, kRealign = 1, kElem = 2 };
 
 struct TileParams {
