@@ -115,3 +115,97 @@ def test_misaligned_pointers_are_refused_before_the_device(lib, name):
             assert b"aligned" in lib.sbt_last_error_message()
     # aligned pointers pass validation and stop only at device selection (no GPU here)
     assert fn(ctx, *args) == sbt.SBT_ERR_CUDA, lib.sbt_last_error_message()
+
+
+# --------------------------------------------------------------------------- argument validation
+# Each case changes one argument of a valid call (the alignment cases above) and expects the
+# status the host returns before touching the device: SBT_OK for an empty call (nothing is
+# launched), an error code otherwise.  Same stand-in context, same CPU-only guard.
+F16 = 2
+E5M2, E2M1 = 1, 3
+
+
+def _validation_cases():
+    base = {name: args for name, (args, _) in _alignment_cases().items()}
+    ok, bad, uns, aln = sbt.SBT_OK, sbt.SBT_ERR_INVALID_ARG, sbt.SBT_ERR_UNSUPPORTED, sbt.SBT_ERR_ALIGNMENT
+    return [  # (call, {argument index: value}, expected status, what)
+        ("sbt_tile_load_padded", {0: 7}, uns, "dtype"),
+        ("sbt_tile_load_padded", {2: -1}, bad, "negative rows"),
+        ("sbt_tile_load_padded", {12: 0}, bad, "tile_r 0"),
+        ("sbt_tile_load_padded", {13: 257}, bad, "tile_c 257"),
+        ("sbt_tile_load_padded", {5: 0}, bad, "stride_c 0"),
+        ("sbt_tile_load_padded", {14: None}, bad, "dst_tiles NULL"),
+        ("sbt_tile_load_padded", {1: None}, bad, "src NULL"),
+        ("sbt_tile_load_padded", {10: 0}, ok, "empty grid"),
+        ("sbt_tile_store_clipped", {2: -1}, bad, "negative grid"),
+        ("sbt_tile_store_clipped", {4: 0}, bad, "tile_r 0"),
+        ("sbt_tile_store_clipped", {10: 0}, bad, "stride_r 0"),
+        ("sbt_tile_store_clipped", {6: None}, bad, "dst NULL"),
+        ("sbt_tile_store_clipped", {7: 0}, ok, "empty array"),
+        ("sbt_gather_rows", {4: 2}, bad, "ld_src < cols"),
+        ("sbt_gather_rows", {13: 2}, bad, "ld_out < tile_c"),
+        ("sbt_gather_rows", {5: None}, bad, "idx NULL"),
+        ("sbt_gather_rows", {9: 0}, bad, "tile_c 0"),
+        ("sbt_gather_rows", {10: X + 4096 * 9, 11: 2}, bad, "ld_mask < tile_c"),
+        ("sbt_gather_rows", {6: 0}, ok, "no indices"),
+        ("sbt_gather_cols", {11: 1}, bad, "ld_out < n_idx"),
+        ("sbt_gather_cols", {9: 0}, bad, "tile_r 0"),
+        ("sbt_gather_cols", {6: -1}, bad, "negative n_idx"),
+        ("sbt_gather_cols", {6: 0}, ok, "no indices"),
+        ("sbt_scatter_rows_masked", {4: 2}, bad, "ld_dst < cols"),
+        ("sbt_scatter_rows_masked", {10: 2}, bad, "ld_src < tile_c"),
+        ("sbt_scatter_rows_masked", {1: None}, bad, "dst NULL"),
+        ("sbt_scatter_rows_masked", {6: 0}, ok, "no indices"),
+        ("sbt_scatter_add_rows", {0: 7}, uns, "dtype"),
+        ("sbt_scatter_add_rows", {4: 2}, bad, "ld_dst < cols"),
+        ("sbt_scatter_add_rows", {11: 0}, bad, "tile_c 0"),
+        ("sbt_scatter_add_rows", {2: 0}, ok, "empty destination"),
+        ("sbt_ragged_tile_load", {3: -1}, bad, "negative heads"),
+        ("sbt_ragged_tile_load", {5: 0}, bad, "ld_row 0"),
+        ("sbt_ragged_tile_load", {7: None}, bad, "cu_seqlens NULL"),
+        ("sbt_ragged_tile_load", {8: 0}, ok, "no sequences"),
+        ("sbt_ragged_tile_store", {9: 0}, bad, "ld_row 0"),
+        ("sbt_ragged_tile_store", {7: None}, bad, "x NULL"),
+        ("sbt_ragged_tile_store", {8: 0}, ok, "empty packed array"),
+        ("sbt_gemm_bounded", {1: 2}, bad, "lda < K"),
+        ("sbt_gemm_bounded", {5: 2}, bad, "ldc < N"),
+        ("sbt_gemm_bounded", {6: F16}, uns, "c_dtype"),
+        ("sbt_gemm_bounded", {7: -1}, bad, "negative M"),
+        ("sbt_gemm_bounded", {4: None}, bad, "C NULL"),
+        ("sbt_gemm_bounded", {11: 16}, aln, "workspace too small"),
+        ("sbt_gemm_bounded", {10: X + 4096 * 16 + 16}, aln, "workspace not 256-byte aligned"),
+        ("sbt_gemm_bounded", {7: 0}, ok, "empty C"),
+        ("sbt_gemm_block_scaled", {0: E8M0}, uns, "operand format E8M0"),
+        ("sbt_gemm_block_scaled", {6: E5M2}, uns, "scale format E5M2"),
+        ("sbt_gemm_block_scaled", {11: 3}, bad, "K_s does not divide K"),
+        ("sbt_gemm_block_scaled", {0: E2M1, 2: 33}, bad, "E2M1 A with an odd lda"),
+        ("sbt_gemm_block_scaled", {8: 0}, bad, "ld_sa < K_s"),
+        ("sbt_gemm_block_scaled", {12: X + 4096 * 5, 13: 5, 15: 4}, bad, "acc aliasing D with another ld"),
+        ("sbt_gemm_block_scaled", {20: 16}, aln, "workspace too small"),
+        ("sbt_gemm_block_scaled", {16: 0}, ok, "empty D"),
+    ], base
+
+
+@pytest.mark.parametrize("i", range(len(_validation_cases()[0])))
+def test_argument_validation_before_the_device(lib, i):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("CPU-only check: a stand-in context must never reach a device")
+    cases, base = _validation_cases()
+    name, change, want, what = cases[i]
+    args = list(base[name])
+    for k, v in change.items():
+        args[k] = v
+    ctx = ctypes.create_string_buffer(4096)
+    assert getattr(lib, name)(ctx, *args) == want, (what, lib.sbt_last_error_message())
+
+
+def test_workspace_queries_validate_on_the_host(lib):
+    ctx = ctypes.create_string_buffer(4096)
+    n = ctypes.c_size_t(0)
+    assert lib.sbt_gemm_bounded_workspace_size(ctx, 8, 8, 8, 8, 8, ctypes.byref(n)) == sbt.SBT_OK
+    assert lib.sbt_gemm_bounded_workspace_size(ctx, 8, 8, 8, 4, 8, ctypes.byref(n)) == sbt.SBT_ERR_INVALID_ARG
+    assert lib.sbt_gemm_bounded_workspace_size(ctx, -1, 8, 8, 8, 8, ctypes.byref(n)) == sbt.SBT_ERR_INVALID_ARG
+    assert lib.sbt_gemm_bounded_workspace_size(None, 8, 8, 8, 8, 8, ctypes.byref(n)) == sbt.SBT_ERR_INVALID_ARG
+    assert lib.sbt_gemm_block_scaled_workspace_size(ctx, 8, 8, -8, ctypes.byref(n)) == sbt.SBT_ERR_INVALID_ARG
+    assert lib.sbt_gemm_block_scaled_workspace_size(ctx, 8, 8, 64, ctypes.byref(n)) == sbt.SBT_OK
