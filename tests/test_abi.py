@@ -209,3 +209,15 @@ def test_workspace_queries_validate_on_the_host(lib):
     assert lib.sbt_gemm_bounded_workspace_size(None, 8, 8, 8, 8, 8, ctypes.byref(n)) == sbt.SBT_ERR_INVALID_ARG
     assert lib.sbt_gemm_block_scaled_workspace_size(ctx, 8, 8, -8, ctypes.byref(n)) == sbt.SBT_ERR_INVALID_ARG
     assert lib.sbt_gemm_block_scaled_workspace_size(ctx, 8, 8, 64, ctypes.byref(n)) == sbt.SBT_OK
+
+
+def test_noalloc_refuses_a_shape_beyond_its_scratch_on_the_host(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("CPU-only check: a stand-in context must never reach a device")
+    ctx = ctypes.create_string_buffer(4096)
+    p = lambda k: X + 4096 * k
+    # odd leading dimensions at 4096^3 need staging far beyond the fixed 16 MiB array
+    st = lib.sbt_gemm_bounded_noalloc(ctx, p(0), 4097, p(1), 4097, p(2), 4097, BF16, 4096, 4096, 4096, None)
+    assert st == sbt.SBT_ERR_INVALID_ARG and b"fixed" in lib.sbt_last_error_message()
+    assert lib.sbt_gemm_bounded_noalloc(None, p(0), 8, p(1), 8, p(2), 8, BF16, 4, 4, 4, None) == sbt.SBT_ERR_INVALID_ARG
