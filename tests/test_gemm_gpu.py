@@ -1,6 +1,6 @@
 """GPU parity of sbt_gemm_bounded (tcgen05) against the fp64 CPU oracle.
 
-Gate (spec tolerance, read for a bf16 output): relative Frobenius error
+Gate (the GEMM's 1e-3 relative Frobenius tolerance, read for a bf16 output):
 ||C - bf16(ref)||_F / ||ref||_F <= 1e-3, where ref is the exact-product,
 double-accumulated oracle and bf16() its round-to-nearest-even.  An fp32
 output is compared with ref directly at the same bound.  Integer-valued
