@@ -239,3 +239,13 @@ def test_bulk_row_run_store_model_equals_element_stores(es, shape):
     for base_off in (0, es, 2 * es, 16 - es):  # destination pointer offset within 16 bytes
         got = model_store_bulk(tiles, rows, cols, ld, r0, c0, tr, es, base_off)
         assert np.array_equal(got.view(dtype).reshape(rows, ld), want), base_off
+
+
+def test_bulk_model_constants_match_the_kernel():
+    import os
+    import re
+    src = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "scatter_boundary_tile_gb300",
+                            "csrc", "k_tiles_runs.cu")).read()
+    threads = int(re.search(r"constexpr int kBulkThreads = (\d+);", src).group(1))
+    per = int(re.search(r"constexpr int kBulkPer = (\d+);", src).group(1))
+    assert (threads, per) == (BULK_THREADS, BULK_PER)
