@@ -42,6 +42,15 @@ MUTATIONS = {
     "tile_load_column_bound_dropped": (
         "if (r >= 0 && r < rows && c >= 0 && c < cols)\n                        put(dst, o, es, at(src",
         "if (r >= 0 && r < rows && c >= 0)\n                        put(dst, o, es, at(src"),
+    "tile_load_pad_written_as_zero": (
+        "                        put(dst, o, es, pad);",
+        "                        { static const unsigned char z[8] = {0}; put(dst, o, es, z); }"),
+    "tile_load_row_step_read_as_tile_height": (
+        "int64_t r = origin_r + (int64_t)ti * step_r + i;\n                    int64_t c = origin_c + (int64_t)tj * step_c + j;\n                    int64_t o = (((int64_t)ti * grid_c + tj) * tile_r + i) * tile_c + j;\n                    if (r >= 0 && r < rows && c >= 0 && c < cols)\n                        put(dst, o,",
+        "int64_t r = origin_r + (int64_t)ti * tile_r + i;\n                    int64_t c = origin_c + (int64_t)tj * step_c + j;\n                    int64_t o = (((int64_t)ti * grid_c + tj) * tile_r + i) * tile_c + j;\n                    if (r >= 0 && r < rows && c >= 0 && c < cols)\n                        put(dst, o,"),
+    "ragged_load_tail_not_zeroed": (
+        "                        put(out, o, es, zero);",
+        "                        put(out, o, es, at(x, 0, es));"),
     "tile_store_writes_one_column_past": (
         "if (r >= 0 && r < rows && c >= 0 && c < cols)\n                        put(dst, r * stride_r",
         "if (r >= 0 && r < rows && c >= 0 && c <= cols)\n                        put(dst, r * stride_r"),
