@@ -54,7 +54,26 @@ MUTATIONS = {
     "tile_store_writes_one_column_past": (
         "if (r >= 0 && r < rows && c >= 0 && c < cols)\n                        put(dst, r * stride_r",
         "if (r >= 0 && r < rows && c >= 0 && c <= cols)\n                        put(dst, r * stride_r"),
+    "tile_store_row_bound_dropped": (
+        "if (r >= 0 && r < rows && c >= 0 && c < cols)\n                        put(dst, r * stride_r",
+        "if (r >= 0 && c >= 0 && c < cols)\n                        put(dst, r * stride_r"),
+    "tile_store_row_step_read_as_tile_height": (
+        "int64_t r = origin_r + (int64_t)ti * step_r + i;\n                    int64_t c = origin_c + (int64_t)tj * step_c + j;\n                    int64_t o = (((int64_t)ti * grid_c + tj) * tile_r + i) * tile_c + j;\n                    if (r >= 0 && r < rows && c >= 0 && c < cols)\n                        put(dst, r * stride_r",
+        "int64_t r = origin_r + (int64_t)ti * tile_r + i;\n                    int64_t c = origin_c + (int64_t)tj * step_c + j;\n                    int64_t o = (((int64_t)ti * grid_c + tj) * tile_r + i) * tile_c + j;\n                    if (r >= 0 && r < rows && c >= 0 && c < cols)\n                        put(dst, r * stride_r"),
+    "gather_col_offset_ignored": (
+        "            int64_t c = col_offset + j;\n            int m = mask ? (mask[k * ld_mask + j] != 0) : 1;\n            if (m && r >= 0 && r < rows && c >= 0 && c < cols)\n                put(out",
+        "            int64_t c = j;\n            int m = mask ? (mask[k * ld_mask + j] != 0) : 1;\n            if (m && r >= 0 && r < rows && c >= 0 && c < cols)\n                put(out"),
     # masked scatter
+    "scatter_row_offset_ignored": (
+        "        int64_t r = (int64_t)idx[k] + row_offset;\n        for (int32_t j = 0; j < tile_c; ++j) {\n            int64_t c = col_offset + j;\n            int m = mask ? (mask[k * ld_mask + j] != 0) : 1;\n            if (m && r >= 0 && r < rows && c >= 0 && c < cols)\n                put(dst",
+        "        int64_t r = (int64_t)idx[k];\n        for (int32_t j = 0; j < tile_c; ++j) {\n            int64_t c = col_offset + j;\n            int m = mask ? (mask[k * ld_mask + j] != 0) : 1;\n            if (m && r >= 0 && r < rows && c >= 0 && c < cols)\n                put(dst"),
+    "scatter_add_row_offset_ignored": (
+        "        int64_t r = (int64_t)idx[k] + row_offset;\n        if (r < 0 || r >= rows) continue;",
+        "        int64_t r = (int64_t)idx[k];\n        if (r < 0 || r >= rows) continue;"),
+    "ragged_store_head_and_row_strides_swapped": (
+        "put(x, row * ld_row + (int64_t)h * ld_head + d, es,",
+        "put(x, row * ld_head + (int64_t)h * ld_row + d, es,"),
+    "block_scaled_acc_read_with_ldd": ("acc[m * ld_acc + n]", "acc[m * ldd + n]"),
     "scatter_mask_ignored": (
         "            int m = mask ? (mask[k * ld_mask + j] != 0) : 1;\n            if (m && r >= 0 && r < rows && c >= 0 && c < cols)\n                put(dst",
         "            int m = 1;\n            if (m && r >= 0 && r < rows && c >= 0 && c < cols)\n                put(dst"),

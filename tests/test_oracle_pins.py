@@ -300,6 +300,29 @@ def test_scatter_duplicates_take_a_candidate():
 
 # ----------------------------------------------------------------------------- scatter-add (gather backward)
 
+def test_scatter_with_row_and_column_offsets_equals_numpy():
+    # cuTile.jl "Memory", "Sparse views": source element (k, j) goes to row row_offset + idx[k],
+    # column col_offset + j, clipped to the array.  Written out with numpy fancy indexing on the
+    # valid (row, column) pairs; the leading dimension is wider than the array.
+    rows, cols, ld, n, tile_c, row_offset, col_offset = 60, 30, 33, 40, 31, -5, 2
+    idx = (synth.permutation_prefix(37, rows, n) + 5).astype(np.int32)  # rows idx - 5: a permutation prefix
+    idx[0], idx[1] = 2, rows + 5                                         # rows -3 and `rows`: clipped
+    dst = synth.uniform_f32(38, (rows, ld), -1.0, 1.0)
+    before = dst.copy()
+    src = synth.uniform_f32(39, (n, tile_c), 5.0, 6.0)
+    mask = synth.bernoulli_u8(40, (n, tile_c), 0.8)
+    oracle.scatter_rows_masked(dst, rows, cols, ld, idx, src, tile_c, tile_c, row_offset=row_offset,
+                               col_offset=col_offset, mask=mask)
+    want = before.copy()
+    r = idx.astype(np.int64) + row_offset
+    c = col_offset + np.arange(tile_c)
+    keep_r, keep_c = (r >= 0) & (r < rows), (c >= 0) & (c < cols)
+    rr, cc = r[keep_r][:, None], c[keep_c][None, :]
+    m = mask[keep_r][:, keep_c] != 0
+    want[rr, cc] = np.where(m, src[keep_r][:, keep_c], before[rr, cc])
+    np.testing.assert_array_equal(dst, want)
+
+
 def test_scatter_add_unique_fp32_equals_numpy_rounding():
     rows, cols, n = 300, 40, 120
     dst = synth.uniform_f32(61, (rows, cols), -1.0, 1.0)
@@ -351,6 +374,23 @@ def test_scatter_add_fp16_subnormals_equal_torch():
     tb = torch.from_numpy(b_bits.view(np.int16)).view(torch.float16)
     want = (ta.float() + tb.float()).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
     np.testing.assert_array_equal(dst.reshape(8), want)
+
+
+def test_scatter_add_with_row_and_column_offsets_equals_numpy_add_at():
+    # The gather's backward with both offsets: source element (k, j) adds into row row_offset + idx[k],
+    # column col_offset + j when that is inside the array.  Integer values keep every sum exact.
+    rows, cols, ld, n, tile_c, row_offset, col_offset = 12, 10, 13, 300, 9, -2, 3
+    dst = synth.int_below(70, rows * ld, 9, lo=-4).astype(np.float32).reshape(rows, ld)
+    idx = synth.int_below(71, n, rows + 4, lo=0).astype(np.int32)  # rows -2 .. rows + 1: some clipped
+    src = synth.int_below(72, n * tile_c, 7, lo=-3).astype(np.float32).reshape(n, tile_c)
+    want = dst.astype(np.int64)
+    r = idx.astype(np.int64) + row_offset
+    c = col_offset + np.arange(tile_c)
+    keep_r, keep_c = (r >= 0) & (r < rows), (c >= 0) & (c < cols)
+    np.add.at(want, (r[keep_r][:, None], c[keep_c][None, :]), src[keep_r][:, keep_c].astype(np.int64))
+    oracle.scatter_add_rows(dst, rows, cols, ld, idx, src, tile_c, tile_c, row_offset=row_offset,
+                            col_offset=col_offset)
+    np.testing.assert_array_equal(dst, want.astype(np.float32))
 
 
 def test_scatter_add_clips_rows_and_columns():
@@ -626,6 +666,18 @@ def test_block_scaled_closed_form_with_acc():
     C = oracle.gemm_block_scaled_f64(A, K, SA, 3, B, N, SB, N, M, N, K, bs, acc=acc, ld_acc=N)
     want = np.array([[bs * 2.0 ** (m % 3) * 4 for n in range(N)] for m in range(M)]) + acc
     np.testing.assert_array_equal(C, want)
+
+
+def test_block_scaled_acc_with_its_own_leading_dimension():
+    # acc is an (M, N) view with its own leading dimension: D = closed form + acc[:, :N]
+    M, N, K, bs, ld_acc = 5, 4, 64, 32, 7
+    A = np.full((M, K), 0x38, np.uint8)
+    B = np.full((K, N), 0x38, np.uint8)
+    SA = np.full((M, 2), 127, np.uint8)
+    SB = np.full((2, N), 128, np.uint8)   # 2.0
+    acc = synth.uniform_f32(73, (M, ld_acc), -4.0, 4.0)
+    C = oracle.gemm_block_scaled_f64(A, K, SA, 2, B, N, SB, N, M, N, K, bs, acc=acc, ld_acc=ld_acc)
+    np.testing.assert_array_equal(C, 2.0 * K + acc[:, :N].astype(np.float64))
 
 
 def test_block_scaled_nan_stays_in_its_row_and_column():
