@@ -74,6 +74,21 @@ MUTATIONS = {
         "put(x, row * ld_row + (int64_t)h * ld_head + d, es,",
         "put(x, row * ld_head + (int64_t)h * ld_row + d, es,"),
     "block_scaled_acc_read_with_ldd": ("acc[m * ld_acc + n]", "acc[m * ldd + n]"),
+    "bf16_rounded_to_nine_bits": (
+        "int q_exp = e - 8 > -133 ? e - 8 : -133;",
+        "int q_exp = e - 9 > -133 ? e - 9 : -133;"),
+    "f16_overflow_tested_before_rounding": (
+        "if (y >= 65520.0 || isinf(a)) return sign | 0x7C00;",
+        "if (a > 65504.0 || isinf(a)) return sign | 0x7C00;"),
+    "ragged_store_packed_bound_dropped": (
+        "if (r < len && row >= 0 && row < total_rows)\n                        put(x,",
+        "if (r < len && row >= 0)\n                        put(x,"),
+    "gather_cols_row_bound_dropped": (
+        "if (r >= 0 && r < rows && c >= 0 && c < cols)\n                put(out, i * ld_out + k",
+        "if (r >= 0 && c >= 0 && c < cols)\n                put(out, i * ld_out + k"),
+    "scatter_column_bound_dropped": (
+        "if (m && r >= 0 && r < rows && c >= 0 && c < cols)\n                put(dst",
+        "if (m && r >= 0 && r < rows && c >= 0)\n                put(dst"),
     "scatter_mask_ignored": (
         "            int m = mask ? (mask[k * ld_mask + j] != 0) : 1;\n            if (m && r >= 0 && r < rows && c >= 0 && c < cols)\n                put(dst",
         "            int m = 1;\n            if (m && r >= 0 && r < rows && c >= 0 && c < cols)\n                put(dst"),
@@ -181,7 +196,9 @@ MUTATIONS = {
 # Not in the list because no input can tell them from the oracle (equivalent mutants): rounding a
 # scatter-add sum through binary32 before bf16 (binary32 carries more than 2p + 2 bits for p = 8, so
 # the double rounding is innocuous), and dropping the subnormal clamp of the fp16 rounding (a sum of
-# two binary16 values that lands below 2^-14 is a multiple of 2^-24 and needs no rounding).
+# two binary16 values that lands below 2^-14 is a multiple of 2^-24 and needs no rounding), and testing the
+# rounded fp16 sum for overflow with `> 65504` instead of `>= 65520` (the rounded value is on the fp16 grid,
+# where the next value after 65504 is 65536, so the two tests agree).
 
 IGNORE = shutil.ignore_patterns("__pycache__", "*.tmp*")
 

@@ -376,6 +376,20 @@ def test_scatter_add_fp16_subnormals_equal_torch():
     np.testing.assert_array_equal(dst.reshape(8), want)
 
 
+def test_scatter_add_fp16_overflow_threshold_equals_torch():
+    # binary16 sums next to the overflow threshold 65520 (the largest finite 65504 plus half an ulp):
+    # below it they round to 65504, at and above it to infinity; torch adds in fp32 and rounds once
+    a_bits = np.array([0x7BFF, 0x7BFF, 0x7BFF, 0x7BFF, 0xFBFF, 0xFBFF, 0x7BFE, 0x7BFF], np.uint16)
+    b_bits = np.array([0x4800, 0x4B80, 0x4C00, 0x4C80, 0xC800, 0xCC00, 0x4C00, 0x0000], np.uint16)
+    dst = a_bits.reshape(1, 8).copy()
+    oracle.scatter_add_rows(dst, 1, 8, 8, np.array([0], np.int32), b_bits.reshape(1, 8), 8, 8, kind="f16")
+    ta = torch.from_numpy(a_bits.view(np.int16)).view(torch.float16)
+    tb = torch.from_numpy(b_bits.view(np.int16)).view(torch.float16)
+    want = (ta.float() + tb.float()).to(torch.float16).view(torch.int16).numpy().view(np.uint16)
+    assert (want == 0x7C00).any() and (want == 0x7BFF).any()  # both sides of the threshold occur
+    np.testing.assert_array_equal(dst.reshape(8), want)
+
+
 def test_scatter_add_with_row_and_column_offsets_equals_numpy_add_at():
     # The gather's backward with both offsets: source element (k, j) adds into row row_offset + idx[k],
     # column col_offset + j when that is inside the array.  Integer values keep every sum exact.
@@ -492,6 +506,18 @@ def test_ragged_store_leaves_rows_outside_every_sequence():
     np.testing.assert_array_equal(x[0:3], tiles[0, :, :3].transpose(1, 0, 2))
     np.testing.assert_array_equal(x[3:8], tiles[2, :, :5].transpose(1, 0, 2))
     assert np.all(x[8:12] == 0x1234)
+
+
+def test_ragged_store_stops_at_the_packed_array_end():
+    # A sequence whose rows run past total_rows: the packed array is the first 10 rows of a 14-row
+    # buffer, and the rows after it must keep their bits (a store never writes outside the array).
+    cu = np.array([0, 6, 13], np.int32)  # sequence 1 claims packed rows 6..12
+    tiles = synth.normal_bf16(46, (2, 2, 8, 4))
+    buf = np.full((14, 2, 4), 0x1234, np.uint16)
+    oracle.ragged_tile_store(tiles, buf[:10], 10, 8, 4, cu)
+    np.testing.assert_array_equal(buf[0:6], tiles[0, :, :6].transpose(1, 0, 2))
+    np.testing.assert_array_equal(buf[6:10], tiles[1, :, :4].transpose(1, 0, 2))
+    assert np.all(buf[10:] == 0x1234)
 
 
 # ----------------------------------------------------------------------------- GEMM and bf16 rounding
