@@ -80,6 +80,21 @@ MUTATIONS = {
     "f16_overflow_tested_before_rounding": (
         "if (y >= 65520.0 || isinf(a)) return sign | 0x7C00;",
         "if (a > 65504.0 || isinf(a)) return sign | 0x7C00;"),
+    "gather_output_leading_dimension_ignored": (
+        "put(out, k * ld_out + j, es, at(src, r * ld_src + c, es));",
+        "put(out, k * tile_c + j, es, at(src, r * ld_src + c, es));"),
+    "gather_mask_leading_dimension_ignored": (
+        "            int m = mask ? (mask[k * ld_mask + j] != 0) : 1;\n            if (m && r >= 0 && r < rows && c >= 0 && c < cols)\n                put(out",
+        "            int m = mask ? (mask[k * tile_c + j] != 0) : 1;\n            if (m && r >= 0 && r < rows && c >= 0 && c < cols)\n                put(out"),
+    "scatter_mask_leading_dimension_ignored": (
+        "            int m = mask ? (mask[k * ld_mask + j] != 0) : 1;\n            if (m && r >= 0 && r < rows && c >= 0 && c < cols)\n                put(dst",
+        "            int m = mask ? (mask[k * tile_c + j] != 0) : 1;\n            if (m && r >= 0 && r < rows && c >= 0 && c < cols)\n                put(dst"),
+    "scatter_source_leading_dimension_ignored": (
+        "put(dst, r * ld_dst + c, es, at(src, k * ld_src + j, es));",
+        "put(dst, r * ld_dst + c, es, at(src, k * tile_c + j, es));"),
+    "scatter_add_source_leading_dimension_ignored": (
+        "const char* s = (const char*)src + (k * ld_src + j) * es;",
+        "const char* s = (const char*)src + (k * tile_c + j) * es;"),
     "ragged_store_packed_bound_dropped": (
         "if (r < len && row >= 0 && row < total_rows)\n                        put(x,",
         "if (r < len && row >= 0)\n                        put(x,"),

@@ -117,6 +117,26 @@ def test_gather_general_equals_numpy_pad_and_clip():
         np.testing.assert_array_equal(out, want)
 
 
+def test_gather_with_its_own_output_and_mask_leading_dimensions():
+    # warp.tile_load_indexed with a per-element mask (cuTile.jl "Memory"): out[k*ld_out + j] and
+    # mask[k*ld_mask + j] for j < tile_c, every leading dimension wider than the tile; the mask's extra
+    # columns are all ones, so reading them for the real ones would show.
+    rows, cols, ld, n, tile_c, ld_out, ld_mask = 30, 24, 29, 50, 20, 27, 23
+    a = synth.uniform_f32(18, (rows, ld), -1.0, 1.0)
+    idx = synth.int_below(19, n, rows + 6, lo=-3).astype(np.int32)
+    mask = np.ones((n, ld_mask), np.uint8)
+    mask[:, :tile_c] = synth.bernoulli_u8(20, (n, tile_c), 0.5)
+    pad = np.float32(9.0)
+    out = oracle.gather_rows(a, rows, cols, ld, idx, tile_c=tile_c, col_offset=2, mask=mask, ld_mask=ld_mask,
+                             pad=pad, ld_out=ld_out)
+    big = padded_reference(a[:, :cols], pad, 1)
+    r = np.clip(idx.astype(np.int64), -1, rows) + 1
+    c = np.clip(np.arange(tile_c) + 2, -1, cols) + 1
+    want = np.where(mask[:, :tile_c] != 0, big[r][:, c], pad)
+    np.testing.assert_array_equal(out[:, :tile_c], want)
+    assert not out[:, tile_c:].any()  # columns past the tile are never written
+
+
 def test_gather_cols_equals_numpy_fancy_indexing_and_pad_clip():
     rows, cols, ld = 30, 50, 53
     a = synth.uniform_f32(71, (rows, ld), -1.0, 1.0)
@@ -321,6 +341,35 @@ def test_scatter_with_row_and_column_offsets_equals_numpy():
     m = mask[keep_r][:, keep_c] != 0
     want[rr, cc] = np.where(m, src[keep_r][:, keep_c], before[rr, cc])
     np.testing.assert_array_equal(dst, want)
+
+
+def test_scatter_with_its_own_source_and_mask_leading_dimensions():
+    # src[k*ld_src + j] and mask[k*ld_mask + j] for j < tile_c, both wider than the tile; their extra
+    # columns hold values (and all-one mask bytes) that a wrong leading dimension would pick up.
+    rows, cols, n, tile_c, ld_src, ld_mask = 80, 16, 30, 16, 21, 19
+    dst = synth.uniform_f32(41, (rows, cols), -1.0, 1.0)
+    before = dst.copy()
+    idx = synth.permutation_prefix(42, rows, n)
+    src = np.full((n, ld_src), 100.0, np.float32)
+    src[:, :tile_c] = synth.uniform_f32(43, (n, tile_c), 5.0, 6.0)
+    mask = np.ones((n, ld_mask), np.uint8)
+    mask[:, :tile_c] = synth.bernoulli_u8(44, (n, tile_c), 0.5)
+    oracle.scatter_rows_masked(dst, rows, cols, cols, idx, src, ld_src, tile_c, mask=mask, ld_mask=ld_mask)
+    want = before.copy()
+    want[idx] = np.where(mask[:, :tile_c] != 0, src[:, :tile_c], before[idx])
+    np.testing.assert_array_equal(dst, want)
+
+
+def test_scatter_add_with_its_own_source_leading_dimension():
+    rows, cols, n, tile_c, ld_src = 20, 8, 60, 8, 11
+    dst = synth.int_below(74, rows * cols, 9, lo=-4).astype(np.float32).reshape(rows, cols)
+    idx = synth.int_below(75, n, rows).astype(np.int32)
+    src = np.full((n, ld_src), 1000.0, np.float32)
+    src[:, :tile_c] = synth.int_below(76, n * tile_c, 7, lo=-3).astype(np.float32).reshape(n, tile_c)
+    want = dst.astype(np.int64)
+    np.add.at(want, idx, src[:, :tile_c].astype(np.int64))
+    oracle.scatter_add_rows(dst, rows, cols, cols, idx, src, ld_src, tile_c)
+    np.testing.assert_array_equal(dst, want.astype(np.float32))
 
 
 def test_scatter_add_unique_fp32_equals_numpy_rounding():
