@@ -95,6 +95,21 @@ MUTATIONS = {
     "scatter_add_source_leading_dimension_ignored": (
         "const char* s = (const char*)src + (k * ld_src + j) * es;",
         "const char* s = (const char*)src + (k * tile_c + j) * es;"),
+    "gather_cols_output_leading_dimension_ignored": (
+        "put(out, i * ld_out + k, es, at(src, r * ld_src + c, es));",
+        "put(out, i * n_idx + k, es, at(src, r * ld_src + c, es));"),
+    "ragged_load_row_stride_read_as_dense": (
+        "put(out, o, es, at(x, row * ld_row + (int64_t)h * ld_head + d, es));",
+        "put(out, o, es, at(x, row * (int64_t)heads * depth + (int64_t)h * ld_head + d, es));"),
+    "ragged_store_row_stride_read_as_dense": (
+        "put(x, row * ld_row + (int64_t)h * ld_head + d, es,",
+        "put(x, row * (int64_t)heads * depth + (int64_t)h * ld_head + d, es,"),
+    "tile_load_row_stride_read_as_cols": (
+        "put(dst, o, es, at(src, r * stride_r + c * stride_c, es));",
+        "put(dst, o, es, at(src, r * cols + c * stride_c, es));"),
+    "tile_store_row_stride_read_as_cols": (
+        "put(dst, r * stride_r + c * stride_c, es, at(src_tiles, o, es));",
+        "put(dst, r * cols + c * stride_c, es, at(src_tiles, o, es));"),
     "ragged_store_packed_bound_dropped": (
         "if (r < len && row >= 0 && row < total_rows)\n                        put(x,",
         "if (r < len && row >= 0)\n                        put(x,"),

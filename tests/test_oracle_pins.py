@@ -154,6 +154,18 @@ def test_gather_cols_equals_numpy_fancy_indexing_and_pad_clip():
     np.testing.assert_array_equal(out, big[r][:, c])
 
 
+def test_gather_cols_with_its_own_output_leading_dimension():
+    rows, cols, n, tile_r, ld_out = 14, 20, 9, 12, 13
+    a = synth.uniform_f32(74, (rows, cols), -1.0, 1.0)
+    idx = synth.int_below(75, n, cols + 4, lo=-2).astype(np.int32)
+    out = oracle.gather_cols(a, rows, cols, cols, idx, tile_r=tile_r, row_offset=1, pad=4.0, ld_out=ld_out)
+    big = padded_reference(a, np.float32(4.0), 1)
+    r = np.clip(np.arange(tile_r) + 1, -1, rows) + 1
+    c = np.clip(idx.astype(np.int64), -1, cols) + 1
+    np.testing.assert_array_equal(out[:, :n], big[r][:, c])
+    assert not out[:, n:].any()
+
+
 def test_gather_cols_is_row_gather_of_the_transpose():
     a = synth.uniform_f32(73, (12, 9), -1.0, 1.0)
     idx = np.array([8, -1, 3, 3, 9, 0], np.int32)
@@ -555,6 +567,32 @@ def test_ragged_store_leaves_rows_outside_every_sequence():
     np.testing.assert_array_equal(x[0:3], tiles[0, :, :3].transpose(1, 0, 2))
     np.testing.assert_array_equal(x[3:8], tiles[2, :, :5].transpose(1, 0, 2))
     assert np.all(x[8:12] == 0x1234)
+
+
+def test_ragged_load_and_store_with_padded_packed_rows():
+    # Mojo "RaggedTMA3DTile": the packed array is addressed through its own strides: element (row, h, d)
+    # at row*ld_row + h*ld_head + d.  Here heads are 3 apart beyond their depth and rows 5 beyond their
+    # heads, so a stride read as the dense one lands elsewhere; expected positions come from numpy index
+    # arithmetic on the flat buffer.
+    heads, depth, ld_head = 3, 4, 7
+    ld_row = heads * ld_head + 5
+    cu = np.array([0, 5, 5, 11], np.int32)
+    total, t_pad, batch = 11, 8, 3
+    flat = synth.normal_bf16(47, total * ld_row)
+    out = oracle.ragged_tile_load(flat, total, heads, depth, ld_row, ld_head, cu, t_pad)
+    lens = np.diff(cu)
+    b, h, r, d = np.meshgrid(np.arange(batch), np.arange(heads), np.arange(t_pad), np.arange(depth), indexing="ij")
+    valid = r < lens[b]
+    pos = (cu[b] + r) * ld_row + h * ld_head + d
+    want = np.where(valid, flat[np.where(valid, pos, 0)], 0).astype(np.uint16)
+    np.testing.assert_array_equal(out, want)
+    # the store writes exactly those positions back, from other tiles, and nothing else of the buffer
+    tiles = synth.normal_bf16(48, (batch, heads, t_pad, depth))
+    canvas = np.full(total * ld_row, 0xBEEF, np.uint16)
+    oracle.ragged_tile_store(tiles, canvas, total, ld_row, ld_head, cu)
+    want_c = np.full(total * ld_row, 0xBEEF, np.uint16)
+    want_c[pos[valid]] = tiles[valid]
+    np.testing.assert_array_equal(canvas, want_c)
 
 
 def test_ragged_store_stops_at_the_packed_array_end():
