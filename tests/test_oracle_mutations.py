@@ -110,6 +110,15 @@ MUTATIONS = {
     "tile_store_row_stride_read_as_cols": (
         "put(dst, r * stride_r + c * stride_c, es, at(src_tiles, o, es));",
         "put(dst, r * cols + c * stride_c, es, at(src_tiles, o, es));"),
+    "ragged_load_output_head_major": (
+        "int64_t o = (((int64_t)b * heads + h) * t_pad + r) * depth + d;",
+        "int64_t o = (((int64_t)h * batch + b) * t_pad + r) * depth + d;"),
+    "tile_load_output_tile_column_major": (
+        "int64_t o = (((int64_t)ti * grid_c + tj) * tile_r + i) * tile_c + j;\n                    if (r >= 0 && r < rows && c >= 0 && c < cols)\n                        put(dst, o, es, at(src",
+        "int64_t o = (((int64_t)tj * grid_r + ti) * tile_r + i) * tile_c + j;\n                    if (r >= 0 && r < rows && c >= 0 && c < cols)\n                        put(dst, o, es, at(src"),
+    "tile_store_input_tile_column_major": (
+        "int64_t o = (((int64_t)ti * grid_c + tj) * tile_r + i) * tile_c + j;\n                    if (r >= 0 && r < rows && c >= 0 && c < cols)\n                        put(dst, r * stride_r",
+        "int64_t o = (((int64_t)tj * grid_r + ti) * tile_r + i) * tile_c + j;\n                    if (r >= 0 && r < rows && c >= 0 && c < cols)\n                        put(dst, r * stride_r"),
     "ragged_store_packed_bound_dropped": (
         "if (r < len && row >= 0 && row < total_rows)\n                        put(x,",
         "if (r < len && row >= 0)\n                        put(x,"),
